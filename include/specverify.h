@@ -1,0 +1,146 @@
+/*
+ * specverify.h -- C ABI of the batched speculative-decoding verification
+ * library (libspecverify.so, CUDA kernels for sm_103a).
+ *
+ * The operation (one verification round per sequence) is the rule stated in
+ *   - nextadmin.net lesson "Speculative Decoding (دیکودینگ گمانه‌زن)",
+ *     § Core algorithm, steps 4-6, and § Step 1 (accept/reject), § Step 2
+ *     (residual distribution), § Step 3 (one speculative step);
+ *   - aiengineeringfromscratch.com Phase 10 lesson 25 "Speculative Decoding",
+ *     § The exact rule and § Greedy case;
+ *   - runelab.ai "Küçük bir model büyük olanı nasıl hızlandırır?", § the
+ *     exact rule (points 1-3 and the bonus token);
+ *   - for the shortlisted draft, the DynaSpec summary (lowest.today, "DynaSpec:
+ *     Context-aware Dynamic Speculative Sampling for Large-Vocabulary Language
+ *     Models"), § Abstract and § Method 3: the drafter works on a
+ *     per-context shortlist, verification keeps the full vocabulary.
+ * Notation: q = target distribution, p = draft distribution, d_i = drafted
+ * tokens (i = 1..K), V = vocabulary size, T = temperature.
+ *
+ * For each sequence b, with q_i = softmax(target[b][i-1] / T) and
+ * p_i = softmax(draft[b][i-1] / T) (or the given draft probabilities):
+ *   for i = 1..K, left to right, accept d_i iff u_i < min(1, q_i(d_i)/p_i(d_i))
+ *   (always when p_i(d_i) == 0); at the first rejection j emit a token drawn
+ *   from (q_j - p_j)_+ / R_j (R_j its total; q_j itself when R_j == 0) and stop;
+ *   if all K are accepted emit a bonus token drawn from q_{K+1}.
+ *   T == 0 is greedy: accept d_i while d_i == argmax q_i (lowest index on
+ *   ties), then emit argmax q_j at the first mismatch (argmax q_{K+1} if none).
+ * Uniforms: Philox4x32-10 (Salmon et al., SC'11) with counter
+ *   (position i-1, sequence b, 0, 0) and key (seed & 0xffffffff, seed >> 32);
+ *   word 0 gives u_i, word 1 gives the sampling uniform v; a word w maps to
+ *   ((w >> 8) + 0.5) * 2^-24.  Sampling is inverse-CDF in ascending token
+ *   order: the smallest x with sum_{y<=x} r(y) > v * R.
+ *
+ * Conventions for every entry point:
+ *   - All array pointers are DEVICE pointers owned by the caller; rows are
+ *     contiguous and row-major.  Rows whose start is 16-byte aligned (row
+ *     length times element size a multiple of 16 and a 16-byte aligned base)
+ *     take the bulk-copy path; other shapes are correct but slower.
+ *   - `workspace` is caller-owned device scratch of at least
+ *     spec_workspace_bytes(B, K, V, S) bytes.  It must be zero-filled before
+ *     its first use; every call that returns SPEC_OK leaves it zero-filled
+ *     again when its kernel finishes.  One workspace per call in flight: two
+ *     calls that overlap on the GPU must not share one.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream).  Argument errors are returned synchronously, before
+ *     anything is launched.  Data errors are found on the device, in the rows
+ *     the left-to-right rule examines: that sequence gets out_accept_len[b] =
+ *     -code and out_tokens[b][*] = -1, and aux->device_status (if given)
+ *     receives the code of one failing sequence after the kernel ends.  The
+ *     device never traps.
+ *   - out_tokens[b] holds the accepted draft tokens followed by one target
+ *     token; out_accept_len[b] is the number of accepted draft tokens (0..K),
+ *     so out_accept_len[b] + 1 tokens are emitted; unused slots are -1.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1,  /* bad size, pointer, dtype, temperature or workspace size */
+    SPEC_ERR_NONFINITE = 2,    /* NaN / +inf logit, all -inf row, or bad draft probability */
+    SPEC_ERR_TOKEN_RANGE = 3,  /* a drafted token outside [0, V) */
+    SPEC_ERR_SHORTLIST = 4,    /* shortlist not ascending and unique inside [0, V) */
+    SPEC_ERR_UNSUPPORTED = 5,  /* no usable sm_103a device for this build */
+    SPEC_ERR_CUDA = 6,         /* a CUDA runtime call or launch failed */
+    SPEC_ERR_TIMEOUT = 7       /* a bounded on-device wait ran out (the kernel gave up) */
+} spec_status_t;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
+
+/* Optional per-call outputs.  Any NULL member is not written.  Asking for
+ * q_draft, p_draft or row_lse makes the call evaluate every position (it then
+ * reads every row), not only the positions up to the first rejection.
+ * All pointers are device pointers.                                          */
+typedef struct {
+    float *q_draft;          /* [B][K]     q_i(d_i); NaN where row or token is invalid   */
+    float *p_draft;          /* [B][K]     p_i(d_i); NaN where row or token is invalid   */
+    float *residual_mass;    /* [B]        total R of the distribution the last token was
+                                           drawn from (residual, or q_{K+1} for a bonus) */
+    float *row_lse;          /* [B][2K+1]  log sum exp(z / T): target rows 0..K, then draft
+                                           rows 0..K-1 (NaN for draft probabilities)      */
+    int32_t *device_status;  /* [1]        0, or the code of one failing sequence         */
+} spec_aux_t;
+
+/* Bytes of device workspace a call with these sizes needs (S = 0 without a
+ * shortlist).  Returns 0 for sizes the library rejects.                      */
+size_t spec_workspace_bytes(int B, int K, int V, int S);
+
+/* Stochastic verification; T == 0 runs the greedy rule.
+ *   target_logits  [B][K+1][V]  dtype `tdt`
+ *   draft          [B][K][V]    logits of dtype `tdt`, or float32 probabilities
+ *                               when draft_is_probs != 0 (ddt must then be SPEC_F32)
+ *   draft_tokens   [B][K]       int32
+ *   out_tokens     [B][K+1]     int32;  out_accept_len [B] int32
+ * Limits: B >= 1, 1 <= K <= 31, V >= 1, T finite and >= 0.                     */
+spec_status_t spec_verify(const void *target_logits, spec_dtype_t tdt,
+                          const void *draft, spec_dtype_t ddt, int draft_is_probs,
+                          const int32_t *draft_tokens,
+                          int B, int K, int V, float T, uint64_t seed,
+                          int32_t *out_tokens, int32_t *out_accept_len,
+                          void *workspace, size_t workspace_bytes,
+                          const spec_aux_t *aux, void *stream);
+
+/* Greedy verification ([SD-EN] § Greedy case): only the target logits are read. */
+spec_status_t spec_verify_greedy(const void *target_logits, spec_dtype_t tdt,
+                                 const int32_t *draft_tokens, int B, int K, int V,
+                                 int32_t *out_tokens, int32_t *out_accept_len,
+                                 void *workspace, size_t workspace_bytes,
+                                 const spec_aux_t *aux, void *stream);
+
+/* Verification with a draft defined on a per-sequence shortlist (DynaSpec):
+ *   draft_sl       [B][K][S]  logits (dtype `tdt`) or float32 probabilities over
+ *                             the shortlisted tokens; p is 0 off the shortlist
+ *   shortlist_idx  [B][S]     int32, strictly ascending, each in [0, V)
+ * The target distribution and the residual stay over the full vocabulary.
+ * A drafted token outside its shortlist has p_i(d_i) = 0 and is accepted.    */
+spec_status_t spec_verify_shortlist(const void *target_logits, spec_dtype_t tdt,
+                                    const void *draft_sl, spec_dtype_t ddt, int draft_is_probs,
+                                    const int32_t *shortlist_idx, int S,
+                                    const int32_t *draft_tokens,
+                                    int B, int K, int V, float T, uint64_t seed,
+                                    int32_t *out_tokens, int32_t *out_accept_len,
+                                    void *workspace, size_t workspace_bytes,
+                                    const spec_aux_t *aux, void *stream);
+
+/* Philox4x32-10 words as the verification kernels draw them, for checking:
+ * out[(b * P + pos) * 4 + w] = word w of Philox(counter (pos, b, tag, 0),
+ * key (seed low, seed high)) for b < B, pos < P.  `out` is a device pointer of
+ * B * P * 4 uint32 entries.                                                   */
+spec_status_t spec_philox_words(uint64_t seed, uint32_t tag, int B, int P, uint32_t *out,
+                                void *stream);
+
+/* A static description of a status code. */
+const char *spec_status_string(spec_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPECVERIFY_H */

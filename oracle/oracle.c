@@ -49,8 +49,11 @@
  *     [0, V), a shortlist that is not ascending and unique inside [0, V),
  *     negative or non-finite draft probabilities) are checked at the positions
  *     the left-to-right rule examines, in the order: shortlist (position 0),
- *     token, target row, draft row.  A sequence with an error gets
- *     accept_len = -code and every token -1.
+ *     token, target row, draft row.  Logit rows are checked whole (their
+ *     softmax needs every entry); given draft probabilities are checked where
+ *     the rule reads them: p_i(d_i) at each examined position, and the whole
+ *     row p_j at a rejection, whose residual uses it.  A sequence with an
+ *     error gets accept_len = -code and every token -1.
  */
 #include <math.h>
 #include <pthread.h>
@@ -263,12 +266,8 @@ static int draft_dist(const struct job *J, int b, int i, struct scratch *w, doub
     if (lse)
         *lse = NAN;
     if (J->draft_is_probs) {
-        for (int x = 0; x < n; ++x) {
-            double v = elem(J->draft, OR_F32, off + x);
-            if (!(v >= 0.0) || v == INFINITY)
-                return OR_ERR_NONFINITE;
-            w->r[x] = v;
-        }
+        for (int x = 0; x < n; ++x)
+            w->r[x] = elem(J->draft, OR_F32, off + x);
     } else {
         for (int x = 0; x < n; ++x)
             w->z[x] = elem(J->draft, J->ddt, off + x);
@@ -286,6 +285,23 @@ static int draft_dist(const struct job *J, int b, int i, struct scratch *w, doub
             w->p[idx[s]] = w->r[s];
     }
     return OR_OK;
+}
+
+/* A given draft probability is usable when it is finite and >= 0. */
+static int prob_ok(double v)
+{
+    return v >= 0.0 && v != INFINITY;
+}
+
+/* Every entry of draft probability row (b, i) usable. */
+static int prob_row_ok(const struct job *J, int b, int i)
+{
+    int n = J->shortlist ? J->S : J->V;
+    size_t off = ((size_t)b * J->K + i) * (size_t)n;
+    for (int x = 0; x < n; ++x)
+        if (!prob_ok(elem(J->draft, OR_F32, off + x)))
+            return 0;
+    return 1;
 }
 
 static int shortlist_ok(const struct job *J, int b)
@@ -340,7 +356,8 @@ static void verify_stochastic(const struct job *J, int b, struct scratch *w)
             emit_error(J, b, OR_ERR_TOKEN_RANGE);
             return;
         }
-        if (target_dist(J, b, i, w, NULL) || draft_dist(J, b, i, w, NULL)) {
+        if (target_dist(J, b, i, w, NULL) || draft_dist(J, b, i, w, NULL)
+            || (J->draft_is_probs && !prob_ok(w->p[d]))) {
             emit_error(J, b, OR_ERR_NONFINITE);
             return;
         }
@@ -353,6 +370,10 @@ static void verify_stochastic(const struct job *J, int b, struct scratch *w)
             continue;
         }
         /* First rejection at position i: residual sample, then stop. */
+        if (J->draft_is_probs && !prob_row_ok(J, b, i)) {
+            emit_error(J, b, OR_ERR_NONFINITE);
+            return;
+        }
         double R = oracle_residual(w->q, w->p, V, w->r);
         double v = verify_uniform(J->seed, b, i, 1);
         double margin;
@@ -411,7 +432,7 @@ static void all_positions(const struct job *J, int b, struct scratch *w)
         if (J->row_lse)
             J->row_lse[(size_t)b * (2 * K + 1) + K + 1 + i] = bad_d ? NAN : lse_d;
         int d = J->tokens[(size_t)b * K + i];
-        int ok = !bad_t && !bad_d && d >= 0 && d < J->V;
+        int ok = !bad_t && !bad_d && d >= 0 && d < J->V && (!J->draft_is_probs || prob_ok(w->p[d]));
         if (J->q_draft)
             J->q_draft[(size_t)b * K + i] = ok ? w->q[d] : NAN;
         if (J->p_draft)

@@ -441,3 +441,25 @@ def test_shortlist_equals_full_vocab_with_minus_inf():
     bad[0, 3] = bad[0, 2]
     c = oracle.verify(zt, comp, d, 1.0, seed=8, shortlist=bad)
     assert c["accept_len"][0] == -4
+
+
+def test_draft_probability_errors_only_where_read():
+    """Given draft probabilities are used at p_i(d_i) for the accept test and
+    as a whole row only at a rejection: a bad entry elsewhere in an accepted
+    position's row is never read."""
+    B, K, V = 3, 2, 8
+    q = np.full(V, 1.0 / V)
+    p = np.full(V, 1.0 / V)
+    tgt, drf = _batch([q, q, q], [p, p], np.zeros((B, K), dtype=np.int32))
+    drf = drf.clone()
+    d = torch.zeros((B, K), dtype=torch.int32)
+    drf[0, 0, 5] = -0.25     # p == q elsewhere: position 1 accepted, entry 5 never read
+    drf[1, 0, 0] = math.nan  # the drafted token's own probability: read at position 1
+    drf[2, 0, 0] = 0.25      # q/p = 0.5: some seeds reject, then the row is read
+    drf[2, 0, 3] = math.inf
+    out = oracle.verify(tgt, drf, d, 1.0, seed=2, draft_is_probs=True)
+    assert out["accept_len"][0] == K
+    assert out["accept_len"][1] == -2
+    outs = [oracle.verify(tgt, drf, d, 1.0, seed=s, draft_is_probs=True)["accept_len"][2]
+            for s in range(40)]
+    assert -2 in outs and all(x in (-2, 1, 2) for x in outs)
