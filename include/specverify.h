@@ -38,9 +38,11 @@
  *     take the bulk-copy path; other shapes are correct but slower.
  *   - `workspace` is caller-owned device scratch of at least
  *     spec_workspace_bytes(B, K, V, S) bytes.  It must be zero-filled before
- *     its first use; every call that returns SPEC_OK leaves it zero-filled
- *     again when its kernel finishes.  One workspace per call in flight: two
- *     calls that overlap on the GPU must not share one.
+ *     its first use with given sizes (B, K, V, S); a call that returns SPEC_OK
+ *     leaves it ready for the next call with the same sizes.  Before reusing it
+ *     with other sizes, zero-fill it again: its control words sit at offsets
+ *     that depend on the sizes.  One workspace per call in flight: two calls
+ *     that overlap on the GPU must not share one.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL is the legacy
  *     default stream).  Argument errors are returned synchronously, before
  *     anything is launched.  Data errors are found on the device, in the rows
@@ -108,7 +110,8 @@ spec_status_t spec_verify(const void *target_logits, spec_dtype_t tdt,
                           void *workspace, size_t workspace_bytes,
                           const spec_aux_t *aux, void *stream);
 
-/* Greedy verification ([SD-EN] § Greedy case): only the target logits are read. */
+/* Greedy verification (aiengineeringfromscratch.com lesson 25, § Greedy case):
+ * only the target logits are read. */
 spec_status_t spec_verify_greedy(const void *target_logits, spec_dtype_t tdt,
                                  const int32_t *draft_tokens, int B, int K, int V,
                                  int32_t *out_tokens, int32_t *out_accept_len,

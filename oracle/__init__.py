@@ -68,7 +68,7 @@ def _load():
                                           P, ctypes.c_int, P,
                                           ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_double, ctypes.c_uint64,
-                                          P, P, P, P, P, P, P, P, P, ctypes.c_int]
+                                          P, P, P, P, P, P, P, P, P, P, ctypes.c_int]
             lib.oracle_verify.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -164,7 +164,7 @@ def _i32(t):
 
 
 def verify(target, draft, draft_tokens, T: float, seed: int, *, draft_is_probs: bool = False,
-           shortlist=None, full: bool = False, threads: int | None = None) -> dict:
+           shortlist=None, full: bool = False, threads: int | None = None, seq_ids=None) -> dict:
     """One verification round for every sequence of the batch.
 
     target: [B][K+1][V] float32 or bfloat16 logits; draft: [B][K][V] logits or
@@ -173,7 +173,9 @@ def verify(target, draft, draft_tokens, T: float, seed: int, *, draft_is_probs: 
     returns q_i(d_i), p_i(d_i) and the log-sum-exp of every row.
     Returns numpy arrays: tokens [B][K+1], accept_len [B], terminal [B],
     residual_mass [B], accept_margin [B][K], sample_margin [B] (and q_draft,
-    p_draft, row_lse when ``full``).
+    p_draft, row_lse when ``full``).  ``seq_ids`` [B] gives the sequence index
+    that keys each row's uniforms (default: the row number), so that a sample
+    of a larger batch draws the same uniforms as the full batch.
     """
     tgt, tdt = _raw(target)
     B, K1, V = tgt.shape
@@ -203,11 +205,12 @@ def verify(target, draft, draft_tokens, T: float, seed: int, *, draft_is_probs: 
         row_lse = np.zeros((B, 2 * K + 1), dtype=np.float64)
     if threads is None:
         threads = os.cpu_count() or 1
+    sid = None if seq_ids is None else np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int32))
     st = _load().oracle_verify(_ptr(tgt), tdt, _ptr(drf), ddt, int(bool(draft_is_probs)),
                                _ptr(sl), S, _ptr(tok), B, K, V, float(T), int(seed) & (2**64 - 1),
                                _ptr(out_tokens), _ptr(out_len), _ptr(q_draft), _ptr(p_draft),
                                _ptr(res_mass), _ptr(row_lse), _ptr(acc_margin), _ptr(smp_margin),
-                               _ptr(terminal), int(threads))
+                               _ptr(terminal), _ptr(sid), int(threads))
     if st:
         raise ValueError("oracle_verify: invalid arguments")
     out = dict(tokens=out_tokens, accept_len=out_len, terminal=terminal, residual_mass=res_mass,

@@ -240,10 +240,17 @@ struct job {
     double *accept_margin;              /* [B][K]   optional                    */
     double *sample_margin;              /* [B]      optional                    */
     int32_t *terminal;                  /* [B]      optional                    */
+    const int32_t *seq_ids;             /* [B] sequence index for the uniforms, or NULL (= b) */
     int nthreads;
 };
 
 struct scratch { double *z, *q, *p, *r; };
+
+/* The sequence index that keys the uniforms of batch row b. */
+static int seq_of(const struct job *J, int b)
+{
+    return J->seq_ids ? J->seq_ids[b] : b;
+}
 
 /* q_i: softmax of target row (b, i). */
 static int target_dist(const struct job *J, int b, int i, struct scratch *w, double *lse)
@@ -361,7 +368,7 @@ static void verify_stochastic(const struct job *J, int b, struct scratch *w)
             emit_error(J, b, OR_ERR_NONFINITE);
             return;
         }
-        double u = verify_uniform(J->seed, b, i, 0);
+        double u = verify_uniform(J->seed, seq_of(J, b), i, 0);
         double a = oracle_accept_prob(w->q[d], w->p[d]);
         if (J->accept_margin && w->p[d] > 0.0)
             J->accept_margin[(size_t)b * K + i] = fabs(u - a);
@@ -375,7 +382,7 @@ static void verify_stochastic(const struct job *J, int b, struct scratch *w)
             return;
         }
         double R = oracle_residual(w->q, w->p, V, w->r);
-        double v = verify_uniform(J->seed, b, i, 1);
+        double v = verify_uniform(J->seed, seq_of(J, b), i, 1);
         double margin;
         int x;
         if (R > 0.0) {
@@ -404,7 +411,7 @@ static void verify_stochastic(const struct job *J, int b, struct scratch *w)
     double Rq = 0.0;
     for (int y = 0; y < V; ++y)
         Rq += w->q[y];
-    double v = verify_uniform(J->seed, b, K, 1), margin;
+    double v = verify_uniform(J->seed, seq_of(J, b), K, 1), margin;
     tok[K] = oracle_inverse_cdf(w->q, V, Rq, v, &margin);
     J->out_accept_len[b] = K;
     if (J->terminal)
@@ -421,6 +428,7 @@ static void verify_stochastic(const struct job *J, int b, struct scratch *w)
 static void all_positions(const struct job *J, int b, struct scratch *w)
 {
     const int K = J->K;
+    int sl_bad = J->shortlist && !shortlist_ok(J, b);
     for (int i = 0; i <= K; ++i) {
         double lse_t = NAN, lse_d = NAN;
         int bad_t = target_dist(J, b, i, w, &lse_t);
@@ -428,7 +436,9 @@ static void all_positions(const struct job *J, int b, struct scratch *w)
             J->row_lse[(size_t)b * (2 * K + 1) + i] = bad_t ? NAN : lse_t;
         if (i == K)
             break;
-        int bad_d = draft_dist(J, b, i, w, &lse_d);
+        int bad_d = sl_bad ? 1 : draft_dist(J, b, i, w, &lse_d);
+        if (sl_bad)
+            lse_d = NAN;
         if (J->row_lse)
             J->row_lse[(size_t)b * (2 * K + 1) + K + 1 + i] = bad_d ? NAN : lse_d;
         int d = J->tokens[(size_t)b * K + i];
@@ -447,6 +457,8 @@ static void verify_greedy(const struct job *J, int b, struct scratch *w)
 {
     const int K = J->K, V = J->V;
     int32_t *tok = J->out_tokens + (size_t)b * (K + 1);
+    if (J->residual_mass)
+        J->residual_mass[b] = NAN;
     for (int i = 0; i <= K; ++i)
         tok[i] = -1;
     for (int i = 0; i <= K; ++i) {
@@ -515,7 +527,7 @@ int oracle_verify(const void *target, int tdt, const void *draft, int ddt, int d
                   int32_t *out_tokens, int32_t *out_accept_len,
                   double *q_draft, double *p_draft, double *residual_mass, double *row_lse,
                   double *accept_margin, double *sample_margin, int32_t *terminal,
-                  int nthreads)
+                  const int32_t *seq_ids, int nthreads)
 {
     if (B < 1 || K < 1 || V < 1 || !(T >= 0.0) || !target || !tokens || !out_tokens || !out_accept_len)
         return 1;
@@ -529,7 +541,7 @@ int oracle_verify(const void *target, int tdt, const void *draft, int ddt, int d
         nthreads = B;
     struct job J = { target, tdt, draft, ddt, draft_is_probs, shortlist, S, tokens, B, K, V, T, seed,
                      out_tokens, out_accept_len, q_draft, p_draft, residual_mass, row_lse,
-                     accept_margin, sample_margin, terminal, nthreads };
+                     accept_margin, sample_margin, terminal, seq_ids, nthreads };
     pthread_t *th = malloc(sizeof(pthread_t) * (size_t)nthreads);
     struct worker *wk = malloc(sizeof(struct worker) * (size_t)nthreads);
     for (int t = 0; t < nthreads; ++t) {

@@ -1,0 +1,264 @@
+"""Batched speculative-decoding verification on GB300 (sm_103a).
+
+A thin ctypes binding over ``libspecverify.so``, whose C ABI is declared in
+``include/specverify.h``.  Every step of the verification runs in the
+library's CUDA kernels; this module only checks tensor shapes and dtypes,
+allocates outputs and scratch with PyTorch, and passes device pointers and
+the current CUDA stream.  There is no CPU fallback: if the library is not
+built, the calls raise.
+
+Notation (nextadmin.net "Speculative Decoding", § Core algorithm): q is the
+target distribution, p the draft distribution, d_i the K drafted tokens.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from .build import LIB as _LIB_PATH
+
+__all__ = [
+    "SpecVerifyError", "Aux", "spec_verify", "spec_verify_greedy", "spec_verify_shortlist",
+    "spec_workspace_bytes", "spec_philox_words", "spec_status_string", "library_path", "load",
+]
+
+SPEC_F32, SPEC_BF16 = 0, 1
+STATUS = {0: "SPEC_OK", 1: "SPEC_ERR_INVALID_ARG", 2: "SPEC_ERR_NONFINITE", 3: "SPEC_ERR_TOKEN_RANGE",
+          4: "SPEC_ERR_SHORTLIST", 5: "SPEC_ERR_UNSUPPORTED", 6: "SPEC_ERR_CUDA", 7: "SPEC_ERR_TIMEOUT"}
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(code, code)} ({spec_status_string(code)})")
+        self.code = code
+
+
+class _AuxStruct(ctypes.Structure):
+    _fields_ = [("q_draft", ctypes.c_void_p), ("p_draft", ctypes.c_void_p),
+                ("residual_mass", ctypes.c_void_p), ("row_lse", ctypes.c_void_p),
+                ("device_status", ctypes.c_void_p)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libspecverify.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise ImportError(f"{_LIB_PATH} is missing: build it first "
+                                  "(python -c 'import __graft_entry__ as g; g.build()')")
+            lib = ctypes.CDLL(_LIB_PATH)
+            P, I, U64, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_float
+            Z = ctypes.c_size_t
+            lib.spec_workspace_bytes.argtypes = [I, I, I, I]
+            lib.spec_workspace_bytes.restype = Z
+            lib.spec_verify.argtypes = [P, I, P, I, I, P, I, I, I, F, U64, P, P, P, Z, P, P]
+            lib.spec_verify.restype = I
+            lib.spec_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, Z, P, P]
+            lib.spec_verify_greedy.restype = I
+            lib.spec_verify_shortlist.argtypes = [P, I, P, I, I, P, I, P, I, I, I, F, U64, P, P, P, Z, P, P]
+            lib.spec_verify_shortlist.restype = I
+            lib.spec_philox_words.argtypes = [U64, ctypes.c_uint32, I, I, P, P]
+            lib.spec_philox_words.restype = I
+            lib.spec_status_string.argtypes = [I]
+            lib.spec_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def spec_status_string(code: int) -> str:
+    return load().spec_status_string(int(code)).decode()
+
+
+def spec_workspace_bytes(B: int, K: int, V: int, S: int = 0) -> int:
+    return int(load().spec_workspace_bytes(int(B), int(K), int(V), int(S)))
+
+
+class Aux:
+    """Optional per-call outputs (device tensors, any may be None).  Asking for
+    q_draft, p_draft or row_lse makes the call evaluate every position."""
+
+    def __init__(self, q_draft=None, p_draft=None, residual_mass=None, row_lse=None, device_status=None):
+        self.q_draft, self.p_draft, self.residual_mass = q_draft, p_draft, residual_mass
+        self.row_lse, self.device_status = row_lse, device_status
+
+    @classmethod
+    def alloc(cls, B: int, K: int, device, full: bool = True) -> "Aux":
+        f = dict(dtype=torch.float32, device=device)
+        nan = float("nan")
+        return cls(q_draft=torch.full((B, K), nan, **f) if full else None,
+                   p_draft=torch.full((B, K), nan, **f) if full else None,
+                   residual_mass=torch.full((B,), nan, **f),
+                   row_lse=torch.full((B, 2 * K + 1), nan, **f) if full else None,
+                   device_status=torch.full((1,), -1, dtype=torch.int32, device=device))
+
+    def _struct(self, B, K):
+        def ptr(t, shape, dtype):
+            if t is None:
+                return None
+            _check(t, shape, (dtype,), "aux")
+            return t.data_ptr()
+        return _AuxStruct(ptr(self.q_draft, (B, K), torch.float32), ptr(self.p_draft, (B, K), torch.float32),
+                          ptr(self.residual_mass, (B,), torch.float32),
+                          ptr(self.row_lse, (B, 2 * K + 1), torch.float32),
+                          ptr(self.device_status, (1,), torch.int32))
+
+
+# ------------------------------------------------------------------ helpers
+def _check(t, shape, dtypes, name):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _dt(t):
+    return SPEC_BF16 if t.dtype == torch.bfloat16 else SPEC_F32
+
+
+_ws_cache: dict = {}
+
+
+def _workspace(device, stream, nbytes, sizes):
+    """A workspace cached per (device, stream).  The library leaves it ready
+    for the next call with the same sizes; when the sizes change, it is
+    zero-filled again (on the same stream) before the call."""
+    key = (device.index, stream)
+    ent = _ws_cache.get(key)
+    if ent is None or ent[0].numel() < nbytes:
+        ent = [torch.zeros(max(nbytes, 1 << 16), dtype=torch.uint8, device=device), sizes]
+        _ws_cache[key] = ent
+    elif ent[1] != sizes:
+        ent[0].zero_()
+        ent[1] = sizes
+    return ent[0]
+
+
+def _outs(B, K, device, out_tokens, out_accept_len):
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=device)
+    if out_accept_len is None:
+        out_accept_len = torch.empty((B,), dtype=torch.int32, device=device)
+    _check(out_tokens, (B, K + 1), (torch.int32,), "out_tokens")
+    _check(out_accept_len, (B,), (torch.int32,), "out_accept_len")
+    return out_tokens, out_accept_len
+
+
+def _stream(device, stream):
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ws_args(device, st, nbytes, workspace, sizes):
+    if workspace is None:
+        workspace = _workspace(device, st, nbytes, sizes)
+    elif not isinstance(workspace, torch.Tensor) or not workspace.is_cuda:
+        raise TypeError("workspace must be a CUDA tensor")
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+# ------------------------------------------------------------------ entry points
+def spec_verify(target: torch.Tensor, draft: torch.Tensor, draft_tokens: torch.Tensor, T: float, seed: int,
+                *, draft_is_probs: bool = False, out_tokens=None, out_accept_len=None, workspace=None,
+                aux: Aux | None = None, stream=None):
+    """One verification round for B sequences.
+
+    target [B][K+1][V] float32/bfloat16 logits; draft [B][K][V] logits of the
+    same dtype, or float32 probabilities with ``draft_is_probs``; draft_tokens
+    [B][K] int32.  T == 0 runs the greedy rule.  Returns (out_tokens [B][K+1],
+    out_accept_len [B]) on the device, asynchronously on the current stream.
+    """
+    B, K1, V = target.shape
+    K = K1 - 1
+    _check(target, (B, K + 1, V), (torch.float32, torch.bfloat16), "target")
+    _check(draft, (B, K, V), (torch.float32,) if draft_is_probs else (target.dtype,), "draft")
+    _check(draft_tokens, (B, K), (torch.int32,), "draft_tokens")
+    dev = target.device
+    out_tokens, out_accept_len = _outs(B, K, dev, out_tokens, out_accept_len)
+    st = _stream(dev, stream)
+    workspace, wsb = _ws_args(dev, st, spec_workspace_bytes(B, K, V, 0), workspace, (B, K, V, 0))
+    ax = aux._struct(B, K) if aux is not None else None
+    rc = load().spec_verify(target.data_ptr(), _dt(target), draft.data_ptr(), _dt(draft), int(draft_is_probs),
+                            draft_tokens.data_ptr(), B, K, V, float(T), int(seed) & (2**64 - 1),
+                            out_tokens.data_ptr(), out_accept_len.data_ptr(), workspace.data_ptr(), wsb,
+                            ctypes.byref(ax) if ax is not None else None, st)
+    if rc:
+        raise SpecVerifyError(rc, "spec_verify")
+    return out_tokens, out_accept_len
+
+
+def spec_verify_greedy(target: torch.Tensor, draft_tokens: torch.Tensor, *, out_tokens=None,
+                       out_accept_len=None, workspace=None, aux: Aux | None = None, stream=None):
+    """Greedy verification: accept d_i while d_i == argmax q_i (lowest index on ties)."""
+    B, K1, V = target.shape
+    K = K1 - 1
+    _check(target, (B, K + 1, V), (torch.float32, torch.bfloat16), "target")
+    _check(draft_tokens, (B, K), (torch.int32,), "draft_tokens")
+    dev = target.device
+    out_tokens, out_accept_len = _outs(B, K, dev, out_tokens, out_accept_len)
+    st = _stream(dev, stream)
+    workspace, wsb = _ws_args(dev, st, spec_workspace_bytes(B, K, V, 0), workspace, (B, K, V, 0))
+    ax = aux._struct(B, K) if aux is not None else None
+    rc = load().spec_verify_greedy(target.data_ptr(), _dt(target), draft_tokens.data_ptr(), B, K, V,
+                                   out_tokens.data_ptr(), out_accept_len.data_ptr(), workspace.data_ptr(), wsb,
+                                   ctypes.byref(ax) if ax is not None else None, st)
+    if rc:
+        raise SpecVerifyError(rc, "spec_verify_greedy")
+    return out_tokens, out_accept_len
+
+
+def spec_verify_shortlist(target: torch.Tensor, draft_sl: torch.Tensor, shortlist_idx: torch.Tensor,
+                          draft_tokens: torch.Tensor, T: float, seed: int, *, draft_is_probs: bool = False,
+                          out_tokens=None, out_accept_len=None, workspace=None, aux: Aux | None = None,
+                          stream=None):
+    """Verification with a draft defined on a per-sequence shortlist.
+
+    draft_sl [B][K][S] (logits of the target's dtype, or float32 probabilities),
+    shortlist_idx [B][S] int32 strictly ascending inside [0, V)."""
+    B, K1, V = target.shape
+    K = K1 - 1
+    S = shortlist_idx.shape[-1]
+    _check(target, (B, K + 1, V), (torch.float32, torch.bfloat16), "target")
+    _check(draft_sl, (B, K, S), (torch.float32,) if draft_is_probs else (target.dtype,), "draft_sl")
+    _check(shortlist_idx, (B, S), (torch.int32,), "shortlist_idx")
+    _check(draft_tokens, (B, K), (torch.int32,), "draft_tokens")
+    dev = target.device
+    out_tokens, out_accept_len = _outs(B, K, dev, out_tokens, out_accept_len)
+    st = _stream(dev, stream)
+    workspace, wsb = _ws_args(dev, st, spec_workspace_bytes(B, K, V, S), workspace, (B, K, V, S))
+    ax = aux._struct(B, K) if aux is not None else None
+    rc = load().spec_verify_shortlist(target.data_ptr(), _dt(target), draft_sl.data_ptr(), _dt(draft_sl),
+                                      int(draft_is_probs), shortlist_idx.data_ptr(), S, draft_tokens.data_ptr(),
+                                      B, K, V, float(T), int(seed) & (2**64 - 1), out_tokens.data_ptr(),
+                                      out_accept_len.data_ptr(), workspace.data_ptr(), wsb,
+                                      ctypes.byref(ax) if ax is not None else None, st)
+    if rc:
+        raise SpecVerifyError(rc, "spec_verify_shortlist")
+    return out_tokens, out_accept_len
+
+
+def spec_philox_words(seed: int, tag: int, B: int, P: int, device=None, stream=None) -> torch.Tensor:
+    """The Philox4x32-10 words the kernels draw: [B][P][4] (int32 storage of uint32)."""
+    device = torch.device(device if device is not None else "cuda")
+    out = torch.empty((B, P, 4), dtype=torch.int32, device=device)
+    st = _stream(device, stream)
+    rc = load().spec_philox_words(int(seed) & (2**64 - 1), int(tag), B, P, out.data_ptr(), st)
+    if rc:
+        raise SpecVerifyError(rc, "spec_philox_words")
+    return out

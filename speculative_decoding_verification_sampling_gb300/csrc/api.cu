@@ -1,0 +1,287 @@
+// api.cu -- the C ABI declared in include/specverify.h: argument checks,
+// workspace layout, task geometry and kernel dispatch.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "specverify.h"
+#include "sv_launch.h"
+#include "sv_params.h"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int kStageBytes = 16384;   // bytes per ring stage (matches the kernel)
+constexpr int kResStage = 2048;      // elements per residual stage (matches the kernel)
+constexpr uint32_t kDefaultSpin = 1u << 22;
+
+// entry ids: 0..3 stoch (tdt*2 + probs), 4..5 greedy (tdt), 6..9 shortlist (tdt*2 + probs)
+constexpr int kEntries = 10;
+
+struct DeviceInfo {
+    bool init = false;
+    bool usable = false;
+    int sms = 0;
+    int occ[kEntries] = {};
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+
+sv::KernelEntry entry_for(int mode, int tdt, bool probs, int *id)
+{
+    if (mode == sv::MODE_GREEDY) {
+        *id = 4 + tdt;
+        return sv::entry_greedy(tdt);
+    }
+    if (mode == sv::MODE_SHORT) {
+        *id = 6 + tdt * 2 + (probs ? 1 : 0);
+        return sv::entry_short(tdt, probs);
+    }
+    *id = tdt * 2 + (probs ? 1 : 0);
+    return sv::entry_stoch(tdt, probs);
+}
+
+// Current device: must be compute capability 10.3 (the build targets sm_103a).
+spec_status_t device_setup(int *sms, int mode, int tdt, bool probs, sv::KernelEntry *entry, int *occ)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices)
+        return SPEC_ERR_UNSUPPORTED;
+    int id = 0;
+    *entry = entry_for(mode, tdt, probs, &id);
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.init) {
+        int major = 0, minor = 0, n = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SPEC_ERR_CUDA;
+        d.usable = (major == 10 && minor == 3);
+        d.sms = n;
+        d.init = true;
+    }
+    if (!d.usable)
+        return SPEC_ERR_UNSUPPORTED;
+    if (d.occ[id] == 0) {
+        int o = 0;
+        if (entry->occupancy(&o) != cudaSuccess || o < 1)
+            return SPEC_ERR_CUDA;
+        d.occ[id] = o;
+    }
+    *sms = d.sms;
+    *occ = d.occ[id];
+    return SPEC_OK;
+}
+
+uint32_t spin_limit()
+{
+    const char *s = std::getenv("SPECVERIFY_SPIN_LIMIT");
+    if (s && *s) {
+        const unsigned long v = std::strtoul(s, nullptr, 10);
+        if (v > 0 && v < 0xffffffffUL)
+            return (uint32_t)v;
+    }
+    return kDefaultSpin;
+}
+
+inline int cdiv(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+bool sizes_ok(int B, int K, int V, int S)
+{
+    if (B < 1 || K < 1 || K > 31 || V < 1 || V > (1 << 30) || S < 0 || S > V)
+        return false;
+    // task counters are 32-bit: bound the worst-case number of tasks
+    const long long rows = (long long)B * (2LL * K + 1);
+    const long long chunks = (long long)(V / 4096 + 1);
+    return rows * chunks < (1LL << 31) && (long long)B * (V / kResStage + 1) < (1LL << 31);
+}
+
+spec_status_t run(int mode, const void *target, spec_dtype_t tdt, const void *draft, spec_dtype_t ddt,
+                  int probs, const int32_t *shortlist, int S, const int32_t *tokens, int B, int K, int V,
+                  float T, uint64_t seed, int32_t *out_tokens, int32_t *out_len, void *workspace,
+                  size_t workspace_bytes, const spec_aux_t *aux, void *stream)
+{
+    // ---- synchronous argument checks (nothing touches the GPU before these pass)
+    if (!sizes_ok(B, K, V, mode == sv::MODE_SHORT ? S : 0))
+        return SPEC_ERR_INVALID_ARG;
+    if (mode == sv::MODE_SHORT && S < 1)
+        return SPEC_ERR_INVALID_ARG;
+    if (!target || !tokens || !out_tokens || !out_len || !workspace)
+        return SPEC_ERR_INVALID_ARG;
+    if (tdt != SPEC_F32 && tdt != SPEC_BF16)
+        return SPEC_ERR_INVALID_ARG;
+    if (!std::isfinite(T) || T < 0.0f)
+        return SPEC_ERR_INVALID_ARG;
+    if (T == 0.0f)
+        mode = sv::MODE_GREEDY;
+    if (mode != sv::MODE_GREEDY) {
+        if (!draft)
+            return SPEC_ERR_INVALID_ARG;
+        if (probs ? ddt != SPEC_F32 : ddt != tdt)
+            return SPEC_ERR_INVALID_ARG;
+        if (mode == sv::MODE_SHORT && !shortlist)
+            return SPEC_ERR_INVALID_ARG;
+        const double c = 1.4426950408889634 / (double)T;
+        if (!std::isfinite((float)c))
+            return SPEC_ERR_INVALID_ARG;
+    }
+    const int S_eff = mode == sv::MODE_SHORT ? S : 0;
+    const sv::WsLayout L = sv::ws_layout(B, K, V, S_eff);
+    if (workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 15u))
+        return SPEC_ERR_INVALID_ARG;
+
+    int sms = 0, occ = 0;
+    sv::KernelEntry entry{};
+    spec_status_t st = device_setup(&sms, mode, tdt == SPEC_BF16 ? 1 : 0, probs != 0, &entry, &occ);
+    if (st != SPEC_OK)
+        return st;
+
+    sv::Params P{};
+    const bool greedy = mode == sv::MODE_GREEDY;
+    const bool is_probs = !greedy && probs != 0;
+    P.target = target;
+    P.draft = greedy ? nullptr : draft;
+    P.shortlist = mode == sv::MODE_SHORT ? shortlist : nullptr;
+    P.tokens = tokens;
+    P.B = B;
+    P.K = K;
+    P.V = V;
+    P.S = S_eff;
+    P.Vd = mode == sv::MODE_SHORT ? S : V;
+    const double Tsafe = greedy ? 1.0 : (double)T;
+    P.cd = 1.4426950408889634 / Tsafe;
+    P.c = (float)P.cd;
+    P.invT = 1.0 / Tsafe;
+    P.key0 = (uint32_t)(seed & 0xffffffffu);
+    P.key1 = (uint32_t)(seed >> 32);
+    P.out_tokens = out_tokens;
+    P.out_len = out_len;
+    if (aux) {
+        P.aux_q = greedy ? nullptr : aux->q_draft;
+        P.aux_p = greedy ? nullptr : aux->p_draft;
+        P.aux_R = aux->residual_mass;
+        P.aux_lse = greedy ? nullptr : aux->row_lse;
+        P.aux_status = aux->device_status;
+    }
+    P.full = (P.aux_q || P.aux_p || P.aux_lse) ? 1 : 0;
+
+    char *w = static_cast<char *>(workspace);
+    P.ctl = reinterpret_cast<uint32_t *>(w + L.ctl);
+    P.state = reinterpret_cast<unsigned long long *>(w + L.state);
+    P.res_seq = reinterpret_cast<int32_t *>(w + L.res_seq);
+    P.pair_cnt = reinterpret_cast<uint32_t *>(w + L.pair_cnt);
+    P.res_cnt = reinterpret_cast<uint32_t *>(w + L.res_cnt);
+    P.fin = reinterpret_cast<int32_t *>(w + L.fin);
+    P.errres = reinterpret_cast<int32_t *>(w + L.errres);
+    P.errcode = reinterpret_cast<int32_t *>(w + L.errcode);
+    P.terminal = reinterpret_cast<int32_t *>(w + L.terminal);
+    P.gtok = reinterpret_cast<int32_t *>(w + L.gtok);
+    P.dec = reinterpret_cast<sv::Dec *>(w + L.dec);
+    P.part = reinterpret_cast<sv::Partial *>(w + L.part);
+    P.seg = reinterpret_cast<sv::SegMass *>(w + L.seg);
+    P.seglast = reinterpret_cast<int32_t *>(w + L.seglast);
+    P.sl_lb = reinterpret_cast<int32_t *>(w + L.sl_lb);
+
+    // ---- task geometry
+    P.es_t = tdt == SPEC_F32 ? 4 : 2;
+    P.es_d = is_probs ? 4 : P.es_t;
+    P.se_t = kStageBytes / P.es_t;
+    P.se_d = kStageBytes / P.es_d;
+    const bool draft_stats = !greedy && !is_probs;
+    const long long stages_t = cdiv(V, P.se_t), stages_d = draft_stats ? cdiv(P.Vd, P.se_d) : 0;
+    const long long total_stages = (long long)B * ((K + 1) * stages_t + (long long)K * stages_d);
+    const long long grid_max = (long long)sms * occ;
+    const int spt = total_stages >= 16 * grid_max ? 4 : (total_stages >= 8 * grid_max ? 2 : 1);
+    P.spt_t = P.spt_d = spt;
+    P.nct = cdiv(V, (long long)spt * P.se_t);
+    P.ncd = draft_stats ? cdiv(P.Vd, (long long)spt * P.se_d) : 0;
+    P.npt = P.nct + P.ncd;
+    const long long res_stages = (long long)B * cdiv(V, kResStage);
+    P.rspt = res_stages >= 8 * grid_max ? 4 : 1;
+    P.ncr = cdiv(V, (long long)P.rspt * kResStage);
+    P.nseg = L.nseg;
+    P.n_stats = (uint32_t)((long long)K * B * P.npt + (long long)B * P.nct);
+    P.n_res = greedy ? 0u : (uint32_t)((long long)B * P.ncr);
+    P.spin_limit = spin_limit();
+    P.bulk_t = (reinterpret_cast<uintptr_t>(target) % 16 == 0) && ((long long)V * P.es_t) % 16 == 0;
+    P.bulk_d = !greedy && (reinterpret_cast<uintptr_t>(draft) % 16 == 0) &&
+               ((long long)P.Vd * P.es_d) % 16 == 0;
+
+    const long long grid = std::min<long long>(grid_max, std::max<long long>(1, (long long)P.n_stats));
+    if (entry.launch(P, (int)grid, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t spec_workspace_bytes(int B, int K, int V, int S)
+{
+    if (!sizes_ok(B, K, V, S))
+        return 0;
+    return sv::ws_layout(B, K, V, S).total;
+}
+
+spec_status_t spec_verify(const void *target_logits, spec_dtype_t tdt, const void *draft, spec_dtype_t ddt,
+                          int draft_is_probs, const int32_t *draft_tokens, int B, int K, int V, float T,
+                          uint64_t seed, int32_t *out_tokens, int32_t *out_accept_len, void *workspace,
+                          size_t workspace_bytes, const spec_aux_t *aux, void *stream)
+{
+    return run(sv::MODE_STOCH, target_logits, tdt, draft, ddt, draft_is_probs, nullptr, 0, draft_tokens, B, K,
+               V, T, seed, out_tokens, out_accept_len, workspace, workspace_bytes, aux, stream);
+}
+
+spec_status_t spec_verify_greedy(const void *target_logits, spec_dtype_t tdt, const int32_t *draft_tokens,
+                                 int B, int K, int V, int32_t *out_tokens, int32_t *out_accept_len,
+                                 void *workspace, size_t workspace_bytes, const spec_aux_t *aux, void *stream)
+{
+    return run(sv::MODE_GREEDY, target_logits, tdt, nullptr, tdt, 0, nullptr, 0, draft_tokens, B, K, V, 0.0f,
+               0, out_tokens, out_accept_len, workspace, workspace_bytes, aux, stream);
+}
+
+spec_status_t spec_verify_shortlist(const void *target_logits, spec_dtype_t tdt, const void *draft_sl,
+                                    spec_dtype_t ddt, int draft_is_probs, const int32_t *shortlist_idx, int S,
+                                    const int32_t *draft_tokens, int B, int K, int V, float T, uint64_t seed,
+                                    int32_t *out_tokens, int32_t *out_accept_len, void *workspace,
+                                    size_t workspace_bytes, const spec_aux_t *aux, void *stream)
+{
+    if (S < 1)
+        return SPEC_ERR_INVALID_ARG;
+    return run(sv::MODE_SHORT, target_logits, tdt, draft_sl, ddt, draft_is_probs, shortlist_idx, S,
+               draft_tokens, B, K, V, T, seed, out_tokens, out_accept_len, workspace, workspace_bytes, aux,
+               stream);
+}
+
+spec_status_t spec_philox_words(uint64_t seed, uint32_t tag, int B, int P, uint32_t *out, void *stream)
+{
+    if (B < 1 || P < 1 || !out || (long long)B * P > (1LL << 28))
+        return SPEC_ERR_INVALID_ARG;
+    if (sv::launch_philox_words((uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32), tag, B, P, out,
+                                static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+const char *spec_status_string(spec_status_t status)
+{
+    switch (status) {
+    case SPEC_OK: return "ok";
+    case SPEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPEC_ERR_NONFINITE: return "non-finite logit, all -inf row, or bad draft probability";
+    case SPEC_ERR_TOKEN_RANGE: return "draft token outside [0, V)";
+    case SPEC_ERR_SHORTLIST: return "shortlist not strictly ascending inside [0, V)";
+    case SPEC_ERR_UNSUPPORTED: return "no usable sm_103a device";
+    case SPEC_ERR_CUDA: return "CUDA runtime error";
+    case SPEC_ERR_TIMEOUT: return "on-device wait ran out";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,129 @@
+// sv_params.h -- launch parameters shared by the host launcher and the
+// verification kernels (plain C++ types only).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+namespace sv {
+
+enum Mode { MODE_STOCH = 0, MODE_GREEDY = 1, MODE_SHORT = 2 };
+
+// Status codes; the same values as spec_status_t.
+enum Status { ST_OK = 0, ST_NONFINITE = 2, ST_TOKEN = 3, ST_SHORTLIST = 4, ST_TIMEOUT = 7 };
+
+// Words of the control block at the start of the workspace.
+enum Ctl { CTL_STATS_NEXT = 0, CTL_RES_TICKET = 1, CTL_RES_COUNT = 2, CTL_EXIT = 3, CTL_STATUS = 4,
+           CTL_WORDS = 8 };
+
+// Partial result of one stats task (one chunk of one row):
+//   logits: m = max raw logit of the chunk, s = sum 2^((x - m) * c) over the chunk;
+//   greedy: m = max raw logit and its lowest index.
+// flag bit 0: NaN or +inf seen; bit 1: shortlist entry out of range or out of order.
+struct Partial {
+    float m;
+    int flag;
+    float s_hi;   // s = s_hi + s_lo (a float pair; greedy: s_hi holds the index bits)
+    float s_lo;
+};
+
+// Residual mass r and target mass q of one 256-token segment.
+struct SegMass {
+    float r, q;
+};
+
+// Per (sequence, position) quantities the residual pass needs, in float32:
+// Mt = max target logit, Lt2 = log2 of the target sum, dL = log2(Z_draft / Z_target)
+// split into a high and a low float.
+struct Dec {
+    float Mt, Lt2, dLhi, dLlo;
+};
+
+struct Params {
+    // inputs (device)
+    const void *target;        // [B][K+1][V]
+    const void *draft;         // [B][K][Vd]  (Vd = V, or S with a shortlist)
+    const int32_t *shortlist;  // [B][S] or nullptr
+    const int32_t *tokens;     // [B][K]
+    int B, K, V, Vd, S;
+    float c;                   // log2(e) / T
+    double cd;                 // log2(e) / T in float64
+    double invT;               // 1 / T
+    uint32_t key0, key1;       // Philox key (seed low, seed high)
+    int full;                  // evaluate every position (per-position outputs requested)
+
+    // outputs (device)
+    int32_t *out_tokens;       // [B][K+1]
+    int32_t *out_len;          // [B]
+    float *aux_q, *aux_p, *aux_R, *aux_lse;
+    int32_t *aux_status;
+
+    // workspace (device)
+    uint32_t *ctl;                 // [CTL_WORDS]
+    unsigned long long *state;     // [B]  decided positions (low word) | accepted positions (high word)
+    int32_t *res_seq;              // [B]  sequence + 1 for each published residual slot
+    uint32_t *pair_cnt;            // [B][K+1] finished stats tasks per position
+    uint32_t *res_cnt;             // [B]  finished residual tasks per sequence
+    int32_t *fin;                  // [B]  1 once the sequence's outputs are written
+    int32_t *errres;               // [B]  1 when the residual pass met a bad draft probability
+    int32_t *errcode;              // [B][K+1] data error found at the position (0 = none)
+    int32_t *terminal;             // [B]  position of the emitted target token (-1 on error)
+    int32_t *gtok;                 // [B][K+1] greedy argmax per position
+    Dec *dec;                      // [B][K+1]
+    Partial *part;                 // [B][K+1][npt]
+    SegMass *seg;                  // [B][nseg] residual mass and target mass per 256-token segment
+    int32_t *seglast;              // [B][nseg] last token with positive residual in the segment
+    int32_t *sl_lb;                // [B][nseg+1] first shortlist entry at or after token 256*t
+
+    // task geometry
+    int es_t, es_d;                // element sizes of target and draft rows
+    int se_t, se_d;                // elements per stats stage
+    int spt_t, spt_d;              // stages per stats task
+    int nct, ncd, npt;             // stats tasks per target row, per draft row, per position
+    int rspt, ncr;                 // stages per residual task, residual tasks per sequence
+    int nseg;                      // 256-token segments per target row
+    uint32_t n_stats, n_res;       // total stats tasks, total residual tasks
+    uint32_t spin_limit;           // bound on every on-device wait loop
+    int bulk_t, bulk_d;            // rows eligible for bulk copies (16-byte aligned)
+};
+
+// Workspace layout for (B, K, V, S); every array starts 256-byte aligned.
+struct WsLayout {
+    size_t ctl, state, res_seq, pair_cnt, res_cnt, fin, errres, errcode, terminal, gtok, dec, part,
+        seg, seglast, sl_lb, total;
+    size_t reset_end;   // [ctl, reset_end) holds what a call must find zeroed
+    int npt_max, nseg;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Stats chunks are at least 4096 elements (16 KB of float32), so this bounds
+// the number of partials any chunking chooses.
+inline WsLayout ws_layout(int B, int K, int V, int S)
+{
+    WsLayout w{};
+    const size_t Bz = (size_t)B, P = (size_t)K + 1;
+    const int Vd = S > 0 ? S : V;
+    w.nseg = (V + 255) / 256;
+    w.npt_max = (V + 4095) / 4096 + (Vd + 4095) / 4096;
+    size_t o = 0;
+    w.ctl = o;      o = align256(o + 8 * sizeof(uint32_t));
+    w.state = o;    o = align256(o + Bz * 8);
+    w.res_seq = o;  o = align256(o + Bz * 4);
+    w.pair_cnt = o; o = align256(o + Bz * P * 4);
+    w.res_cnt = o;  o = align256(o + Bz * 4);
+    w.fin = o;      o = align256(o + Bz * 4);
+    w.errres = o;   o = align256(o + Bz * 4);
+    w.reset_end = o;
+    w.errcode = o;  o = align256(o + Bz * P * 4);
+    w.terminal = o; o = align256(o + Bz * 4);
+    w.gtok = o;     o = align256(o + Bz * P * 4);
+    w.dec = o;      o = align256(o + Bz * P * sizeof(Dec));
+    w.part = o;     o = align256(o + Bz * P * (size_t)w.npt_max * sizeof(Partial));
+    w.seg = o;      o = align256(o + Bz * (size_t)w.nseg * sizeof(SegMass));
+    w.seglast = o;  o = align256(o + Bz * (size_t)w.nseg * 4);
+    w.sl_lb = o;    o = align256(o + (S > 0 ? Bz * (size_t)(w.nseg + 1) * 4 : 0));
+    w.total = o;
+    return w;
+}
+
+}  // namespace sv
