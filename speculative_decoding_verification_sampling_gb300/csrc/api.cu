@@ -3,6 +3,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <algorithm>
 #include <mutex>
 
 #include "specverify.h"
@@ -12,8 +13,8 @@
 namespace {
 
 constexpr int kMaxDevices = 64;
-constexpr int kStageBytes = 16384;   // bytes per ring stage (matches the kernel)
-constexpr int kResStage = 2048;      // elements per residual stage (matches the kernel)
+constexpr int kStageBytes = 4096;    // bytes per ring stage (matches the kernel)
+constexpr int kWorkersPerSM = 16;    // worker warps per CTA, one CTA per SM (matches the kernel)
 constexpr uint32_t kDefaultSpin = 1u << 22;
 
 // entry ids: 0..3 stoch (tdt*2 + probs), 4..5 greedy (tdt), 6..9 shortlist (tdt*2 + probs)
@@ -97,8 +98,8 @@ bool sizes_ok(int B, int K, int V, int S)
         return false;
     // task counters are 32-bit: bound the worst-case number of tasks
     const long long rows = (long long)B * (2LL * K + 1);
-    const long long chunks = (long long)(V / 4096 + 1);
-    return rows * chunks < (1LL << 31) && (long long)B * (V / kResStage + 1) < (1LL << 31);
+    const long long chunks = (long long)(V / 1024 + 1);
+    return rows * chunks < (1LL << 31);
 }
 
 spec_status_t run(int mode, const void *target, spec_dtype_t tdt, const void *draft, spec_dtype_t ddt,
@@ -173,7 +174,7 @@ spec_status_t run(int mode, const void *target, spec_dtype_t tdt, const void *dr
     char *w = static_cast<char *>(workspace);
     P.ctl = reinterpret_cast<uint32_t *>(w + L.ctl);
     P.state = reinterpret_cast<unsigned long long *>(w + L.state);
-    P.res_seq = reinterpret_cast<int32_t *>(w + L.res_seq);
+    P.res_rec = reinterpret_cast<sv::ResRec *>(w + L.res_rec);
     P.pair_cnt = reinterpret_cast<uint32_t *>(w + L.pair_cnt);
     P.res_cnt = reinterpret_cast<uint32_t *>(w + L.res_cnt);
     P.fin = reinterpret_cast<int32_t *>(w + L.fin);
@@ -184,7 +185,6 @@ spec_status_t run(int mode, const void *target, spec_dtype_t tdt, const void *dr
     P.dec = reinterpret_cast<sv::Dec *>(w + L.dec);
     P.part = reinterpret_cast<sv::Partial *>(w + L.part);
     P.seg = reinterpret_cast<sv::SegMass *>(w + L.seg);
-    P.seglast = reinterpret_cast<int32_t *>(w + L.seglast);
     P.sl_lb = reinterpret_cast<int32_t *>(w + L.sl_lb);
 
     // ---- task geometry
@@ -193,26 +193,33 @@ spec_status_t run(int mode, const void *target, spec_dtype_t tdt, const void *dr
     P.se_t = kStageBytes / P.es_t;
     P.se_d = kStageBytes / P.es_d;
     const bool draft_stats = !greedy && !is_probs;
-    const long long stages_t = cdiv(V, P.se_t), stages_d = draft_stats ? cdiv(P.Vd, P.se_d) : 0;
-    const long long total_stages = (long long)B * ((K + 1) * stages_t + (long long)K * stages_d);
-    const long long grid_max = (long long)sms * occ;
-    const int spt = total_stages >= 16 * grid_max ? 4 : (total_stages >= 8 * grid_max ? 2 : 1);
-    P.spt_t = P.spt_d = spt;
-    P.nct = cdiv(V, (long long)spt * P.se_t);
-    P.ncd = draft_stats ? cdiv(P.Vd, (long long)spt * P.se_d) : 0;
+    // stats units: one stage of one row each
+    P.nct = cdiv(V, P.se_t);
+    P.ncd = draft_stats ? cdiv(P.Vd, P.se_d) : 0;
     P.npt = P.nct + P.ncd;
-    const long long res_stages = (long long)B * cdiv(V, kResStage);
-    P.rspt = res_stages >= 8 * grid_max ? 4 : 1;
-    P.ncr = cdiv(V, (long long)P.rspt * kResStage);
-    P.nseg = L.nseg;
     P.n_stats = (uint32_t)((long long)K * B * P.npt + (long long)B * P.nct);
+    // a residual stage holds the same tokens of the target row and, at a
+    // rejection over the full vocabulary, of the draft row
+    const int res_es = P.es_t + ((mode == sv::MODE_STOCH) ? P.es_d : 0);
+    P.rse = (kStageBytes / res_es) / 256 * 256;
+    P.rd_off = P.rse * P.es_t;
+    const long long grid_max = (long long)sms * occ;
+    const long long grid =
+        std::min<long long>(grid_max, std::max<long long>(1, cdiv(P.n_stats, 2 * kWorkersPerSM)));
+    P.workers = (uint32_t)(grid * kWorkersPerSM);
+    const long long res_stages = cdiv(V, P.rse);
+    P.rspt = (int)std::max<long long>(1, std::min<long long>(3, (long long)B * res_stages / ((long long)P.workers * 4)));
+    P.ncr = cdiv(V, (long long)P.rspt * P.rse);
+    P.nseg = L.nseg;
     P.n_res = greedy ? 0u : (uint32_t)((long long)B * P.ncr);
+    // first batches: about a sixth of the units, at most 16 per worker
+    P.g0 = (uint32_t)std::max<long long>(1, std::min<long long>(16, (long long)P.n_stats / (6LL * P.workers)));
+    P.first_units = std::min<uint32_t>(P.n_stats, P.g0 * P.workers);
     P.spin_limit = spin_limit();
     P.bulk_t = (reinterpret_cast<uintptr_t>(target) % 16 == 0) && ((long long)V * P.es_t) % 16 == 0;
     P.bulk_d = !greedy && (reinterpret_cast<uintptr_t>(draft) % 16 == 0) &&
                ((long long)P.Vd * P.es_d) % 16 == 0;
 
-    const long long grid = std::min<long long>(grid_max, std::max<long long>(1, (long long)P.n_stats));
     if (entry.launch(P, (int)grid, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SPEC_ERR_CUDA;
     return SPEC_OK;

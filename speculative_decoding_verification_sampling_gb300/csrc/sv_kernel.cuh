@@ -8,30 +8,31 @@
 // Work is split into tasks, scheduled left to right by position:
 //   stats task    one chunk of one row at position i: the online maximum and
 //                 sum of 2^((x - m) * log2(e) / T) (greedy: maximum and its
-//                 lowest index).  All positions-0 tasks of every sequence come
+//                 lowest index).  All position-0 tasks of every sequence come
 //                 first, then position 1, ...; a task whose sequence already
 //                 stopped before position i is skipped without reading its
 //                 rows (the rule discards everything after the first rejection).
-//   decision      the last stats task of (sequence, position) merges the
-//                 chunk partials in float64, draws u_i (Philox) and decides
-//                 accept_i = u_i < min(1, q_i(d_i) / p_i(d_i)).  Decisions are
-//                 published in a per-sequence bit word; the first non-accepted
-//                 decided position j with all earlier ones accepted ends the
-//                 sequence.
+//   decision      the worker that finishes the last chunk of (sequence,
+//                 position) merges the chunk partials in float64, draws u_i
+//                 (Philox) and decides accept_i = u_i < min(1, q_i(d_i)/p_i(d_i)).
+//                 Decisions are published in a per-sequence bit word; the first
+//                 non-accepted decided position j, with all earlier ones
+//                 accepted, ends the sequence.
 //   residual task one chunk of rows j (target and draft) of an ended
 //                 sequence: r(x) = max(0, q_j(x) - p_j(x)) (r = q_{K+1} for a
-//                 bonus), summed per 256-token segment.  The last one locates
-//                 the token by inverse CDF: a float64 scan over segment masses,
-//                 then a scan inside one segment.  No probability is stored.
+//                 bonus), summed per 256-token segment.  The worker finishing the
+//                 last one locates the token by inverse CDF: a float64 scan over
+//                 segment masses, then a scan inside one segment.  No
+//                 probability is stored.
 //
-// Each CTA has three roles:
-//   warp 8  (producer)  pops tasks and streams their rows into a ring of
-//                       shared-memory stages with cp.async.bulk, completion on
-//                       mbarriers;
-//   warps 0-7 (consumers) process stages and hand per-task warp results over;
-//   warp 9  (finisher)  publishes partials, decides, resolves and locates.
+// Every warp is an independent worker: it pops tasks from global counters,
+// streams its tasks' rows through its own ring of shared-memory stages with
+// cp.async.bulk (completion on one mbarrier per stage), reduces them, and
+// publishes, decides or locates itself.  Warps share nothing but the CTA's
+// shared-memory carve-up, so a slow warp never holds the others back; sixteen
+// workers per SM hide each other's memory and synchronisation latency.
 // Every wait is bounded by Params::spin_limit; a wait that runs out sets
-// SPEC_ERR_TIMEOUT and the CTA winds down, draining its own bulk copies.
+// SPEC_ERR_TIMEOUT and the worker winds down after draining its own copies.
 // The last CTA to finish resets the workspace control words for the next call.
 #pragma once
 #include <cstdint>
@@ -42,46 +43,27 @@
 
 namespace sv {
 
-constexpr int NCW = 8;                       // consumer warps
-constexpr int W_PROD = NCW;                  // producer warp
-constexpr int W_FIN = NCW + 1;               // finisher warp
-constexpr int NTHREADS = (NCW + 2) * 32;
-constexpr int STAGE_BYTES = 16384;
-constexpr int NST = 6;                       // ring stages
-constexpr int NH = 8;                        // hand-off slots
-constexpr int RSE = 2048;                    // elements per residual stage
-constexpr int RD_OFF = 8192;                 // byte offset of the draft part of a residual stage
+constexpr int NWARP = 16;                    // workers per CTA
+constexpr int NTHREADS = NWARP * 32;
+constexpr int RS = 3;                        // ring stages per worker
+constexpr int SB = 4096;                     // bytes per stage
 constexpr int SEG = 256;                     // tokens per segment
 constexpr uint32_t DRAIN_LIMIT = 1u << 24;   // polls while waiting for our own bulk copies
 #define F_INF __int_as_float(0x7f800000)
 
-enum Kind { K_EXIT = 0, K_STAT_T = 1, K_STAT_D = 2, K_RES = 3 };
+enum Kind { K_NONE = 0, K_STAT_T = 1, K_STAT_D = 2, K_RES = 3 };
 
+// What one ring stage holds.
 struct Meta {
-    int kind, b, pos, k, e0, n, last, direct;
+    int kind, b, pos;
+    int kf;           // stats: first unit of the run this stage belongs to; residual: task index
+    int ku;           // stats: this stage's unit
+    int e0, n, last, direct;
     const void *g0;   // row element e0 (target row, or draft row for K_STAT_D)
     const void *g1;   // residual: draft row element e0
+    float4 rc;        // residual: Mt, Lt2, dLhi, dLlo of the sequence's last position
 };
 
-struct Hand {
-    int kind, b, pos, k;
-    float wm[NCW];
-    int wf[NCW];
-    int wi[NCW];
-    float ws_hi[NCW];
-    float ws_lo[NCW];
-};
-
-struct Shared {
-    unsigned long long full[NST], empty[NST], hfull[NH], hempty[NH];
-    Meta meta[NST];
-    Hand hand[NH];
-    float pscr[NCW + 1][SEG];
-    volatile int abort;
-    int last_cta;
-};
-
-constexpr size_t SMEM_BYTES = (size_t)NST * STAGE_BYTES + sizeof(Shared);
 
 // ------------------------------------------------------------------ PTX helpers
 __device__ __forceinline__ uint32_t saddr(const void *p)
@@ -160,6 +142,55 @@ __device__ __forceinline__ float fmax_nan(float a, float b)
 {
     float r;
     asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+// Two floats in one 64-bit register, for the packed f32x2 instructions.
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 pk(float lo, float hi)
+{
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ f2 pku(uint32_t lo, uint32_t hi)
+{
+    f2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ void upk(f2 v, float &lo, float &hi)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f2 add2(f2 a, f2 b)
+{
+    f2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 mul2(f2 a, f2 b)
+{
+    f2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c)
+{
+    f2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ f2 ex2x2(f2 v)
+{
+    float a, b;
+    upk(v, a, b);
+    return pk(ex2a(a), ex2a(b));
+}
+// Elementwise NaN-propagating max of two bfloat16 pairs.
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
 template <class T> __device__ __forceinline__ T ld_vol(const T *p) { return *(const volatile T *)p; }
@@ -324,6 +355,32 @@ struct F32 {
         return __ldcg(static_cast<const float *>(base) + i);
     }
     __device__ static __forceinline__ uint4 neg_inf() { return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u); }
+    // element pairs (2i, 2i+1) of one 16-byte vector
+    __device__ static __forceinline__ f2 pair(const uint4 &v, int i)
+    {
+        return i == 0 ? pku(v.x, v.y) : pku(v.z, v.w);
+    }
+    // NaN-propagating max of the elements of four vectors
+    __device__ static __forceinline__ float quad_max(const uint4 *v)
+    {
+        float m[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            m[2 * k] = fmax_nan(__uint_as_float(v[k].x), __uint_as_float(v[k].y));
+            m[2 * k + 1] = fmax_nan(__uint_as_float(v[k].z), __uint_as_float(v[k].w));
+        }
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i)
+                m[i] = fmax_nan(m[i], m[i + w]);
+        return m[0];
+    }
+    __device__ static __forceinline__ float vec_max(const uint4 &v)
+    {
+        return fmax_nan(fmax_nan(__uint_as_float(v.x), __uint_as_float(v.y)),
+                        fmax_nan(__uint_as_float(v.z), __uint_as_float(v.w)));
+    }
 };
 struct BF16 {
     static constexpr int ES = 2;
@@ -350,17 +407,40 @@ struct BF16 {
         return __uint_as_float((uint32_t)h << 16);
     }
     __device__ static __forceinline__ uint4 neg_inf() { return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u); }
+    __device__ static __forceinline__ f2 pair(const uint4 &v, int i)
+    {
+        const uint32_t w = i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+        return pku(w << 16, w & 0xffff0000u);
+    }
+    __device__ static __forceinline__ float word_max(uint32_t w)
+    {
+        return fmax_nan(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+    __device__ static __forceinline__ float quad_max(const uint4 *v)
+    {
+        uint32_t m[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            m[2 * k] = bmax2(v[k].x, v[k].y);
+            m[2 * k + 1] = bmax2(v[k].z, v[k].w);
+        }
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i)
+                m[i] = bmax2(m[i], m[i + w]);
+        return word_max(m[0]);
+    }
+    __device__ static __forceinline__ float vec_max(const uint4 &v)
+    {
+        return word_max(bmax2(bmax2(v.x, v.y), bmax2(v.z, v.w)));
+    }
 };
 
 // ------------------------------------------------------------------ small shared steps
 __device__ __forceinline__ void set_status(const Params &P, int code)
 {
     atomicCAS(&P.ctl[CTL_STATUS], 0u, (uint32_t)code);
-}
-__device__ __forceinline__ void abort_cta(const Params &P, Shared &sh)
-{
-    set_status(P, ST_TIMEOUT);
-    sh.abort = 1;
 }
 __device__ __forceinline__ void write_error(const Params &P, int b, int code)
 {
@@ -378,206 +458,18 @@ __device__ __forceinline__ bool resolved(unsigned long long st, int &j)
     j = __ffs(~A) - 1;
     return (D >> j) & 1u;
 }
-__device__ __forceinline__ bool seq_dead(const Params &P, int b, int pos)
-{
-    int j;
-    return resolved(ld_vol(&P.state[b]), j) && j < pos;
-}
 
-// =================================================================== producer
-struct Ring {
-    uint32_t slot = 0, ph = 0, txmask = 0, phmask = 0;
-};
-
-__device__ __forceinline__ bool ring_acquire(const Params &P, Shared &sh, Ring &r)
-{
-    return mbar_wait(&sh.empty[r.slot], r.ph ^ 1u, P.spin_limit, &sh.abort);
-}
-__device__ __forceinline__ void ring_advance(Ring &r)
-{
-    if (++r.slot == NST) {
-        r.slot = 0;
-        r.ph ^= 1u;
-    }
-}
-// Publish the stage in r.slot: bulk copies of `bytes0` from g0 (and `bytes1`
-// from g1 at RD_OFF), or a plain arrival when the consumers read global memory.
-__device__ __forceinline__ void ring_publish(Shared &sh, uint8_t *ring, Ring &r, bool bulk,
-                                             const void *g0, uint32_t bytes0, const void *g1,
-                                             uint32_t bytes1)
-{
-    unsigned long long *bar = &sh.full[r.slot];
-    if (bulk) {
-        mbar_arrive_tx(bar, bytes0 + bytes1);
-        uint8_t *dst = ring + (size_t)r.slot * STAGE_BYTES;
-        bulk_g2s(dst, g0, bytes0, bar);
-        if (bytes1)
-            bulk_g2s(dst + RD_OFF, g1, bytes1, bar);
-        r.txmask |= 1u << r.slot;
-        r.phmask = (r.phmask & ~(1u << r.slot)) | (r.ph << r.slot);
-    } else {
-        mbar_arrive(bar);
-    }
-}
-
-template <class E, int MODE, bool PROBS>
-__device__ bool issue_stats(const Params &P, Shared &sh, uint8_t *ring, Ring &r, int b, int pos, int k)
-{
-    const bool is_t = k < P.nct;
-    const int kk = is_t ? k : k - P.nct;
-    const int es = is_t ? P.es_t : P.es_d, se = is_t ? P.se_t : P.se_d;
-    const int spt = is_t ? P.spt_t : P.spt_d, n_row = is_t ? P.V : P.Vd;
-    const bool bulk = is_t ? P.bulk_t : P.bulk_d;
-    const char *row = is_t ? static_cast<const char *>(P.target) +
-                                 ((size_t)b * (P.K + 1) + pos) * (size_t)P.V * es
-                           : static_cast<const char *>(P.draft) +
-                                 ((size_t)b * P.K + pos) * (size_t)P.Vd * es;
-    const int e_begin = kk * spt * se;
-    const int e_end = min(n_row, e_begin + spt * se);
-    for (int e0 = e_begin; e0 < e_end; e0 += se) {
-        const int n = min(se, e_end - e0);
-        if (!ring_acquire(P, sh, r))
-            return false;
-        Meta &m = sh.meta[r.slot];
-        m.kind = is_t ? K_STAT_T : K_STAT_D;
-        m.b = b;
-        m.pos = pos;
-        m.k = k;
-        m.e0 = e0;
-        m.n = n;
-        m.last = (e0 + se >= e_end);
-        m.direct = !bulk;
-        m.g0 = row + (size_t)e0 * es;
-        m.g1 = nullptr;
-        ring_publish(sh, ring, r, bulk, m.g0, (uint32_t)(n * es), nullptr, 0);
-        ring_advance(r);
-    }
-    return true;
-}
-
-template <class E, int MODE, bool PROBS>
-__device__ bool issue_residual(const Params &P, Shared &sh, uint8_t *ring, Ring &r, int b, int j, int k)
-{
-    const bool has_d = (MODE == MODE_STOCH) && j < P.K;
-    const char *row_t = static_cast<const char *>(P.target) + ((size_t)b * (P.K + 1) + j) * (size_t)P.V * P.es_t;
-    const char *row_d = has_d ? static_cast<const char *>(P.draft) + ((size_t)b * P.K + j) * (size_t)P.Vd * P.es_d
-                              : nullptr;
-    const bool bulk = P.bulk_t && (!has_d || P.bulk_d);
-    const int e_begin = k * P.rspt * RSE;
-    const int e_end = min(P.V, e_begin + P.rspt * RSE);
-    for (int e0 = e_begin; e0 < e_end; e0 += RSE) {
-        const int n = min(RSE, e_end - e0);
-        if (!ring_acquire(P, sh, r))
-            return false;
-        Meta &m = sh.meta[r.slot];
-        m.kind = K_RES;
-        m.b = b;
-        m.pos = j;
-        m.k = k;
-        m.e0 = e0;
-        m.n = n;
-        m.last = (e0 + RSE >= e_end);
-        m.direct = !bulk;
-        m.g0 = row_t + (size_t)e0 * P.es_t;
-        m.g1 = has_d ? row_d + (size_t)e0 * P.es_d : nullptr;
-        ring_publish(sh, ring, r, bulk, m.g0, (uint32_t)(n * P.es_t), m.g1,
-                     has_d ? (uint32_t)(n * P.es_d) : 0u);
-        ring_advance(r);
-    }
-    return true;
-}
-
-template <class E, int MODE, bool PROBS>
-__device__ void producer(const Params &P, Shared &sh, uint8_t *ring)
-{
-    Ring r;
-    uint32_t ticket = P.n_res ? atomicAdd(&P.ctl[CTL_RES_TICKET], 1u) : 0xffffffffu;
-    // The next stats task id is always fetched one task ahead, so the atomic's
-    // round trip overlaps the issue of the current task.
-    uint32_t t_next = atomicAdd(&P.ctl[CTL_STATS_NEXT], 1u);
-    bool stats_left = true, ok = true;
-    uint32_t idle = 0;
-    const uint32_t per_pos = (uint32_t)P.B * (uint32_t)P.npt;
-    while (ok) {
-        if (sh.abort) {
-            ok = false;
-            break;
-        }
-        const uint32_t t = t_next;
-        const bool have_t = stats_left && t < P.n_stats;
-        int pos = 0, b = 0, k = 0;
-        if (have_t) {
-            if (t < (uint32_t)P.K * per_pos) {
-                pos = (int)(t / per_pos);
-                const uint32_t rr = t % per_pos;
-                b = (int)(rr / (uint32_t)P.npt);
-                k = (int)(rr % (uint32_t)P.npt);
-            } else {
-                const uint32_t rr = t - (uint32_t)P.K * per_pos;
-                pos = P.K;
-                b = (int)(rr / (uint32_t)P.nct);
-                k = (int)(rr % (uint32_t)P.nct);
-            }
-        }
-        // Both loads go out back to back; one round trip covers them.
-        const bool want_res = ticket < P.n_res;
-        const int b1 = want_res ? ld_acquire(&P.res_seq[ticket / (uint32_t)P.ncr]) : 0;
-        const bool check_dead = have_t && pos > 0 && !P.full;
-        const unsigned long long st = check_dead ? ld_vol(&P.state[b]) : 0ull;
-
-        // 1. residual work for our ticket, once its sequence has ended (first,
-        //    so that the rows it re-reads are still in L2)
-        if (b1 > 0) {
-            const int rb = b1 - 1, kres = (int)(ticket % (uint32_t)P.ncr);
-            ticket = atomicAdd(&P.ctl[CTL_RES_TICKET], 1u);
-            const int j = ld_vol(&P.terminal[rb]);
-            if (j >= 0)
-                ok = issue_residual<E, MODE, PROBS>(P, sh, ring, r, rb, j, kres);
-            idle = 0;
-            continue;
-        }
-        // 2. the next stats task, left to right by position; skipped when its
-        //    sequence already ended before this position
-        if (have_t) {
-            t_next = atomicAdd(&P.ctl[CTL_STATS_NEXT], 1u);
-            int j;
-            if (check_dead && resolved(st, j) && j < pos)
-                continue;
-            ok = issue_stats<E, MODE, PROBS>(P, sh, ring, r, b, pos, k);
-            idle = 0;
-            continue;
-        }
-        stats_left = false;
-        if (!want_res)
-            break;
-        if (ld_vol(&P.ctl[CTL_STATUS]) == (uint32_t)ST_TIMEOUT || ++idle > P.spin_limit) {
-            ok = false;
-            break;
-        }
-        __nanosleep(256);
-    }
-    if (ok && ring_acquire(P, sh, r)) {
-        sh.meta[r.slot].kind = K_EXIT;
-        mbar_arrive(&sh.full[r.slot]);
-        return;
-    }
-    // Winding down: make the other warps leave, then wait for our own copies.
-    abort_cta(P, sh);
-    for (int s = 0; s < NST; ++s)
-        if (r.txmask & (1u << s))
-            mbar_wait(&sh.full[s], (r.phmask >> s) & 1u, DRAIN_LIMIT, nullptr);
-}
-
-// =================================================================== consumers
+// =================================================================== stage math
 struct Acc {
     float m;     // running max (raw logits) / greedy best value
-    float s;     // running sum relative to m
+    float s;     // running sum of 2^((x - m) c)
     int idx;     // greedy best index
-    int flag;
+    int flag;    // bit 0: NaN / +inf seen; bit 1: bad shortlist entry
 };
 
+// Four 16-byte vectors of a stats stage for this lane: vector v = lane + 32*(4h + k).
 template <class E>
-__device__ __forceinline__ void load_stage(const Meta &m, const uint8_t *st, int ctid, float *x)
+__device__ __forceinline__ void load_quad(const Meta &m, const uint8_t *st, int lane, int h, uint4 *v)
 {
     constexpr int VE = E::VE;
     if (!m.direct) {
@@ -585,71 +477,89 @@ __device__ __forceinline__ void load_stage(const Meta &m, const uint8_t *st, int
         const int nvec = m.n / VE;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int v = ctid + 256 * k;
-            const uint4 w = v < nvec ? sv[v] : E::neg_inf();
-            E::unpack(w, x + k * VE);
+            const int i = lane + 32 * (4 * h + k);
+            v[k] = i < nvec ? sv[i] : E::neg_inf();
         }
     } else {
+        // unaligned rows: element loads, -inf past the end (same bit layout as a vector)
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < 4; ++k) {
+            uint32_t w[4];
 #pragma unroll
-            for (int e = 0; e < VE; ++e) {
-                const int i = (ctid + 256 * k) * VE + e;
-                x[k * VE + e] = i < m.n ? E::load(m.g0, i) : -F_INF;
+            for (int q = 0; q < 4; ++q) {
+                if (E::ES == 4) {
+                    const int i = (lane + 32 * (4 * h + k)) * 4 + q;
+                    w[q] = i < m.n ? __float_as_uint(E::load(m.g0, i)) : 0xff800000u;
+                } else {
+                    const int i = (lane + 32 * (4 * h + k)) * 8 + 2 * q;
+                    const uint32_t lo = i < m.n ? (__float_as_uint(E::load(m.g0, i)) >> 16) : 0xff80u;
+                    const uint32_t hi = i + 1 < m.n ? (__float_as_uint(E::load(m.g0, i + 1)) >> 16) : 0xff80u;
+                    w[q] = lo | (hi << 16);
+                }
             }
+            v[k] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
     }
 }
 
-// Online max / sum of 2^((x - m) c) over the 4*VE elements of this thread.
-template <int NE>
-__device__ __forceinline__ void online_update(const float *x, float c, Acc &a)
+// Online max / sum of 2^((x - m) c) over the elements of four vectors:
+// packed bf16x2 max tree, f32x2 arithmetic, tree sums.
+template <class E>
+__device__ __forceinline__ void online_update(const uint4 *v, float c, Acc &a)
 {
-    float lm = x[0];
-#pragma unroll
-    for (int i = 1; i < NE; ++i)
-        lm = fmax_nan(lm, x[i]);
-    const float mn = fmax_nan(a.m, lm);
+    constexpr int NP = 2 * E::VE;   // element pairs in four vectors
+    const float mn = fmax_nan(a.m, E::quad_max(v));
     const float ref = (mn == -F_INF) ? 0.0f : mn;
     if (mn != a.m)
         a.s *= ex2a((a.m - ref) * c);
-    float t[NE];
+    const f2 nref = pk(-ref, -ref), cc = pk(c, c);
+    f2 e[NP];
 #pragma unroll
-    for (int i = 0; i < NE; ++i)
-        t[i] = ex2a((x[i] - ref) * c);
+    for (int p = 0; p < NP; ++p)
+        e[p] = ex2x2(mul2(add2(E::pair(v[p / (NP / 4)], p % (NP / 4)), nref), cc));
 #pragma unroll
-    for (int w = NE / 2; w >= 1; w >>= 1)
+    for (int w = NP / 2; w >= 1; w >>= 1)
 #pragma unroll
         for (int i = 0; i < w; ++i)
-            t[i] += t[i + w];
-    a.s += t[0];
+            e[i] = add2(e[i], e[i + w]);
+    float lo, hi;
+    upk(e[0], lo, hi);
+    a.s += lo + hi;
     a.m = mn;
 }
 
+// Running (max, lowest index): a vector's elements are examined one by one
+// only when its maximum beats the lane's best so far (rare after the start).
 template <class E>
-__device__ __forceinline__ void greedy_update(const float *x, const Meta &m, int ctid, Acc &a)
+__device__ __forceinline__ void greedy_update(const uint4 *v, const Meta &m, int lane, int h, Acc &a)
 {
     constexpr int VE = E::VE;
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+    for (int k = 0; k < 4; ++k) {
+        const float vm = E::vec_max(v[k]);
+        if (vm != vm) {
+            a.flag |= 1;
+        } else if (vm > a.m) {
+            float x[VE];
+            E::unpack(v[k], x);
+            const int base = m.e0 + (lane + 32 * (4 * h + k)) * VE;
 #pragma unroll
-        for (int e = 0; e < VE; ++e) {
-            const float v = x[k * VE + e];
-            a.flag |= (v != v);
-            if (v > a.m) {
-                a.m = v;
-                a.idx = m.e0 + (ctid + 256 * k) * VE + e;
-            }
+            for (int e = VE - 1; e >= 0; --e)
+                if (x[e] == vm)
+                    a.idx = base + e;
+            a.m = vm;
         }
+    }
 }
 
 // Shortlist: check entries [e0, e0+n) of sequence b's index row (ascending,
 // unique, inside [0, V)); at position 0 also record, for each 256-token
 // segment t, the first entry whose token is >= 256 t.
-static __device__ void shortlist_scan(const Params &P, const Meta &m, int ctid, bool record, int &flag)
+static __device__ void shortlist_scan(const Params &P, const Meta &m, int lane, bool record, int &flag)
 {
     const int32_t *idx = P.shortlist + (size_t)m.b * P.S;
     int32_t *lb = P.sl_lb + (size_t)m.b * (P.nseg + 1);
-    for (int s = m.e0 + ctid; s < m.e0 + m.n; s += 256) {
+    for (int s = m.e0 + lane; s < m.e0 + m.n; s += 32) {
         const int cur = __ldg(idx + s);
         const int prev = s > 0 ? __ldg(idx + s - 1) : -1;
         if (cur < 0 || cur >= P.V || cur <= prev) {
@@ -678,35 +588,95 @@ __device__ __forceinline__ ResCoef load_coef(const Params &P, int b, int j)
     const float4 v = __ldcg(reinterpret_cast<const float4 *>(P.dec + (size_t)b * (P.K + 1) + j));
     return ResCoef{v.x, v.y, v.z, v.w, P.c};
 }
-// r(x) for one token: target logit xt, draft value xd (logit, or probability
-// when PROBS); q receives q(x).  `bonus` samples q itself.
+// r(x) and q(x) for 8 tokens given as 4 target pairs XT and 4 draft pairs XD
+// (draft logits, or probabilities when PROBS); `bonus` samples q itself.
+//   q = 2^((xt - Mt) c - log2 St)
+//   delta = log2(p / q) = (xd - xt) c - dL, and r = q (1 - 2^delta) for delta < 0,
+// where 1 - 2^delta comes from -expm1(delta ln 2) as a degree-8 Taylor
+// polynomial on (-1, 0) (no cancellation near 0; truncation below 1.5e-7
+// relative) and from 1 - ex2(delta) below -1.  Tokens with xt = -inf give 0.
 template <bool PROBS>
-__device__ __forceinline__ float res_elem(float xt, float xd, const ResCoef &k, bool bonus, float &q)
+__device__ __forceinline__ void res8(const f2 *XT, const f2 *XD, const ResCoef &k, bool bonus, f2 *R, f2 *Q)
 {
-    if (xt == -F_INF) {
-        q = 0.0f;
-        return 0.0f;
+    const f2 nMt = pk(-k.Mt, -k.Mt), cc = pk(k.c, k.c), nLt = pk(-k.Lt2, -k.Lt2);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const f2 q = ex2x2(fma2(add2(XT[p], nMt), cc, nLt));
+        Q[p] = q;
+        if (bonus) {
+            R[p] = q;
+        } else if (PROBS) {
+            float q0, q1, p0, p1;
+            upk(q, q0, q1);
+            upk(XD[p], p0, p1);
+            R[p] = pk(fmaxf(q0 - p0, 0.0f), fmaxf(q1 - p1, 0.0f));
+        } else {
+            const f2 dd = fma2(XT[p], pk(-1.0f, -1.0f), XD[p]);                             // xd - xt
+            const f2 dl = add2(fma2(dd, cc, pk(-k.dLhi, -k.dLhi)), pk(-k.dLlo, -k.dLlo));   // delta
+            float d0, d1;
+            upk(dl, d0, d1);
+            d0 = fminf(d0, 0.0f);   // also maps NaN (both logits -inf) to 0
+            d1 = fminf(d1, 0.0f);
+            const f2 t = mul2(pk(fmaxf(d0, -1.0f), fmaxf(d1, -1.0f)), pk(0.69314718055994531f, 0.69314718055994531f));
+            f2 P = pk(-1.0f / 40320.0f, -1.0f / 40320.0f);
+            P = fma2(P, t, pk(-1.0f / 5040.0f, -1.0f / 5040.0f));
+            P = fma2(P, t, pk(-1.0f / 720.0f, -1.0f / 720.0f));
+            P = fma2(P, t, pk(-1.0f / 120.0f, -1.0f / 120.0f));
+            P = fma2(P, t, pk(-1.0f / 24.0f, -1.0f / 24.0f));
+            P = fma2(P, t, pk(-1.0f / 6.0f, -1.0f / 6.0f));
+            P = fma2(P, t, pk(-0.5f, -0.5f));
+            P = fma2(P, t, pk(-1.0f, -1.0f));
+            float o0, o1;
+            upk(mul2(t, P), o0, o1);              // 1 - 2^delta on [-1, 0]
+            if (d0 <= -1.0f)
+                o0 = 1.0f - ex2a(d0);
+            if (d1 <= -1.0f)
+                o1 = 1.0f - ex2a(d1);
+            R[p] = mul2(q, pk(o0, o1));
+        }
     }
-    q = ex2a((xt - k.Mt) * k.c - k.Lt2);
-    if (bonus)
-        return q;
-    if (PROBS) {
-        const float d = q - xd;
-        return d > 0.0f ? d : 0.0f;
-    }
-    const float delta = ((xd - xt) * k.c - k.dLhi) - k.dLlo;   // log2(p(x) / q(x))
-    return delta < 0.0f ? q * one_minus_pow2(delta) : 0.0f;
 }
 
-// Draft values of the 8 tokens [x0 + 8 lane, +8) of a 256-token segment.
-// Full vocabulary: from the stage (bulk) or global memory.  Shortlist: scatter
-// the segment's entries into a per-warp buffer first (absent tokens read as
-// -inf logits / zero probabilities, i.e. p = 0).
+// Target pairs XT and draft pairs XD of the 8 tokens [x0 + 8 lane, +8) of a
+// 256-token segment: from the stage (bulk copies) or global memory; with a
+// shortlist, the segment's entries are first scattered into a per-warp buffer
+// (absent tokens read as -inf logits / zero probabilities, i.e. p = 0).
+// Tokens past the row end read as -inf targets (so r = q = 0).
 template <class E, int MODE, bool PROBS>
-__device__ __forceinline__ void draft_values(const Params &P, int b, int j, int x0, int lane, int cnt,
-                                             const uint8_t *st_d, const void *g_d, bool direct,
-                                             float *pscr, float *xd, int &flag)
+__device__ __forceinline__ void seg_inputs(const Params &P, int b, int j, int x0, int cnt, int lane,
+                                           const uint8_t *st_t, const void *g_t, const uint8_t *st_d,
+                                           const void *g_d, bool direct, float *pscr, f2 *XT, f2 *XD, int &flag)
 {
+    if (!direct && cnt == 8) {
+        const uint4 *sv = reinterpret_cast<const uint4 *>(st_t + (size_t)lane * 8 * E::ES);
+        if (E::VE == 8) {
+            const uint4 v = sv[0];
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+                XT[p] = E::pair(v, p);
+        } else {
+            const uint4 v0 = sv[0], v1 = sv[1];
+            XT[0] = E::pair(v0, 0);
+            XT[1] = E::pair(v0, 1);
+            XT[2] = E::pair(v1, 0);
+            XT[3] = E::pair(v1, 1);
+        }
+    } else {
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            x[e] = e < cnt ? E::load(g_t, (size_t)lane * 8 + e) : -F_INF;
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+            XT[p] = pk(x[2 * p], x[2 * p + 1]);
+    }
+    if (j == P.K) {   // bonus: q only
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+            XD[p] = 0ull;
+        return;
+    }
+    float xd[8];
     if (MODE == MODE_SHORT) {
         const float absent = PROBS ? 0.0f : -F_INF;
 #pragma unroll
@@ -733,18 +703,14 @@ __device__ __forceinline__ void draft_values(const Params &P, int b, int j, int 
         __syncwarp();
     } else {
         using D = typename std::conditional<PROBS, F32, E>::type;
-        if (!direct) {
-            float tmp[8];
+        if (!direct && cnt == 8) {
             const uint4 *sv = reinterpret_cast<const uint4 *>(st_d + (size_t)lane * 8 * D::ES);
             if (D::VE == 8) {
-                D::unpack(sv[0], tmp);
+                D::unpack(sv[0], xd);
             } else {
-                D::unpack(sv[0], tmp);
-                D::unpack(sv[1], tmp + 4);
+                D::unpack(sv[0], xd);
+                D::unpack(sv[1], xd + 4);
             }
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                xd[e] = tmp[e];
         } else {
 #pragma unroll
             for (int e = 0; e < 8; ++e)
@@ -755,187 +721,21 @@ __device__ __forceinline__ void draft_values(const Params &P, int b, int j, int 
             for (int e = 0; e < 8; ++e)
                 flag |= e < cnt && !(xd[e] >= 0.0f && xd[e] != F_INF);
     }
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+        XD[p] = pk(xd[2 * p], xd[2 * p + 1]);
 }
 
-// r and q for the 8 tokens starting at x0 + 8*lane of one segment, the
-// lane's sums (in token order) and the last token with r > 0.
-template <class E, int MODE, bool PROBS>
-__device__ __forceinline__ void residual_lane(const Params &P, int b, int j, int x0, int cnt, int lane,
-                                              const uint8_t *st_t, const void *g_t, const uint8_t *st_d,
-                                              const void *g_d, bool direct, float *pscr,
-                                              const ResCoef &kc, float *r, float &rsum, float &qsum,
-                                              int &last, int &flag)
+// Sum of the 8 values of 4 pairs: (v0 + v4) + (v2 + v6) + ... as a fixed tree.
+__device__ __forceinline__ float sum8(const f2 *V)
 {
-    const bool bonus = (j == P.K);
-    float xt[8], xd[8];
-    if (!direct && cnt == 8) {
-        const uint4 *sv = reinterpret_cast<const uint4 *>(st_t + (size_t)lane * 8 * E::ES);
-        if (E::VE == 8) {
-            E::unpack(sv[0], xt);
-        } else {
-            E::unpack(sv[0], xt);
-            E::unpack(sv[1], xt + 4);
-        }
-    } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            xt[e] = e < cnt ? E::load(g_t, (size_t)lane * 8 + e) : -F_INF;
-    }
-    if (!bonus) {
-        draft_values<E, MODE, PROBS>(P, b, j, x0, lane, cnt, st_d, g_d, direct || cnt != 8, pscr, xd, flag);
-    } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            xd[e] = 0.0f;
-    }
-    rsum = 0.0f;
-    qsum = 0.0f;
-    last = -1;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        float q = 0.0f;
-        r[e] = 0.0f;
-        if (e < cnt)
-            r[e] = res_elem<PROBS>(xt[e], xd[e], kc, bonus, q);
-        rsum += r[e];
-        qsum += q;
-        if (r[e] > 0.0f)
-            last = x0 + lane * 8 + e;
-    }
+    const f2 s = add2(add2(V[0], V[2]), add2(V[1], V[3]));
+    float lo, hi;
+    upk(s, lo, hi);
+    return lo + hi;
 }
 
-// Hand the warp's task result to the finisher.
-__device__ __forceinline__ bool hand_over(const Params &P, Shared &sh, int cw, int lane, uint32_t &hs,
-                                          uint32_t &hph, int kind, const Meta &m, float wm, DF ws,
-                                          int wf, int wi)
-{
-    if (!warp_wait(&sh.hempty[hs], hph ^ 1u, P.spin_limit, &sh.abort, lane))
-        return false;
-    if (lane == 0) {
-        Hand &h = sh.hand[hs];
-        if (cw == 0) {
-            h.kind = kind;
-            h.b = m.b;
-            h.pos = m.pos;
-            h.k = m.k;
-        }
-        h.wm[cw] = wm;
-        h.ws_hi[cw] = ws.hi;
-        h.ws_lo[cw] = ws.lo;
-        h.wf[cw] = wf;
-        h.wi[cw] = wi;
-        mbar_arrive(&sh.hfull[hs]);
-    }
-    __syncwarp();
-    if (++hs == NH) {
-        hs = 0;
-        hph ^= 1u;
-    }
-    return true;
-}
-
-template <class E, int MODE, bool PROBS>
-__device__ void consumer(const Params &P, Shared &sh, const uint8_t *ring, int cw, int lane)
-{
-    constexpr int NE = 4 * E::VE;
-    const int ctid = cw * 32 + lane;
-    uint32_t slot = 0, ph = 0, hs = 0, hph = 0;
-    Acc a{-F_INF, 0.0f, 0x7fffffff, 0};
-    for (;;) {
-        if (!warp_wait(&sh.full[slot], ph, P.spin_limit, &sh.abort, lane)) {
-            abort_cta(P, sh);
-            return;
-        }
-        const Meta m = sh.meta[slot];
-        const uint8_t *st = ring + (size_t)slot * STAGE_BYTES;
-        if (m.kind == K_EXIT) {
-            hand_over(P, sh, cw, lane, hs, hph, K_EXIT, m, 0.0f, DF{0.0f, 0.0f}, 0, 0);
-            return;
-        }
-        if (m.kind == K_RES) {
-            // one 256-token segment per warp
-            int flag = 0;
-            const int eb = cw * SEG;
-            if (eb < m.n) {
-                const int x0 = m.e0 + eb;
-                const int cnt = max(0, min(8, m.n - eb - lane * 8));
-                const ResCoef kc = load_coef(P, m.b, m.pos);
-                float r[8], rsum, qsum;
-                int last;
-                const void *g_t = static_cast<const char *>(m.g0) + (size_t)eb * P.es_t;
-                const void *g_d = m.g1 ? static_cast<const char *>(m.g1) + (size_t)eb * P.es_d : nullptr;
-                residual_lane<E, MODE, PROBS>(P, m.b, m.pos, x0, cnt, lane, st + (size_t)eb * P.es_t, g_t,
-                                              st + RD_OFF + (size_t)eb * P.es_d, g_d, m.direct != 0,
-                                              sh.pscr[cw], kc, r, rsum, qsum, last, flag);
-                rsum = warp_sumf(rsum);
-                qsum = warp_sumf(qsum);
-                last = warp_maxi(last);
-                flag = warp_or(flag);
-                if (lane == 0) {
-                    const size_t si = (size_t)m.b * P.nseg + x0 / SEG;
-                    P.seg[si] = SegMass{rsum, qsum};
-                    P.seglast[si] = last;
-                }
-            }
-            a.flag |= flag;
-        } else {
-            float x[NE];
-            if (m.kind == K_STAT_D && PROBS) {
-                // draft probabilities have no stats pass
-            } else if (m.kind == K_STAT_D) {
-                load_stage<E>(m, st, ctid, x);
-                online_update<NE>(x, P.c, a);
-            } else {
-                load_stage<E>(m, st, ctid, x);
-                if (MODE == MODE_GREEDY)
-                    greedy_update<E>(x, m, ctid, a);
-                else
-                    online_update<NE>(x, P.c, a);
-            }
-            if (MODE == MODE_SHORT && m.kind == K_STAT_D && (m.pos == 0 || P.full))
-                shortlist_scan(P, m, ctid, m.pos == 0, a.flag);
-        }
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(&sh.empty[slot]);
-        if (m.last) {
-            bool hok;
-            if (m.kind == K_RES) {
-                hok = hand_over(P, sh, cw, lane, hs, hph, K_RES, m, 0.0f, DF{0.0f, 0.0f}, warp_or(a.flag), 0);
-            } else if (MODE == MODE_GREEDY) {
-                float v = a.m;
-                int i = a.idx;
-#pragma unroll
-                for (int o = 16; o; o >>= 1) {
-                    const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
-                    const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
-                    argmax_merge(v, i, v2, i2);
-                }
-                const int fl = warp_or(a.flag | (a.m == F_INF));
-                hok = hand_over(P, sh, cw, lane, hs, hph, m.kind, m, v, DF{0.0f, 0.0f}, fl, i);
-            } else {
-                const float wm = warp_max_nan(a.m);
-                const int fl = warp_or(a.flag | (a.m != a.m) | (a.m == F_INF));
-                DF contrib{0.0f, 0.0f};
-                if (a.m > -F_INF && a.s > 0.0f)
-                    contrib = df_scale_pow2(DF{a.s, 0.0f}, (a.m - wm) * P.c);
-                const DF ws = warp_sum_df(contrib);
-                hok = hand_over(P, sh, cw, lane, hs, hph, m.kind, m, wm, ws, fl, 0);
-            }
-            if (!hok) {
-                abort_cta(P, sh);
-                return;
-            }
-            a = Acc{-F_INF, 0.0f, 0x7fffffff, 0};
-        }
-        if (++slot == NST) {
-            slot = 0;
-            ph ^= 1u;
-        }
-    }
-}
-
-// =================================================================== finisher
+// =================================================================== decisions
 static __device__ void emit_tokens(const Params &P, int b, int j, int last_token)
 {
     int32_t *out = P.out_tokens + (size_t)b * (P.K + 1);
@@ -989,9 +789,15 @@ __device__ void resolve(const Params &P, int b, int j)
         st_vol(&P.fin[b], 1);
     }
     if (MODE != MODE_GREEDY) {
-        __threadfence();
         const uint32_t slot = atomicAdd(&P.ctl[CTL_RES_COUNT], 1u);
-        st_vol(&P.res_seq[slot], b + 1);
+        ResRec *rec = P.res_rec + slot;
+        rec->j = code ? -1 : j;
+        if (!code) {
+            const float4 dc = __ldcg(reinterpret_cast<const float4 *>(P.dec + (size_t)b * (P.K + 1) + j));
+            *reinterpret_cast<float4 *>(rec->rc) = dc;
+        }
+        __threadfence();
+        st_vol(&rec->b1, b + 1);
     }
 }
 
@@ -1165,7 +971,7 @@ __device__ void decide(const Params &P, int b, int pos, int lane)
 // Inverse-CDF sample of the ended sequence b (ended at j) from its segment
 // masses: float64 scan over segments, then a scan inside one segment.
 template <class E, int MODE, bool PROBS>
-__device__ void locate(const Params &P, Shared &sh, int b, int j, int lane)
+__device__ void locate(const Params &P, float *pscr, int b, int j, int lane)
 {
     const int nseg = P.nseg;
     const SegMass *sg = P.seg + (size_t)b * nseg;
@@ -1231,30 +1037,17 @@ __device__ void locate(const Params &P, Shared &sh, int b, int j, int lane)
         const bool has_d = (MODE == MODE_STOCH) && j < P.K;
         const char *row_d = has_d ? static_cast<const char *>(P.draft) + ((size_t)b * P.K + j) * (size_t)P.Vd * P.es_d
                                   : nullptr;
-        float r[8], rsum, qsum;
-        int last, flag = 0;
-        residual_lane<E, MODE, PROBS>(P, b, j, x0, cnt, lane, nullptr, row_t + (size_t)x0 * P.es_t, nullptr,
-                                      has_d ? row_d + (size_t)x0 * P.es_d : nullptr, true, sh.pscr[NCW], kc, r,
-                                      rsum, qsum, last, flag);
+        f2 XT[4], XD[4], R[4], Q[4];
+        int flag = 0;
+        seg_inputs<E, MODE, PROBS>(P, b, j, x0, cnt, lane, nullptr, row_t + (size_t)x0 * P.es_t, nullptr,
+                                   has_d ? row_d + (size_t)x0 * P.es_d : nullptr, true, pscr, XT, XD, flag);
+        res8<PROBS>(XT, XD, kc, j == P.K, R, Q);
+        const f2 *W = use_q ? Q : R;
         float qv[8];
-        if (use_q) {
-            // sample q itself: recompute q per token
-            rsum = 0.0f;
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                float q = 0.0f;
-                if (e < cnt) {
-                    const float xt = E::load(row_t + (size_t)x0 * P.es_t, (size_t)lane * 8 + e);
-                    res_elem<PROBS>(xt, 0.0f, kc, true, q);
-                }
-                qv[e] = q;
-                rsum += q;
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                qv[e] = r[e];
-        }
+        for (int p = 0; p < 4; ++p)
+            upk(W[p], qv[2 * p], qv[2 * p + 1]);
+        const float rsum = sum8(W);
         int lastpos = -1;
 #pragma unroll
         for (int e = 0; e < 8; ++e)
@@ -1288,8 +1081,33 @@ __device__ void locate(const Params &P, Shared &sh, int b, int j, int lane)
         // no segment found (rounding): the largest token with positive mass
         int cand = -1;
         for (int s = s0; s < s1; ++s)
-            cand = max(cand, ld_vol(&P.seglast[(size_t)b * nseg + s]));
-        x = warp_maxi(cand);
+            if ((use_q ? ld_vol(&sg[s].q) : ld_vol(&sg[s].r)) > 0.0f)
+                cand = s;
+        cand = warp_maxi(cand);
+        if (cand >= 0) {
+            const int x0 = cand * SEG;
+            const int cnt = max(0, min(8, P.V - x0 - lane * 8));
+            const ResCoef kc = load_coef(P, b, j);
+            const char *row_t = static_cast<const char *>(P.target) + ((size_t)b * (P.K + 1) + j) * (size_t)P.V * P.es_t;
+            const bool has_d = (MODE == MODE_STOCH) && j < P.K;
+            const char *row_d = has_d ? static_cast<const char *>(P.draft) + ((size_t)b * P.K + j) * (size_t)P.Vd * P.es_d
+                                      : nullptr;
+            f2 XT[4], XD[4], R[4], Q[4];
+            int flag = 0;
+            seg_inputs<E, MODE, PROBS>(P, b, j, x0, cnt, lane, nullptr, row_t + (size_t)x0 * P.es_t, nullptr,
+                                       has_d ? row_d + (size_t)x0 * P.es_d : nullptr, true, pscr, XT, XD, flag);
+            res8<PROBS>(XT, XD, kc, j == P.K, R, Q);
+            float v8[8];
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+                upk(use_q ? Q[p] : R[p], v8[2 * p], v8[2 * p + 1]);
+            int lp = -1;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (v8[e] > 0.0f)
+                    lp = x0 + lane * 8 + e;
+            x = warp_maxi(lp);
+        }
         if (x < 0)
             x = P.V - 1;
     }
@@ -1302,14 +1120,276 @@ __device__ void locate(const Params &P, Shared &sh, int b, int j, int lane)
     }
 }
 
-// Merge the 8 warp results of a stats hand-off into one chunk partial.
-template <int MODE>
-__device__ __forceinline__ Partial merge_hand(const Params &P, const Hand &h, int lane)
+// =================================================================== worker
+// Stats work comes in units of one stage (one 4 KB chunk of one row), ordered
+// (position, sequence, chunk), target chunks before draft chunks.  A worker's
+// first batch of units is fixed by its index; later batches come from a global
+// counter, up to 8 units per atomic, fewer as the work runs out.  Consecutive
+// units of one row in a batch form a run, reduced into one partial.
+
+// What lane 0 streams next: one stats unit, or the stages of one residual task.
+struct Cursor {
+    int kind, b, pos, kf, ku, e, e_end, se, es0, es1;
+    bool bulk, run_last;
+    const char *row0, *row1;
+    float4 rc;
+};
+
+// Lane 0's work queue.
+struct Queue {
+    uint32_t u, ue;                // current batch [u, ue)
+    int upos, ub, uk;              // decoded form of unit u (stepped, not divided, within a batch)
+    uint32_t pc, pG;               // counter value and size of the next batch (atomic in flight)
+    int run_pos, run_b, run_t, run_kf;   // the current run
+    bool in_run, run_dead;
+    uint32_t ticket, tnext;        // residual ticket; counter value for the next one
+    int pf_b1, pf_j;               // the ticket's slot record, loaded one batch boundary ahead
+    float4 pf_rc;
+    bool stats_left;
+};
+
+// Lane 0: load the ticket's slot record (flag first, with acquire).
+__device__ __forceinline__ void prefetch_slot(const Params &P, Queue &q)
 {
+    if (q.ticket < P.n_res) {
+        const ResRec *rec = P.res_rec + q.ticket / (uint32_t)P.ncr;
+        q.pf_b1 = ld_acquire(&rec->b1);
+        q.pf_j = __ldcg(&rec->j);
+        q.pf_rc = __ldcg(reinterpret_cast<const float4 *>(rec->rc));
+    }
+}
+
+__device__ __forceinline__ void decode_unit(const Params &P, uint32_t t, int &pos, int &b, int &k)
+{
+    const uint32_t per_pos = (uint32_t)P.B * (uint32_t)P.npt;
+    if (t < (uint32_t)P.K * per_pos) {
+        pos = (int)(t / per_pos);
+        const uint32_t rr = t % per_pos;
+        b = (int)(rr / (uint32_t)P.npt);
+        k = (int)(rr % (uint32_t)P.npt);
+    } else {
+        const uint32_t rr = t - (uint32_t)P.K * per_pos;
+        pos = P.K;
+        b = (int)(rr / (uint32_t)P.nct);
+        k = (int)(rr % (uint32_t)P.nct);
+    }
+}
+
+// Units to ask for next: a third of a per-worker share of what is left, 1..32.
+__device__ __forceinline__ uint32_t guided(const Params &P, uint32_t seen)
+{
+    const uint32_t left = P.n_stats > seen ? P.n_stats - seen : 0u;
+    return max(1u, min(16u, left / (3u * P.workers)));
+}
+
+// The unit after (pos, b, k) in the static order.
+__device__ __forceinline__ void step_unit(const Params &P, int &pos, int &b, int &k)
+{
+    if (++k == (pos < P.K ? P.npt : P.nct)) {
+        k = 0;
+        if (++b == P.B) {
+            b = 0;
+            ++pos;
+        }
+    }
+}
+
+// Lane 0: move to the next batch and ask the counter for the one after it.
+__device__ __forceinline__ void next_batch(const Params &P, Queue &q)
+{
+    q.u = P.first_units + q.pc;
+    q.ue = min(q.u + q.pG, P.n_stats);
+    if (q.u < q.ue)
+        decode_unit(P, q.u, q.upos, q.ub, q.uk);
+    q.pG = guided(P, q.u);
+    q.pc = atomicAdd(&P.ctl[CTL_STATS_NEXT], q.pG);
+}
+
+__device__ __forceinline__ void set_unit_cursor(const Params &P, Cursor &c, int b, int pos, int k, int kf,
+                                                bool run_last)
+{
+    const bool is_t = k < P.nct;
+    const int kk = is_t ? k : k - P.nct;
+    c.kind = is_t ? K_STAT_T : K_STAT_D;
+    c.b = b;
+    c.pos = pos;
+    c.kf = kf;
+    c.ku = k;
+    c.es0 = is_t ? P.es_t : P.es_d;
+    c.es1 = 0;
+    c.se = is_t ? P.se_t : P.se_d;
+    const int n_row = is_t ? P.V : P.Vd;
+    c.bulk = is_t ? P.bulk_t : P.bulk_d;
+    c.row0 = is_t ? static_cast<const char *>(P.target) + ((size_t)b * (P.K + 1) + pos) * (size_t)P.V * P.es_t
+                  : static_cast<const char *>(P.draft) + ((size_t)b * P.K + pos) * (size_t)P.Vd * P.es_d;
+    c.row1 = nullptr;
+    c.e = kk * c.se;
+    c.e_end = min(n_row, c.e + c.se);
+    c.run_last = run_last;
+}
+
+template <int MODE>
+__device__ void set_res_cursor(const Params &P, Cursor &c, int b, int j, int k, float4 rc)
+{
+    const bool has_d = (MODE == MODE_STOCH) && j < P.K;
+    c.kind = K_RES;
+    c.b = b;
+    c.pos = j;
+    c.kf = k;
+    c.ku = k;
+    c.es0 = P.es_t;
+    c.es1 = has_d ? P.es_d : 0;
+    c.se = P.rse;
+    c.bulk = P.bulk_t && (!has_d || P.bulk_d);
+    c.row0 = static_cast<const char *>(P.target) + ((size_t)b * (P.K + 1) + j) * (size_t)P.V * P.es_t;
+    c.row1 = has_d ? static_cast<const char *>(P.draft) + ((size_t)b * P.K + j) * (size_t)P.Vd * P.es_d : nullptr;
+    c.rc = rc;
+    c.e = k * P.rspt * P.rse;
+    c.e_end = min(P.V, c.e + P.rspt * P.rse);
+    c.run_last = true;
+}
+
+// Lane 0: the next unit or residual task for this worker, or false when none
+// is available now.  Residual work is looked for between batches (and while
+// idle), from a load issued one batch earlier.
+template <int MODE>
+__device__ bool pop_task(const Params &P, Queue &q, Cursor &c)
+{
+    for (;;) {
+        if (q.u >= q.ue) {
+            // 1. residual work for our ticket, once its sequence has ended (first,
+            //    so that the rows it re-reads are still in L2)
+            if (q.ticket < P.n_res && q.pf_b1 > 0) {
+                const int b = q.pf_b1 - 1, j = q.pf_j, kres = (int)(q.ticket % (uint32_t)P.ncr);
+                const float4 rc = q.pf_rc;
+                q.ticket = P.workers + q.tnext;
+                q.tnext = atomicAdd(&P.ctl[CTL_RES_TICKET], 1u);
+                q.pf_b1 = 0;
+                if (j < 0)
+                    continue;   // the sequence ended with an error: nothing to sample
+                set_res_cursor<MODE>(P, c, b, j, kres, rc);
+                return true;
+            }
+            prefetch_slot(P, q);   // used at the next boundary
+            // 2. the next batch of stats units
+            if (!q.stats_left)
+                return false;
+            next_batch(P, q);
+            q.in_run = false;
+            if (q.u >= P.n_stats) {
+                q.stats_left = false;
+                return false;
+            }
+        }
+        // the next stats unit, left to right by position
+        ++q.u;
+        const int pos = q.upos, b = q.ub, k = q.uk;
+        step_unit(P, q.upos, q.ub, q.uk);
+        const int is_t = k < P.nct;
+        if (!q.in_run || pos != q.run_pos || b != q.run_b || is_t != q.run_t) {
+            // a new run: skipped whole when its sequence ended before this position
+            q.in_run = true;
+            q.run_pos = pos;
+            q.run_b = b;
+            q.run_t = is_t;
+            q.run_kf = k;
+            q.run_dead = false;
+            if (!P.full && pos > 0) {
+                int j;
+                q.run_dead = resolved(ld_vol(&P.state[b]), j) && j < pos;
+            }
+        }
+        if (q.run_dead)
+            continue;
+        const bool run_last =
+            q.u >= q.ue || !(q.upos == pos && q.ub == b && (q.uk < P.nct) == is_t);
+        set_unit_cursor(P, c, b, pos, k, q.run_kf, run_last);
+        return true;
+    }
+}
+
+// Lane 0: issue the cursor's next stage into ring slot s.
+__device__ __forceinline__ void issue_stage(const Params &P, Meta &m, unsigned long long *bar, uint8_t *ring, int s,
+                                            Cursor &c, bool &tx)
+{
+    const int n = min(c.se, c.e_end - c.e);
+    m.kind = c.kind;
+    m.b = c.b;
+    m.pos = c.pos;
+    m.kf = c.kf;
+    m.ku = c.ku;
+    m.e0 = c.e;
+    m.n = n;
+    m.last = (c.e + c.se >= c.e_end) && c.run_last;
+    m.direct = !c.bulk;
+    m.g0 = c.row0 + (size_t)c.e * c.es0;
+    m.g1 = c.row1 ? c.row1 + (size_t)c.e * c.es1 : nullptr;
+    m.rc = c.rc;
+    if (c.bulk) {
+        const uint32_t b0 = (uint32_t)(n * c.es0), b1 = c.row1 ? (uint32_t)(n * c.es1) : 0u;
+        uint8_t *dst = ring + (size_t)s * SB;
+        // The slot's previous contents were read by this warp's lanes, whose
+        // values are all consumed before the warp gets here: no reader is
+        // left for the copy to overwrite.
+        mbar_arrive_tx(bar, b0 + b1);
+        bulk_g2s(dst, m.g0, b0, bar);
+        if (b1)
+            bulk_g2s(dst + P.rd_off, m.g1, b1, bar);
+        tx = true;
+    } else {
+        mbar_arrive(bar);
+        tx = false;
+    }
+    c.e += c.se;
+    if (c.e >= c.e_end)
+        c.kind = K_NONE;
+}
+
+// Residual stage: one 256-token segment at a time, the warp's lanes 8 tokens each.
+template <class E, int MODE, bool PROBS>
+__device__ __forceinline__ int residual_stage(const Params &P, const Meta &m, const uint8_t *st, float *pscr,
+                                              int lane)
+{
+    int flag = 0;
+    const ResCoef kc{m.rc.x, m.rc.y, m.rc.z, m.rc.w, P.c};
+    for (int eb = 0; eb < m.n; eb += SEG) {
+        const int x0 = m.e0 + eb;
+        const int cnt = max(0, min(8, m.n - eb - lane * 8));
+        const void *g_t = static_cast<const char *>(m.g0) + (size_t)eb * P.es_t;
+        const void *g_d = m.g1 ? static_cast<const char *>(m.g1) + (size_t)eb * P.es_d : nullptr;
+        f2 XT[4], XD[4], R[4], Q[4];
+        seg_inputs<E, MODE, PROBS>(P, m.b, m.pos, x0, cnt, lane, st + (size_t)eb * P.es_t, g_t,
+                                   st + P.rd_off + (size_t)eb * P.es_d, g_d, m.direct != 0, pscr, XT, XD, flag);
+        res8<PROBS>(XT, XD, kc, m.pos == P.K, R, Q);
+        const float rsum = warp_sumf(sum8(R));
+        const float qsum = warp_sumf(sum8(Q));
+        if (lane == 0)
+            P.seg[(size_t)m.b * P.nseg + x0 / SEG] = SegMass{rsum, qsum};
+    }
+    return warp_or(flag);
+}
+
+// Finished runs and residual tasks wait in a per-warp list (entry i held by
+// lane i) and are published together: their results are written, one fence,
+// then their counters are bumped in parallel.  The worker whose bump completes
+// a position decides it; the one completing a sequence's residual locates.
+constexpr int PEND = 1;
+
+struct Pend {
+    int kind, b, pos, kf, cnt;
     Partial out;
-    if (MODE == MODE_GREEDY) {
-        float v = lane < NCW ? h.wm[lane] : -F_INF;
-        int i = lane < NCW ? h.wi[lane] : 0x7fffffff;
+};
+
+// The finished run's (or residual task's) result, on every lane.
+template <int MODE>
+__device__ __forceinline__ Partial run_result(const Params &P, const Meta &m, const Acc &a, int rflag)
+{
+    Partial out{0.0f, 0, 0.0f, 0.0f};
+    if (m.kind == K_RES) {
+        out.flag = warp_or(rflag);
+    } else if (MODE == MODE_GREEDY) {
+        float v = a.m;
+        int i = a.idx;
 #pragma unroll
         for (int o = 16; o; o >>= 1) {
             const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
@@ -1317,156 +1397,237 @@ __device__ __forceinline__ Partial merge_hand(const Params &P, const Hand &h, in
             argmax_merge(v, i, v2, i2);
         }
         out.m = v;
+        out.flag = warp_or(a.flag | (a.m == F_INF));
         out.s_hi = __int_as_float(i);
-        out.s_lo = 0.0f;
     } else {
-        const float wm = lane < NCW ? h.wm[lane] : -F_INF;
-        const float M = warp_max_nan(wm);
-        DF c{0.0f, 0.0f};
-        if (lane < NCW && wm > -F_INF)
-            c = df_scale_pow2(DF{h.ws_hi[lane], h.ws_lo[lane]}, (wm - M) * P.c);
-        const DF t = warp_sum_df(c);
-        out.m = M;
-        out.s_hi = t.hi;
-        out.s_lo = t.lo;
+        const float wm = warp_max_nan(a.m);
+        DF contrib{0.0f, 0.0f};
+        if (a.m > -F_INF && a.s > 0.0f)
+            contrib = df_scale_pow2(DF{a.s, 0.0f}, (a.m - wm) * P.c);
+        const DF ws = warp_sum_df(contrib);
+        out.m = wm;
+        out.flag = warp_or(a.flag | (a.m != a.m) | (a.m == F_INF));
+        out.s_hi = ws.hi;
+        out.s_lo = ws.lo;
     }
-    out.flag = warp_or(lane < NCW ? h.wf[lane] : 0);
     return out;
 }
 
-// The finisher takes every hand-off that is ready (up to NH), merges them,
-// writes all their results, fences once, and bumps all their counters in
-// parallel (one lane per hand-off); the hand-offs whose counter completes a
-// position (or a sequence's residual) then decide (or locate).
 template <class E, int MODE, bool PROBS>
-__device__ void finisher(const Params &P, Shared &sh, int lane)
+__device__ void publish(const Params &P, const Pend *pend, int &npend, float *pscr, int lane)
 {
-    uint32_t hs = 0, hph = 0;
+    Pend pe{};
+    if (lane < npend)
+        pe = pend[lane];
+    const Partial neutral{-F_INF, 0, MODE == MODE_GREEDY ? __int_as_float(0x7fffffff) : 0.0f, 0.0f};
+    if (lane < npend) {
+        if (pe.kind == K_RES) {
+            if (pe.out.flag)
+                st_vol(&P.errres[pe.b], 1);
+        } else {
+            P.part[((size_t)pe.b * (P.K + 1) + pe.pos) * P.npt + pe.kf] = pe.out;
+        }
+    }
+    // neutral partials for the other units of each run
+    for (int e = 0; e < npend; ++e) {
+        const int kind = __shfl_sync(0xffffffffu, pe.kind, e), cnt = __shfl_sync(0xffffffffu, pe.cnt, e);
+        if (kind == K_RES || cnt <= 1)
+            continue;
+        const int b = __shfl_sync(0xffffffffu, pe.b, e), pos = __shfl_sync(0xffffffffu, pe.pos, e);
+        const int kf = __shfl_sync(0xffffffffu, pe.kf, e);
+        Partial *pp = P.part + ((size_t)b * (P.K + 1) + pos) * P.npt + kf;
+        for (int i = 1 + lane; i < cnt; i += 32)
+            pp[i] = neutral;
+    }
+    __threadfence();
+    bool last = false;
+    if (lane < npend) {
+        if (pe.kind == K_RES) {
+            last = atomicAdd(&P.res_cnt[pe.b], 1u) == (uint32_t)P.ncr - 1u;
+        } else {
+            const size_t bp = (size_t)pe.b * (P.K + 1) + pe.pos;
+            const uint32_t nparts = pe.pos < P.K ? (uint32_t)P.npt : (uint32_t)P.nct;
+            last = atomicAdd(&P.pair_cnt[bp], (uint32_t)pe.cnt) + (uint32_t)pe.cnt == nparts;
+        }
+    }
+    unsigned lastmask = __ballot_sync(0xffffffffu, last);
+    if (lastmask)
+        __threadfence();
+    while (lastmask) {
+        const int i = __ffs(lastmask) - 1;
+        lastmask &= lastmask - 1;
+        const int kind = __shfl_sync(0xffffffffu, pe.kind, i);
+        const int b = __shfl_sync(0xffffffffu, pe.b, i);
+        const int pos = __shfl_sync(0xffffffffu, pe.pos, i);
+        if (kind == K_RES)
+            locate<E, MODE, PROBS>(P, pscr, b, pos, lane);
+        else
+            decide<E, MODE, PROBS>(P, b, pos, lane);
+    }
+    npend = 0;
+}
+
+// Per-warp shared memory: the ring's barriers and stage descriptions, lane 0's
+// queue and cursor, the pending results and the shortlist scatter buffer.
+struct WorkerShared {
+    unsigned long long full[RS];
+    Meta meta[RS];
+    Queue q;
+    Cursor c;
+    Pend pend[PEND];
+    float pscr[SEG];
+};
+
+struct Shared {
+    WorkerShared w[NWARP];
+    int last_cta;
+};
+
+constexpr size_t SMEM_BYTES = (size_t)NWARP * RS * SB + sizeof(Shared);
+
+template <class E, int MODE, bool PROBS>
+__device__ void worker(const Params &P, WorkerShared &ws, uint8_t *ring, int wid, int lane)
+{
+    Queue &q = ws.q;
+    Cursor &c = ws.c;
+    uint32_t txmask = 0;   // lane 0: ring slots whose current stage is a bulk copy
+    if (lane == 0) {
+        c.kind = K_NONE;
+        // the first residual ticket and the first batch of units follow from the
+        // worker's index; the counters hand out what comes after them
+        q.ticket = (uint32_t)wid;
+        q.tnext = P.n_res ? atomicAdd(&P.ctl[CTL_RES_TICKET], 1u) : 0u;
+        q.pf_b1 = 0;
+        q.u = (uint32_t)wid * P.g0;
+        q.ue = min(q.u + P.g0, P.n_stats);
+        if (q.u < q.ue)
+            decode_unit(P, q.u, q.upos, q.ub, q.uk);
+        q.pG = guided(P, P.first_units);
+        q.pc = atomicAdd(&P.ctl[CTL_STATS_NEXT], q.pG);
+        q.in_run = false;
+        q.stats_left = true;
+    }
+    uint32_t issued = 0, consumed = 0, idle = 0;
+    // A residual task may come between two units of one stats run: the run's
+    // accumulator and the residual task's flag are kept apart.
+    Acc a{-F_INF, 0.0f, 0x7fffffff, 0};
+    int rflag = 0;
+    int npend = 0;
+    bool ok = true;
     for (;;) {
-        if (!warp_wait(&sh.hfull[hs], hph, P.spin_limit, &sh.abort, lane)) {
-            abort_cta(P, sh);
-            return;
-        }
-        int n = 1;
-        if (lane == 0) {
-            uint32_t s = hs, p = hph;
-            while (n < NH) {
-                if (++s == NH) {
-                    s = 0;
-                    p ^= 1u;
-                }
-                if (!mbar_test(&sh.hfull[s], p))
+        // top up the ring
+        int finished = 0;
+        if (lane == 0 && issued - consumed < (uint32_t)RS) {
+            Queue ql = q;     // register copies for the top-up; the compute phase
+            Cursor cl = c;    // below does not keep them live
+            while (issued - consumed < (uint32_t)RS) {
+                if (cl.kind == K_NONE && !pop_task<MODE>(P, ql, cl))
                     break;
-                ++n;
+                const int s = (int)(issued % RS);
+                bool tx;
+                issue_stage(P, ws.meta[s], &ws.full[s], ring, s, cl, tx);
+                txmask = tx ? (txmask | (1u << s)) : (txmask & ~(1u << s));
+                ++issued;
             }
+            finished = (issued == consumed) && !ql.stats_left && ql.ticket >= P.n_res;
+            q = ql;
+            c = cl;
         }
-        n = __shfl_sync(0xffffffffu, n, 0);
-        int my_kind = -1, my_b = 0, my_pos = 0, my_k = 0;
-        Partial my_out{0.0f, 0, 0.0f, 0.0f};
-        bool exit_seen = false;
-        int m = 0;
-        for (int i = 0; i < n; ++i) {
-            if (i > 0)
-                (void)mbar_test(&sh.hfull[hs], hph);   // this lane's own acquire of the completed phase
-            __syncwarp();
-            const Hand &h = sh.hand[hs];
-            const int kind = h.kind;
-            if (kind == K_EXIT) {
-                exit_seen = true;
+        issued = __shfl_sync(0xffffffffu, issued, 0);
+        finished = __shfl_sync(0xffffffffu, finished, 0);
+        if (issued == consumed) {
+            if (npend) {   // never idle or leave with results unpublished
+                publish<E, MODE, PROBS>(P, ws.pend, npend, ws.pscr, lane);
+                continue;
+            }
+            if (finished)
+                break;
+            // nothing in flight: wait for our residual slot to be published
+            int give_up = 0;
+            if (lane == 0) {
+                give_up = ++idle > P.spin_limit || ld_vol(&P.ctl[CTL_STATUS]) == (uint32_t)ST_TIMEOUT;
+                if (!give_up) {
+                    __nanosleep(256);
+                    Queue ql = q;
+                    prefetch_slot(P, ql);
+                    q = ql;
+                }
+            }
+            if (__shfl_sync(0xffffffffu, give_up, 0)) {
+                ok = false;
                 break;
             }
-            Partial out{0.0f, 0, 0.0f, 0.0f};
-            if (kind == K_RES) {
-                out.flag = warp_or(lane < NCW ? h.wf[lane] : 0);
-            } else {
-                out = merge_hand<MODE>(P, h, lane);
+            continue;
+        }
+        idle = 0;
+        const int s = (int)(consumed % RS);
+        if (!warp_wait(&ws.full[s], (consumed / RS) & 1u, P.spin_limit, nullptr, lane)) {
+            ok = false;
+            break;
+        }
+        const Meta m = ws.meta[s];
+        const uint8_t *st = ring + (size_t)s * SB;
+        if (m.kind == K_RES) {
+            rflag |= residual_stage<E, MODE, PROBS>(P, m, st, ws.pscr, lane);
+        } else if (m.kind == K_STAT_T || !PROBS) {
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                uint4 v[4];
+                load_quad<E>(m, st, lane, h, v);
+                if (MODE == MODE_GREEDY)
+                    greedy_update<E>(v, m, lane, h, a);
+                else
+                    online_update<E>(v, P.c, a);
             }
-            if (lane == i) {
-                my_kind = kind;
-                my_b = h.b;
-                my_pos = h.pos;
-                my_k = h.k;
-                my_out = out;
-            }
-            __syncwarp();
+            if (MODE == MODE_SHORT && m.kind == K_STAT_D && (m.pos == 0 || P.full))
+                shortlist_scan(P, m, lane, m.pos == 0, a.flag);
+        }
+        __syncwarp();
+        ++consumed;
+        if (m.last) {
+            const Partial out = run_result<MODE>(P, m, a, rflag);
             if (lane == 0)
-                mbar_arrive(&sh.hempty[hs]);
-            ++m;
-            if (++hs == NH) {
-                hs = 0;
-                hph ^= 1u;
-            }
-        }
-        // publish: one lane per hand-off writes, one fence, then the counters
-        const size_t bp = (size_t)my_b * (P.K + 1) + my_pos;
-        if (lane < m) {
-            if (my_kind == K_RES) {
-                if (my_out.flag)
-                    st_vol(&P.errres[my_b], 1);
-            } else {
-                P.part[bp * P.npt + my_k] = my_out;
-            }
-        }
-        __threadfence();
-        bool last = false;
-        if (lane < m) {
-            if (my_kind == K_RES) {
-                last = atomicAdd(&P.res_cnt[my_b], 1u) == (uint32_t)P.ncr - 1u;
-            } else {
-                const int nparts = my_pos < P.K ? P.npt : P.nct;
-                last = atomicAdd(&P.pair_cnt[bp], 1u) == (uint32_t)nparts - 1u;
-            }
-        }
-        unsigned lastmask = __ballot_sync(0xffffffffu, last);
-        if (lastmask)
-            __threadfence();
-        while (lastmask) {
-            const int i = __ffs(lastmask) - 1;
-            lastmask &= lastmask - 1;
-            const int kind = __shfl_sync(0xffffffffu, my_kind, i);
-            const int b = __shfl_sync(0xffffffffu, my_b, i);
-            const int pos = __shfl_sync(0xffffffffu, my_pos, i);
-            if (kind == K_RES)
-                locate<E, MODE, PROBS>(P, sh, b, pos, lane);
+                ws.pend[npend] = Pend{m.kind, m.b, m.pos, m.kf, m.ku - m.kf + 1, out};
+            __syncwarp();
+            ++npend;
+            if (m.kind == K_RES)
+                rflag = 0;
             else
-                decide<E, MODE, PROBS>(P, b, pos, lane);
+                a = Acc{-F_INF, 0.0f, 0x7fffffff, 0};
+            if (npend == PEND)
+                publish<E, MODE, PROBS>(P, ws.pend, npend, ws.pscr, lane);
         }
-        if (exit_seen)
-            return;
     }
+    if (!ok) {
+        // Winding down: report, then wait for our own copies still in flight.
+        set_status(P, ST_TIMEOUT);
+        if (lane == 0)
+            for (uint32_t n = consumed; n < issued; ++n)
+                if (txmask & (1u << (n % RS)))
+                    mbar_wait(&ws.full[n % RS], (n / RS) & 1u, DRAIN_LIMIT, nullptr);
+    }
+    __syncwarp();
 }
 
 // =================================================================== kernel
 template <class E, int MODE, bool PROBS>
-__global__ void __launch_bounds__(NTHREADS, 2) verify_kernel(const __grid_constant__ Params P)
+__global__ void __launch_bounds__(NTHREADS, 1) verify_kernel(const __grid_constant__ Params P)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *ring = smem_raw;
-    Shared &sh = *reinterpret_cast<Shared *>(smem_raw + (size_t)NST * STAGE_BYTES);
+    Shared &sh = *reinterpret_cast<Shared *>(smem_raw + (size_t)NWARP * RS * SB);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < NST; ++s) {
-            mbar_init(&sh.full[s], 1);
-            mbar_init(&sh.empty[s], NCW);
-        }
-        for (int h = 0; h < NH; ++h) {
-            mbar_init(&sh.hfull[h], NCW);
-            mbar_init(&sh.hempty[h], 1);
-        }
-        sh.abort = 0;
+    WorkerShared &ws = sh.w[warp];
+    uint8_t *ring = smem_raw + (size_t)warp * RS * SB;
+    if (lane == 0)
+        for (int s = 0; s < RS; ++s)
+            mbar_init(&ws.full[s], 1);
+    if (threadIdx.x == 0)
         sh.last_cta = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    }
-    __syncthreads();
-    if (warp < NCW)
-        consumer<E, MODE, PROBS>(P, sh, ring, warp, lane);
-    else if (warp == W_PROD) {
-        if (lane == 0)
-            producer<E, MODE, PROBS>(P, sh, ring);
-    } else {
-        finisher<E, MODE, PROBS>(P, sh, lane);
-    }
+    __syncwarp();
+    if (lane == 0)
+        asm volatile("fence.mbarrier_init.release.cluster;\n\tfence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    worker<E, MODE, PROBS>(P, ws, ring, blockIdx.x * NWARP + warp, lane);
     __syncthreads();
 
     // The last CTA out finalises: sequences left unfinished by a timeout get

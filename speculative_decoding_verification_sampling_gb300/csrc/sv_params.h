@@ -31,6 +31,14 @@ struct SegMass {
     float r, q;
 };
 
+// A sequence published for its residual pass: b1 = sequence + 1 (0 while the
+// slot is unpublished), j = position of the emitted target token (-1 when the
+// sequence ended with a data error), rc = its Dec.  Written before b1.
+struct alignas(16) ResRec {
+    int32_t b1, j, pad0, pad1;
+    float rc[4];
+};
+
 // Per (sequence, position) quantities the residual pass needs, in float32:
 // Mt = max target logit, Lt2 = log2 of the target sum, dL = log2(Z_draft / Z_target)
 // split into a high and a low float.
@@ -60,7 +68,7 @@ struct Params {
     // workspace (device)
     uint32_t *ctl;                 // [CTL_WORDS]
     unsigned long long *state;     // [B]  decided positions (low word) | accepted positions (high word)
-    int32_t *res_seq;              // [B]  sequence + 1 for each published residual slot
+    ResRec *res_rec;               // [B]  residual slots in publication order
     uint32_t *pair_cnt;            // [B][K+1] finished stats tasks per position
     uint32_t *res_cnt;             // [B]  finished residual tasks per sequence
     int32_t *fin;                  // [B]  1 once the sequence's outputs are written
@@ -71,44 +79,45 @@ struct Params {
     Dec *dec;                      // [B][K+1]
     Partial *part;                 // [B][K+1][npt]
     SegMass *seg;                  // [B][nseg] residual mass and target mass per 256-token segment
-    int32_t *seglast;              // [B][nseg] last token with positive residual in the segment
     int32_t *sl_lb;                // [B][nseg+1] first shortlist entry at or after token 256*t
 
     // task geometry
     int es_t, es_d;                // element sizes of target and draft rows
     int se_t, se_d;                // elements per stats stage
-    int spt_t, spt_d;              // stages per stats task
-    int nct, ncd, npt;             // stats tasks per target row, per draft row, per position
+    int nct, ncd, npt;             // stats units (stages) per target row, per draft row, per position
+    int rse, rd_off;               // elements per residual stage; byte offset of its draft part
     int rspt, ncr;                 // stages per residual task, residual tasks per sequence
     int nseg;                      // 256-token segments per target row
-    uint32_t n_stats, n_res;       // total stats tasks, total residual tasks
+    uint32_t n_stats, n_res;       // total stats units, total residual tasks
+    uint32_t workers;              // worker warps in the grid
+    uint32_t g0, first_units;      // units in each worker's first batch, and in all first batches
     uint32_t spin_limit;           // bound on every on-device wait loop
     int bulk_t, bulk_d;            // rows eligible for bulk copies (16-byte aligned)
 };
 
 // Workspace layout for (B, K, V, S); every array starts 256-byte aligned.
 struct WsLayout {
-    size_t ctl, state, res_seq, pair_cnt, res_cnt, fin, errres, errcode, terminal, gtok, dec, part,
-        seg, seglast, sl_lb, total;
+    size_t ctl, state, res_rec, pair_cnt, res_cnt, fin, errres, errcode, terminal, gtok, dec, part,
+        seg, sl_lb, total;
     size_t reset_end;   // [ctl, reset_end) holds what a call must find zeroed
     int npt_max, nseg;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Stats chunks are at least 4096 elements (16 KB of float32), so this bounds
-// the number of partials any chunking chooses.
+// Stats chunks are at least 1024 elements (one 4 KB stage of float32), so this
+// bounds the number of partials any chunking chooses.
 inline WsLayout ws_layout(int B, int K, int V, int S)
 {
     WsLayout w{};
     const size_t Bz = (size_t)B, P = (size_t)K + 1;
     const int Vd = S > 0 ? S : V;
     w.nseg = (V + 255) / 256;
-    w.npt_max = (V + 4095) / 4096 + (Vd + 4095) / 4096;
+    w.npt_max = (V + 1023) / 1024 + (Vd + 1023) / 1024;
     size_t o = 0;
     w.ctl = o;      o = align256(o + 8 * sizeof(uint32_t));
     w.state = o;    o = align256(o + Bz * 8);
-    w.res_seq = o;  o = align256(o + Bz * 4);
+    w.res_rec = o;  o = align256(o + Bz * sizeof(ResRec));
     w.pair_cnt = o; o = align256(o + Bz * P * 4);
     w.res_cnt = o;  o = align256(o + Bz * 4);
     w.fin = o;      o = align256(o + Bz * 4);
@@ -120,7 +129,6 @@ inline WsLayout ws_layout(int B, int K, int V, int S)
     w.dec = o;      o = align256(o + Bz * P * sizeof(Dec));
     w.part = o;     o = align256(o + Bz * P * (size_t)w.npt_max * sizeof(Partial));
     w.seg = o;      o = align256(o + Bz * (size_t)w.nseg * sizeof(SegMass));
-    w.seglast = o;  o = align256(o + Bz * (size_t)w.nseg * 4);
     w.sl_lb = o;    o = align256(o + (S > 0 ? Bz * (size_t)(w.nseg + 1) * 4 : 0));
     w.total = o;
     return w;

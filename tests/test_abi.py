@@ -46,7 +46,9 @@ def test_status_strings():
 def test_workspace_bytes():
     a = sv.spec_workspace_bytes(256, 4, 128256)
     b = sv.spec_workspace_bytes(256, 4, 128256, 32768)
-    assert 0 < a < b < 64 << 20
+    assert 0 < a < 64 << 20 and 0 < b < 64 << 20
+    # draft partials scale with the shortlist, not the vocabulary
+    assert sv.spec_workspace_bytes(256, 4, 128256, 1024) < a
     assert sv.spec_workspace_bytes(0, 4, 100) == 0
     assert sv.spec_workspace_bytes(1, 32, 100) == 0        # K above 31
     assert sv.spec_workspace_bytes(1, 0, 100) == 0
