@@ -1,0 +1,494 @@
+#!/usr/bin/env python3
+"""Throughput of batched speculative-decoding verification on one GB300.
+
+One step is one `spec_verify` call (the whole path: temperature softmax
+statistics, left-to-right accept/reject, residual or bonus sampling) over the
+throughput workload: B=256 sequences, K=4 drafted tokens, V=128256, bf16
+target and draft logits, T=1, target logits ~ N(0, 2^2) and draft logits =
+target + N(0, 0.5^2), drafted tokens sampled from the draft softmax.
+
+Metric: verified draft positions per second (B*K per step).  Inputs live in
+HBM when the timed region starts; each step reads one of `--rotate` device
+copies of the 591 MB input set, so every step starts with the L2 (129 MB)
+holding none of its rows.  Timing: `--warmup` untimed steps, then exactly
+`--steps` steps between a barrier and a device synchronize on both sides,
+timed with CUDA events on the launching stream; the maximum over ranks is
+reported.  With N > 1 (torchrun, one process per GPU) every rank verifies its
+own independent batch (replicas; nothing is exchanged).
+
+Besides the device-timed value the JSON line carries:
+  e2e          - the same metric through the public call with host buffers:
+                 every step copies its inputs from pinned host memory and
+                 reads its outputs back;
+  roofline     - HBM roofline of the verification kernel: the logits the
+                 left-to-right rule must read (rows up to the first rejection,
+                 or all 2K+1 rows when every draft is accepted) over the mean
+                 kernel duration, against the measured copy bandwidth;
+  cpu_baseline - the float64 CPU oracle on this host's cores, on a bounded
+                 sample of the same batch (rank 0, one GPU only);
+  clocks       - SM clocks and throttle reasons sampled during the run.
+
+`--impl reference` times the float64 oracle instead (there is no other
+implementation of this path to run): rank 0 only, a bounded sample of the
+same workload per step.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+_ROOT = os.path.dirname(os.path.abspath(__file__))
+if _ROOT not in sys.path:
+    sys.path.insert(0, _ROOT)
+
+METRIC = "verified draft positions/s at V=128256 bf16; achieved HBM GB/s vs GB300 peak"
+UNIT = "positions/s"
+V = 128256
+TEMPERATURE = 1.0
+DATA_SEED = 5          # seed of the synthetic batch on rank 0 (rank r uses DATA_SEED + r)
+VERIFY_SEED = 7        # Philox key of the verification uniforms
+CSRC = os.path.join(_ROOT, "speculative_decoding_verification_sampling_gb300", "csrc")
+TRAFFIC_RECORD = os.path.join(_ROOT, "profiles", "verify_kernel_stoch_b256_k4.md")
+REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+# --------------------------------------------------------------------------
+# host-side helpers (no GPU needed; covered by CPU tests)
+# --------------------------------------------------------------------------
+def dist_env() -> tuple[int, int, int]:
+    """(rank, world_size, local_rank) from the torchrun environment."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def replica_seed(rank: int) -> int:
+    """Seed of the synthetic batch a rank verifies: replicas hold different sequences."""
+    return DATA_SEED + rank
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """Maximum of `value` over the ranks of the default process group (the value itself alone)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None) -> None:
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        if device is not None and getattr(device, "type", "cpu") == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def needed_rows(accept_len, K: int) -> int:
+    """Logit rows the left-to-right rule reads for a batch: a sequence that
+    rejects at position j reads target and draft rows 1..j (2j rows); one that
+    accepts all K reads K+1 target rows and K draft rows."""
+    total = 0
+    for L in accept_len:
+        L = int(L)
+        if L < 0:
+            raise ValueError("a sequence reported a data error")
+        total += 2 * K + 1 if L >= K else 2 * (L + 1)
+    return total
+
+
+def needed_bytes(accept_len, K: int, V: int, elem_bytes: int) -> int:
+    """Algorithmic bytes of one call: the needed logit rows, the drafted
+    tokens and the outputs (one read of each, one write of each output)."""
+    B = len(accept_len)
+    return needed_rows(accept_len, K) * V * elem_bytes + B * K * 4 + B * (K + 1) * 4 + B * 4
+
+
+def kernel_sources_digest() -> str:
+    """sha256 over the CUDA and C++ sources of the library, in name order."""
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(name.encode())
+            with open(os.path.join(CSRC, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(path: str = TRAFFIC_RECORD, digest: str | None = None):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    summary is missing or was taken on other kernel sources.  The summary
+    holds the lines `traffic_bytes_per_launch: <int>` and
+    `kernel_sources_sha256: <hex>`."""
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m_t = re.search(r"traffic_bytes_per_launch:\s*(\d+)", text)
+    m_h = re.search(r"kernel_sources_sha256:\s*([0-9a-f]{64})", text)
+    if not m_t or not m_h:
+        return None
+    if m_h.group(1) != (digest or kernel_sources_digest()):
+        return None
+    return int(m_t.group(1))
+
+
+def hbm_peak() -> tuple[float, str]:
+    """Measured copy bandwidth of this machine's GB300 (GB/s) and where it came from."""
+    path = os.path.join(_ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def sm_max_default() -> float | None:
+    try:
+        with open(os.path.join(_ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["sm_max_mhz"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+CLOCK_QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_clock_samples(lines) -> list[dict]:
+    """Parse `nvidia-smi --format=csv,noheader,nounits` lines of CLOCK_QUERY."""
+    out = []
+    for line in lines:
+        parts = [p.strip() for p in line.strip().split(",")]
+        if len(parts) != 9:
+            continue
+        try:
+            sm, smax = float(parts[1]), float(parts[2])
+        except ValueError:
+            continue
+        try:
+            util = float(parts[4])
+        except ValueError:
+            util = float("nan")
+        active = [name for name, v in zip(REASONS, parts[5:9]) if v.lower() == "active"]
+        out.append({"sm": sm, "sm_max": smax, "util": util, "reasons": active})
+    return out
+
+
+def summarize_clocks(samples: list[dict]) -> dict:
+    """Median SM clock over the samples taken under load (all samples when none
+    shows load), the maximum clock, and every throttle reason seen."""
+    if not samples:
+        return {"sm_mhz": None, "sm_max_mhz": sm_max_default(), "reasons": [], "samples": 0,
+                "note": "no nvidia-smi sample fell inside the run"}
+    loaded = [s for s in samples if not math.isnan(s["util"]) and s["util"] > 0] or samples
+    reasons = sorted({r for s in loaded for r in s["reasons"]})
+    return {"sm_mhz": statistics.median(s["sm"] for s in loaded),
+            "sm_max_mhz": max(s["sm_max"] for s in loaded), "reasons": reasons,
+            "samples": len(loaded)}
+
+
+class ClockSampler:
+    """nvidia-smi sampling of this process's GPU every 200 ms while active."""
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        cmd = ["nvidia-smi", f"--query-gpu={CLOCK_QUERY}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        self.file = tempfile.TemporaryFile(mode="w+")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.proc.wait()
+        return False
+
+    def samples(self) -> list[dict]:
+        if self.file is None:
+            return []
+        self.file.seek(0)
+        return parse_clock_samples(self.file.readlines())
+
+
+def workload_name(B: int, K: int) -> str:
+    return (f"stochastic verify B={B} K={K} V={V} bf16 T=1; target logits N(0, 2^2), "
+            f"draft logits = target + N(0, 0.5^2), drafted tokens sampled from the draft softmax")
+
+
+def base_line(args, world: int, value: float, ms_per_step: float, B: int, K: int) -> dict:
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": workload_name(B, K), "B": B, "K": K, "V": V, "T": TEMPERATURE,
+                   "global_batch": B * world, "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {args.rotate} device copies of the "
+                         f"{(2 * K + 1) * B * V * 2 / 1e6:.0f} MB input set, rotated every step"},
+    }
+
+
+# --------------------------------------------------------------------------
+# the float64 oracle on the host cores (reference arm and cpu_baseline)
+# --------------------------------------------------------------------------
+def oracle_rate(cfg, K: int, seconds: float, n_seq: int | None = None):
+    """Positions/s of the oracle over repeated passes on `n_seq` sequences of
+    the batch (all of them by default), for at least `seconds` (one pass at least)."""
+    import oracle
+    B = cfg["draft_tokens"].shape[0]
+    n = B if n_seq is None else max(1, min(B, n_seq))
+    cores = os.cpu_count() or 1
+    tgt, drf, tok = cfg["target"][:n], cfg["draft"][:n], cfg["draft_tokens"][:n]
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle.verify(tgt, drf, tok, TEMPERATURE, VERIFY_SEED, threads=cores)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return passes * n * K / el, cores, passes, n, el
+
+
+def run_reference(args) -> int:
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    import oracle
+    from speculative_decoding_verification_sampling_gb300 import synth
+    oracle.build()
+    B, K = args.batch, args.k
+    cfg = synth.throughput(B=B, K=K, seed=replica_seed(0))
+    cores = os.cpu_count() or 1
+    # size each step so that the whole run stays within about two minutes
+    t0 = time.perf_counter()
+    probe = min(B, 8)
+    oracle.verify(cfg["target"][:probe], cfg["draft"][:probe], cfg["draft_tokens"][:probe], TEMPERATURE,
+                  VERIFY_SEED, threads=cores)
+    per_seq = (time.perf_counter() - t0) / probe
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(B, budget / max(per_seq, 1e-9))))
+    windows = [(s * n) % B for s in range(args.steps + args.warmup)]
+
+    def step(start):
+        idx = torch.arange(start, start + n) % B
+        oracle.verify(cfg["target"][idx], cfg["draft"][idx], cfg["draft_tokens"][idx], TEMPERATURE,
+                      VERIFY_SEED, threads=cores, seq_ids=idx)
+
+    for s in range(args.warmup):
+        step(windows[s])
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        step(windows[args.warmup + s])
+    el = time.perf_counter() - t0
+    value = n * K * args.steps / el
+    line = base_line(args, 1, value, el * 1e3 / args.steps, B, K)
+    line["n_gpus"] = world
+    line["impl"] = "reference"
+    line["dtype"] = "f64"
+    sample = (f"{n} of the {B} sequences per step (consecutive windows of the same batch, same "
+              f"uniforms), float64 C oracle with {cores} threads")
+    line["cpu_baseline"] = {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+    line["e2e"] = {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    line["gpu_launches"] = 0
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------------------
+# the CUDA path
+# --------------------------------------------------------------------------
+def run_gb300(args) -> int:
+    import torch
+    import torch.distributed as dist
+
+    import speculative_decoding_verification_sampling_gb300 as sv
+    from speculative_decoding_verification_sampling_gb300 import synth
+
+    rank, world, local_rank = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU path)")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    sv.load()
+    B, K = args.batch, args.k
+
+    cfg = synth.throughput(B=B, K=K, seed=replica_seed(rank))
+    host_t, host_d, host_k = cfg["target"], cfg["draft"], cfg["draft_tokens"]
+    stream = torch.cuda.Stream(dev)
+    sets = []
+    with torch.cuda.stream(stream):
+        t0, d0, k0 = host_t.to(dev), host_d.to(dev), host_k.to(dev)
+        sets.append((t0, d0, k0))
+        for _ in range(1, args.rotate):
+            sets.append((t0.clone(), d0.clone(), k0.clone()))
+        outs = [(torch.empty(B, K + 1, dtype=torch.int32, device=dev),
+                 torch.empty(B, dtype=torch.int32, device=dev)) for _ in sets]
+    stream.synchronize()
+
+    def call(i):
+        t, d, k = sets[i % len(sets)]
+        ot, ol = outs[i % len(sets)]
+        sv.spec_verify(t, d, k, TEMPERATURE, VERIFY_SEED, out_tokens=ot, out_accept_len=ol, stream=stream)
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    uuid = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else (str(uuid) if uuid else None)
+
+    with ClockSampler(uuid) as clocks:
+        with torch.cuda.stream(stream):
+            for i in range(max(args.warmup, len(sets))):
+                call(i)
+        stream.synchronize()
+        # every copy of the input set gives the same result
+        ref_t, ref_l = outs[0][0].cpu(), outs[0][1].cpu()
+        for ot, ol in outs[1:]:
+            if not (torch.equal(ot.cpu(), ref_t) and torch.equal(ol.cpu(), ref_l)):
+                raise RuntimeError("copies of one input set gave different results")
+        alg_bytes = needed_bytes(ref_l.tolist(), K, V, 2)
+        all_rows_bytes = (2 * K + 1) * B * V * 2
+        mean_len = float(ref_l.double().mean())
+
+        ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        launches0 = sv.spec_launch_count()
+        barrier(dev)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for i in range(args.steps):
+                ev_s[i].record(stream)
+                call(i)
+                ev_e[i].record(stream)
+            stop.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(dev)
+        launches = sv.spec_launch_count() - launches0
+        clock_samples = clocks.samples()
+
+    elapsed_ms = start.elapsed_time(stop)
+    kernel_ms = [a.elapsed_time(b) for a, b in zip(ev_s, ev_e)]
+    elapsed_ms = max_over_ranks(elapsed_ms, dev)
+    value = world * B * K * args.steps / (elapsed_ms / 1e3)
+    mean_kernel_s = statistics.fmean(kernel_ms) / 1e3
+
+    # end to end: pinned host inputs in, results out, every step
+    pin_t, pin_d, pin_k = host_t.pin_memory(), host_d.pin_memory(), host_k.pin_memory()
+    res_t = torch.empty(B, K + 1, dtype=torch.int32).pin_memory()
+    res_l = torch.empty(B, dtype=torch.int32).pin_memory()
+    t0, d0, k0 = sets[0]
+    ot, ol = outs[0]
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            t0.copy_(pin_t, non_blocking=True)
+            d0.copy_(pin_d, non_blocking=True)
+            k0.copy_(pin_k, non_blocking=True)
+            sv.spec_verify(t0, d0, k0, TEMPERATURE, VERIFY_SEED, out_tokens=ot, out_accept_len=ol, stream=stream)
+            res_t.copy_(ot, non_blocking=True)
+            res_l.copy_(ol, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(max(3, min(args.warmup, 10))):
+        e2e_step()
+    e2e_steps = max(3, min(args.steps, 200))
+    barrier(dev)
+    torch.cuda.synchronize(dev)
+    h0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(time.perf_counter() - h0, dev)
+    barrier(dev)
+    if not (torch.equal(res_t, ref_t) and torch.equal(res_l, ref_l)):
+        raise RuntimeError("end-to-end results differ from the device-resident run")
+    h2d = (host_t.numel() * host_t.element_size() + host_d.numel() * host_d.element_size()
+           + host_k.numel() * host_k.element_size())
+    d2h = res_t.numel() * 4 + res_l.numel() * 4
+
+    if rank == 0:
+        line = base_line(args, world, value, elapsed_ms / args.steps, B, K)
+        peak, src = hbm_peak()
+        achieved = alg_bytes / mean_kernel_s / 1e9
+        digest = kernel_sources_digest()
+        line["roofline"] = {
+            "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+            "traffic": recorded_traffic(digest=digest), "peak_source": src,
+            "kernel": "verify_kernel (stochastic, bf16)",
+            "algorithmic_bytes_per_launch": alg_bytes, "mean_kernel_us": mean_kernel_s * 1e6,
+            "all_rows_bytes_per_launch": all_rows_bytes,
+            "all_rows_gbs": all_rows_bytes / mean_kernel_s / 1e9,
+        }
+        line["e2e"] = {"value": world * B * K * e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+        line["gpu_launches"] = int(launches)
+        line["clocks"] = summarize_clocks(clock_samples)
+        line["emitted_tokens_per_s"] = world * float(ref_l.double().add(1).sum()) * args.steps / (elapsed_ms / 1e3)
+        line["mean_accept_len"] = mean_len
+        if world == 1:
+            rate, cores, passes, n, el = oracle_rate(cfg, K, args.cpu_seconds)
+            line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                    "sample": f"{passes} pass(es) of the float64 C oracle over {n} of the "
+                                              f"{B} sequences of the same batch, {el:.1f} s"}
+        else:
+            line["cpu_baseline"] = None
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--batch", type=int, default=256, help="sequences per GPU")
+    ap.add_argument("--k", type=int, default=4, help="drafted tokens per sequence")
+    ap.add_argument("--rotate", type=int, default=4, help="device copies of the input set")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="length of the oracle sample")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
+    _, world, _ = dist_env()
+    if world != args.gpus:
+        if world == 1 and args.gpus > 1:
+            ap.error("--gpus N > 1 runs under torchrun with N processes")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

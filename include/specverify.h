@@ -140,6 +140,11 @@ spec_status_t spec_verify_shortlist(const void *target_logits, spec_dtype_t tdt,
 spec_status_t spec_philox_words(uint64_t seed, uint32_t tag, int B, int P, uint32_t *out,
                                 void *stream);
 
+/* Number of kernels this library has launched in this process, over every
+ * entry point and device (one per successful spec_verify* call, one per
+ * spec_philox_words call).  For accounting; thread-safe.                      */
+uint64_t spec_launch_count(void);
+
 /* A static description of a status code. */
 const char *spec_status_string(spec_status_t status);
 

@@ -22,7 +22,7 @@ from .build import LIB as _LIB_PATH
 
 __all__ = [
     "SpecVerifyError", "Aux", "spec_verify", "spec_verify_greedy", "spec_verify_shortlist",
-    "spec_workspace_bytes", "spec_philox_words", "spec_status_string", "library_path", "load",
+    "spec_workspace_bytes", "spec_philox_words", "spec_status_string", "spec_launch_count", "library_path", "load",
 ]
 
 SPEC_F32, SPEC_BF16 = 0, 1
@@ -73,8 +73,15 @@ def load():
             lib.spec_philox_words.restype = I
             lib.spec_status_string.argtypes = [I]
             lib.spec_status_string.restype = ctypes.c_char_p
+            lib.spec_launch_count.argtypes = []
+            lib.spec_launch_count.restype = U64
             _lib = lib
     return _lib
+
+
+def spec_launch_count() -> int:
+    """Kernels the library has launched in this process (all entry points)."""
+    return int(load().spec_launch_count())
 
 
 def spec_status_string(code: int) -> str:

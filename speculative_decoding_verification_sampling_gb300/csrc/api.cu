@@ -2,15 +2,23 @@
 // workspace layout, task geometry and kernel dispatch.
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <algorithm>
+#include <atomic>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "specverify.h"
 #include "sv_launch.h"
 #include "sv_params.h"
 
 namespace {
+
+// kernels launched by this library in this process (every entry point)
+std::atomic<uint64_t> g_launches{0};
 
 constexpr int kMaxDevices = 64;
 constexpr int kStageBytes = 4096;    // bytes per ring stage (matches the kernel)
@@ -79,6 +87,28 @@ spec_status_t device_setup(int *sms, int mode, int tdt, bool probs, sv::KernelEn
     return SPEC_OK;
 }
 
+// Largest shared-memory footprint per CTA for the cluster kernel: three CTAs
+// (three sequences in flight) per SM at V = 128256 bf16 with clusters of 8.
+constexpr uint32_t kClusterSmemMax = 72 * 1024;
+
+// Kernel choice: SPECVERIFY_KERNEL=general forces the chunk-scheduled kernel
+// for every call (the cluster kernel is used where it applies otherwise).
+bool cluster_disabled()
+{
+    const char *s = std::getenv("SPECVERIFY_KERNEL");
+    return s && std::strcmp(s, "general") == 0;
+}
+
+// SPECVERIFY_DEBUG=1 prints each launch's geometry to stderr.
+bool debug_enabled()
+{
+    const char *s = std::getenv("SPECVERIFY_DEBUG");
+    return s && *s && std::strcmp(s, "0") != 0;
+}
+
+// Co-resident clusters for (kernel, cluster size, shared memory), per device.
+std::map<std::tuple<int, int, int, uint32_t>, int> g_max_clusters;
+
 uint32_t spin_limit()
 {
     const char *s = std::getenv("SPECVERIFY_SPIN_LIMIT");
@@ -100,6 +130,91 @@ bool sizes_ok(int B, int K, int V, int S)
     const long long rows = (long long)B * (2LL * K + 1);
     const long long chunks = (long long)(V / 1024 + 1);
     return rows * chunks < (1LL << 31);
+}
+
+// One sequence per cluster (sv_cluster.cuh).  Applies to stochastic
+// verification with draft logits and to greedy verification, when no
+// per-position output is requested, rows start 16-byte aligned and one CTA's
+// slice of a position fits kClusterSmemMax.  Returns SPEC_ERR_UNSUPPORTED
+// (without launching) when it does not apply.
+spec_status_t run_cluster(bool greedy, const void *target, spec_dtype_t tdt, const void *draft,
+                          const int32_t *tokens, int B, int K, int V, float T, uint64_t seed,
+                          int32_t *out_tokens, int32_t *out_len, uint32_t *ctl, const spec_aux_t *aux,
+                          void *stream)
+{
+    if (cluster_disabled())
+        return SPEC_ERR_UNSUPPORTED;
+    if (aux && (aux->q_draft || aux->p_draft || aux->row_lse) && !greedy)
+        return SPEC_ERR_UNSUPPORTED;
+    const int es = tdt == SPEC_F32 ? 4 : 2;
+    if (((long long)V * es) % 16 != 0 || reinterpret_cast<uintptr_t>(target) % 16 != 0 ||
+        (!greedy && reinterpret_cast<uintptr_t>(draft) % 16 != 0))
+        return SPEC_ERR_UNSUPPORTED;
+    const int rows = greedy ? 1 : 2;
+    const uint32_t hdr = sv::cluster_header_bytes();
+    int csize = 0, chunk = 0;
+    uint32_t smem = 0;
+    for (int cs : {8, 16}) {
+        const int ch = cdiv(cdiv(V, cs), 8) * 8;
+        const long long bytes = (long long)hdr + (long long)ch * es * rows;
+        if (bytes <= kClusterSmemMax) {
+            csize = cs;
+            chunk = ch;
+            smem = (uint32_t)bytes;
+            break;
+        }
+    }
+    if (!csize)
+        return SPEC_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    const int tix = tdt == SPEC_BF16 ? 1 : 0;
+    const sv::ClusterEntry entry = sv::entry_cluster(tix, greedy);
+    int maxc = 0;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        const auto key = std::make_tuple(dev, tix * 2 + (greedy ? 1 : 0), csize, smem);
+        auto it = g_max_clusters.find(key);
+        if (it == g_max_clusters.end()) {
+            if (entry.max_clusters(csize, smem, &maxc) != cudaSuccess)
+                return SPEC_ERR_CUDA;
+            g_max_clusters[key] = maxc;
+        } else {
+            maxc = it->second;
+        }
+    }
+    if (maxc < 1)
+        return SPEC_ERR_UNSUPPORTED;
+    sv::ClusterParams P{};
+    P.target = target;
+    P.draft = greedy ? nullptr : draft;
+    P.tokens = tokens;
+    P.out_tokens = out_tokens;
+    P.out_len = out_len;
+    if (aux) {
+        P.aux_R = aux->residual_mass;
+        P.aux_status = aux->device_status;
+    }
+    P.ctl = ctl;
+    P.B = B;
+    P.K = K;
+    P.V = V;
+    P.chunk = chunk;
+    P.c = greedy ? 1.0f : (float)(1.4426950408889634 / (double)T);
+    P.key0 = (uint32_t)(seed & 0xffffffffu);
+    P.key1 = (uint32_t)(seed >> 32);
+    P.spin_limit = spin_limit();
+    const int clusters = std::min(maxc, B);
+    if (debug_enabled())
+        std::fprintf(stderr, "specverify: cluster kernel %s %s B=%d K=%d V=%d: cluster %d CTAs, chunk %d, "
+                     "%u B shared memory, %d co-resident clusters, %d launched\n",
+                     greedy ? "greedy" : "stochastic", tdt == SPEC_BF16 ? "bf16" : "f32", B, K, V, csize, chunk,
+                     smem, maxc, clusters);
+    if (entry.launch(P, clusters, csize, smem, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return SPEC_OK;
 }
 
 spec_status_t run(int mode, const void *target, spec_dtype_t tdt, const void *draft, spec_dtype_t ddt,
@@ -141,6 +256,17 @@ spec_status_t run(int mode, const void *target, spec_dtype_t tdt, const void *dr
     spec_status_t st = device_setup(&sms, mode, tdt == SPEC_BF16 ? 1 : 0, probs != 0, &entry, &occ);
     if (st != SPEC_OK)
         return st;
+
+    if (mode == sv::MODE_GREEDY || (mode == sv::MODE_STOCH && !probs)) {
+        const bool full = aux && (aux->q_draft || aux->p_draft || aux->row_lse);
+        if (!(full && mode != sv::MODE_GREEDY)) {
+            uint32_t *ctl = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + L.ctl);
+            const spec_status_t cs = run_cluster(mode == sv::MODE_GREEDY, target, tdt, draft, tokens, B, K, V, T,
+                                                 seed, out_tokens, out_len, ctl, aux, stream);
+            if (cs != SPEC_ERR_UNSUPPORTED)
+                return cs;
+        }
+    }
 
     sv::Params P{};
     const bool greedy = mode == sv::MODE_GREEDY;
@@ -222,6 +348,7 @@ spec_status_t run(int mode, const void *target, spec_dtype_t tdt, const void *dr
 
     if (entry.launch(P, (int)grid, static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SPEC_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return SPEC_OK;
 }
 
@@ -273,8 +400,11 @@ spec_status_t spec_philox_words(uint64_t seed, uint32_t tag, int B, int P, uint3
     if (sv::launch_philox_words((uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32), tag, B, P, out,
                                 static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return SPEC_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
     return SPEC_OK;
 }
+
+uint64_t spec_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char *spec_status_string(spec_status_t status)
 {

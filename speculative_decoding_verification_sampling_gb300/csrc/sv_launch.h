@@ -16,6 +16,14 @@ KernelEntry entry_stoch(int tdt, bool probs);
 KernelEntry entry_greedy(int tdt);
 KernelEntry entry_short(int tdt, bool probs);
 
+// The cluster kernel: one sequence per cluster of `csize` CTAs.
+struct ClusterEntry {
+    cudaError_t (*launch)(const ClusterParams &P, int clusters, int csize, uint32_t smem, cudaStream_t stream);
+    cudaError_t (*max_clusters)(int csize, uint32_t smem, int *clusters);
+};
+ClusterEntry entry_cluster(int tdt, bool greedy);
+uint32_t cluster_header_bytes();   // shared memory ahead of the row slices
+
 cudaError_t launch_philox_words(uint32_t k0, uint32_t k1, uint32_t tag, int B, int P, uint32_t *out,
                                 cudaStream_t stream);
 

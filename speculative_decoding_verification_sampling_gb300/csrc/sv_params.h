@@ -12,8 +12,10 @@ enum Mode { MODE_STOCH = 0, MODE_GREEDY = 1, MODE_SHORT = 2 };
 enum Status { ST_OK = 0, ST_NONFINITE = 2, ST_TOKEN = 3, ST_SHORTLIST = 4, ST_TIMEOUT = 7 };
 
 // Words of the control block at the start of the workspace.
+// Words 5..7 belong to the cluster kernel (next sequence to claim, CTAs that
+// have finished, abort flag); both kernels leave every word zeroed.
 enum Ctl { CTL_STATS_NEXT = 0, CTL_RES_TICKET = 1, CTL_RES_COUNT = 2, CTL_EXIT = 3, CTL_STATUS = 4,
-           CTL_WORDS = 8 };
+           CTL_CL_NEXT = 5, CTL_CL_EXIT = 6, CTL_CL_ABORT = 7, CTL_WORDS = 8 };
 
 // Partial result of one stats task (one chunk of one row):
 //   logits: m = max raw logit of the chunk, s = sum 2^((x - m) * c) over the chunk;
@@ -93,6 +95,24 @@ struct Params {
     uint32_t g0, first_units;      // units in each worker's first batch, and in all first batches
     uint32_t spin_limit;           // bound on every on-device wait loop
     int bulk_t, bulk_d;            // rows eligible for bulk copies (16-byte aligned)
+};
+
+// Launch parameters of the cluster kernel (one sequence per thread-block
+// cluster; CTA r of a cluster owns tokens [r*chunk, (r+1)*chunk) of every row).
+struct ClusterParams {
+    const void *target;        // [B][K+1][V]
+    const void *draft;         // [B][K][V] draft logits; nullptr for greedy
+    const int32_t *tokens;     // [B][K]
+    int32_t *out_tokens;       // [B][K+1]
+    int32_t *out_len;          // [B]
+    float *aux_R;              // [B] or nullptr
+    int32_t *aux_status;       // [1] or nullptr
+    uint32_t *ctl;             // [CTL_WORDS] at the start of the workspace
+    int B, K, V;
+    int chunk;                 // tokens of a row per CTA (a multiple of 8)
+    float c;                   // log2(e) / T
+    uint32_t key0, key1;       // Philox key (seed low, seed high)
+    uint32_t spin_limit;       // bound on every on-device wait loop
 };
 
 // Workspace layout for (B, K, V, S); every array starts 256-byte aligned.

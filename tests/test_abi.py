@@ -37,6 +37,15 @@ def test_every_declared_symbol_is_exported():
     assert set(decl) <= exported, set(decl) - exported
 
 
+def test_launch_counter_does_not_count_rejected_calls():
+    lib = sv.load()
+    n0 = sv.spec_launch_count()
+    buf = (ctypes.c_int32 * 64)()
+    p = ctypes.cast(buf, ctypes.c_void_p)
+    assert lib.spec_verify(p, 0, p, 0, 0, p, 0, 4, 16, 1.0, 1, p, p, p, 1 << 8, None, None) == 1
+    assert sv.spec_launch_count() == n0
+
+
 def test_status_strings():
     for code in range(8):
         assert sv.spec_status_string(code)

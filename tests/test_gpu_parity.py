@@ -4,6 +4,7 @@ uniforms (counted); probabilities within 1e-5 absolute."""
 from __future__ import annotations
 
 import math
+import os
 
 import numpy as np
 import pytest
@@ -24,6 +25,19 @@ def _device():
         pytest.skip("no CUDA device")
     torch.cuda.set_device(DEV)
     sv.load()
+
+
+@pytest.fixture(scope="module", autouse=True, params=["cluster", "general"])
+def kernel(request):
+    """Every case runs twice: with the default dispatch (the cluster kernel
+    wherever it applies) and with the chunk-scheduled kernel forced."""
+    old = os.environ.get("SPECVERIFY_KERNEL")
+    os.environ["SPECVERIFY_KERNEL"] = "auto" if request.param == "cluster" else "general"
+    yield request.param
+    if old is None:
+        os.environ.pop("SPECVERIFY_KERNEL", None)
+    else:
+        os.environ["SPECVERIFY_KERNEL"] = old
 
 
 def _to(cfg):
@@ -79,6 +93,7 @@ def test_greedy_full_size_bit_exact():
 @pytest.mark.parametrize("B,K,V,dtype", [
     (1, 1, 1, torch.float32), (3, 31, 257, torch.float32), (5, 7, 4097, torch.bfloat16),
     (2, 3, 50257, torch.bfloat16), (16, 4, 1000, torch.float32), (9, 2, 8192 * 3 + 8, torch.bfloat16),
+    (4, 3, 16, torch.float32), (7, 4, 300, torch.float32), (40, 2, 128256, torch.bfloat16),
 ])
 def test_greedy_edge_shapes(B, K, V, dtype):
     cfg = synth.greedy(B=B, K=K, V=V, dtype=dtype, seed=B * 100 + K)
@@ -140,6 +155,7 @@ def test_throughput_points_sampled(B, K):
 @pytest.mark.parametrize("B,K,V,dtype,T", [
     (3, 1, 1, torch.float32, 1.0), (4, 31, 300, torch.float32, 0.9), (7, 5, 4097, torch.bfloat16, 1.3),
     (5, 3, 50257, torch.bfloat16, 1.0), (2, 6, 2049, torch.float32, 0.5), (33, 2, 8192 * 2 + 16, torch.bfloat16, 1.0),
+    (5, 3, 16, torch.float32, 1.0), (6, 4, 1004, torch.float32, 0.8), (300, 3, 2048, torch.bfloat16, 1.0),
 ])
 def test_stochastic_edge_shapes(B, K, V, dtype, T):
     cfg = synth.stochastic_gaussian(B, K, V, dtype, T, 2.0, 0.5, seed=B * 7 + K)
