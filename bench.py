@@ -57,7 +57,7 @@ TEMPERATURE = 1.0
 DATA_SEED = 5          # seed of the synthetic batch on rank 0 (rank r uses DATA_SEED + r)
 VERIFY_SEED = 7        # Philox key of the verification uniforms
 CSRC = os.path.join(_ROOT, "speculative_decoding_verification_sampling_gb300", "csrc")
-TRAFFIC_RECORD = os.path.join(_ROOT, "profiles", "verify_kernel_stoch_b256_k4.md")
+TRAFFIC_RECORD = os.path.join(_ROOT, "profiles", "cluster_kernel_stoch_b256_k4.md")
 REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
 
@@ -442,7 +442,7 @@ def run_gb300(args) -> int:
         line["roofline"] = {
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": recorded_traffic(digest=digest), "peak_source": src,
-            "kernel": "verify_kernel (stochastic, bf16)",
+            "kernel": "cluster_kernel (stochastic, bf16)",
             "algorithmic_bytes_per_launch": alg_bytes, "mean_kernel_us": mean_kernel_s * 1e6,
             "all_rows_bytes_per_launch": all_rows_bytes,
             "all_rows_gbs": all_rows_bytes / mean_kernel_s / 1e9,

@@ -104,17 +104,62 @@ __device__ __forceinline__ void st_async16(uint32_t dst, uint4 v, uint32_t bar)
                  "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
                  : "memory");
 }
+// Suspend time hint (ns) for the waits below: the warp sleeps in hardware
+// until the phase completes or this much time has passed, instead of
+// spinning and taking issue slots from the warps that compute.
+constexpr uint32_t WAIT_HINT_NS = 20000;
+
 __device__ __forceinline__ bool cl_test(unsigned long long *bar, uint32_t parity)
 {
     uint32_t ok;
     asm volatile(
-        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(saddr(bar)), "r"(parity)
+        : "r"(saddr(bar)), "r"(parity), "r"(WAIT_HINT_NS)
         : "memory");
     return ok != 0;
 }
+// A CTA-local phase wait with the suspend hint (the data came by cp.async.bulk).
+__device__ __forceinline__ bool mbar_test_hint(unsigned long long *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(saddr(bar)), "r"(parity), "r"(WAIT_HINT_NS)
+        : "memory");
+    return ok != 0;
+}
+// Number of hinted waits that make up a spin limit of `limit` polls.
+__device__ __forceinline__ uint32_t hinted_limit(uint32_t limit) { return (limit >> 8) + 16u; }
+// Bounded wait on a ring mbarrier: hinted try_wait sleeps the thread in
+// hardware until the phase completes (or the hint runs out).  Returns false
+// when the waits allowed by `limit` ran out.
+__device__ __forceinline__ bool ring_wait(unsigned long long *bar, uint32_t parity, uint32_t limit)
+{
+    const uint32_t lim = hinted_limit(limit);
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_test_hint(bar, parity))
+            return true;
+        if (it >= lim)
+            return false;
+    }
+}
+// Warp-uniform form: lane 0 waits, then every lane observes the phase.
+__device__ __forceinline__ bool ring_wait_warp(unsigned long long *bar, uint32_t parity, uint32_t limit, int lane)
+{
+    bool ok = true;
+    if (lane == 0)
+        ok = ring_wait(bar, parity, limit);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok)
+        (void)mbar_test(bar, parity);
+    __syncwarp();
+    return ok;
+}
+
 // Warp-uniform bounded wait for an exchange round (records written by peers).
 // Gives up after `limit` polls, or early once another CTA has aborted.
 __device__ __forceinline__ bool cl_wait(unsigned long long *bar, uint32_t parity, uint32_t limit,
@@ -122,15 +167,14 @@ __device__ __forceinline__ bool cl_wait(unsigned long long *bar, uint32_t parity
 {
     bool ok = true;
     if (lane == 0) {
+        const uint32_t lim = hinted_limit(limit);
         for (uint32_t it = 0;; ++it) {
             if (cl_test(bar, parity))
                 break;
-            if (it >= limit || ((it & 255u) == 255u && ld_vol(abortw))) {
+            if (it >= lim || ld_vol(abortw)) {
                 ok = false;
                 break;
             }
-            if (it > 32)
-                __nanosleep(64);
         }
     }
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -315,58 +359,77 @@ __device__ __forceinline__ f2 sum_exp8(const f2 *X, f2 cc, f2 nmc)
     return add2(add2(e[0], e[2]), add2(e[1], e[3]));
 }
 
+// Adds one group (4 float pairs) to a running partial (reference mc in log2
+// units, s = sum 2^(x c - mc)).  The common case is one packed FMA, one ex2
+// and one add per token plus a single compare on the group's sum.  The slow
+// path is taken when that sum is not below 2^32, which covers:
+//   - the first group (mc = -inf),
+//   - a group more than about 2^29 above the reference,
+//   - NaN or +inf (which set `bit` in fl).
+// There the group maximum moves the reference.  Below 2^32 the sum simply
+// grows, so the reference rarely moves.
+__device__ __forceinline__ void acc_group(const f2 *X, float c, float &mc, float &s, int &fl, int bit)
+{
+    const f2 cc = pk(c, c);
+    float lo, hi;
+    upk(sum_exp8(X, cc, pk(-mc, -mc)), lo, hi);
+    const float t = lo + hi;
+    if (t < 4294967296.0f) {
+        s += t;
+        return;
+    }
+    float x[8];
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+        upk(X[p], x[2 * p], x[2 * p + 1]);
+    float gm = x[0];
+#pragma unroll
+    for (int e = 1; e < 8; ++e)
+        gm = fmax_nan(gm, x[e]);
+    if (!(gm == gm) || gm == F_INF) {
+        fl |= bit;
+        return;
+    }
+    if (!(gm > -F_INF))
+        return;
+    const float gmc = gm * c;
+    if (gmc > mc) {
+        s = (mc > -F_INF) ? s * ex2a(mc - gmc) : 0.0f;
+        mc = gmc;
+    }
+    upk(sum_exp8(X, cc, pk(-mc, -mc)), lo, hi);
+    s += lo + hi;
+}
+
 // One thread's partial over the groups tid, tid + T, ... of a slice of n
-// tokens: mc = (its maximum logit) * c rounded to float, and
-// s = sum 2^(x c - mc).  Every element's exponent is one fused multiply-add
-// from the same reference mc, so partials merge exactly by 2^(mc_i - mc_j).
-// The maximum comes first (packed, independent loads); the sum follows with mc
-// fixed.  The last, partial group (n not a multiple of 8) is masked to -inf.
-// NaN or +inf sets `bit` in fl.
+// tokens: a reference mc (a maximum logit times c, rounded) and
+// s = sum 2^(x c - mc), in one pass.  The last, partial group (n not a
+// multiple of 8) is masked to -inf.  NaN or +inf sets `bit` in fl.
 template <class E>
 __device__ __forceinline__ void thread_stats(const uint8_t *base, int n, int tid, float c, float &mc, float &s,
                                              int &fl, int bit)
 {
     const int nf = n >> 3;
-    const bool tail = (n & 7) != 0 && tid == nf % CL_THREADS;
-    typename Grp<E>::Acc a0 = Grp<E>::acc_init(), a1 = Grp<E>::acc_init();
+    mc = -F_INF;
+    s = 0.0f;
     int g = tid;
     for (; g + CL_THREADS < nf; g += 2 * CL_THREADS) {
-        a0 = Grp<E>::acc_max(base, g, a0);
-        a1 = Grp<E>::acc_max(base, g + CL_THREADS, a1);
-    }
-    if (g < nf)
-        a0 = Grp<E>::acc_max(base, g, a0);
-    float m = fmax_nan(Grp<E>::acc_value(a0), Grp<E>::acc_value(a1));
-    f2 T[4];
-    if (tail)
-        m = fmax_nan(m, group8<E>(base, nf, n, T));
-    s = 0.0f;
-    mc = m * c;
-    if (!(m == m) || m == F_INF) {
-        fl |= bit;
-        return;
-    }
-    if (!(m > -F_INF))
-        return;
-    const f2 cc = pk(c, c), nmc = pk(-mc, -mc);
-    f2 s0 = 0ull, s1 = 0ull;
-    for (g = tid; g + CL_THREADS < nf; g += 2 * CL_THREADS) {
         f2 X[4], Y[4];
         Grp<E>::pairs(base, g, X);
         Grp<E>::pairs(base, g + CL_THREADS, Y);
-        s0 = add2(s0, sum_exp8(X, cc, nmc));
-        s1 = add2(s1, sum_exp8(Y, cc, nmc));
+        acc_group(X, c, mc, s, fl, bit);
+        acc_group(Y, c, mc, s, fl, bit);
     }
     if (g < nf) {
         f2 X[4];
         Grp<E>::pairs(base, g, X);
-        s0 = add2(s0, sum_exp8(X, cc, nmc));
+        acc_group(X, c, mc, s, fl, bit);
     }
-    if (tail)
-        s1 = add2(s1, sum_exp8(T, cc, nmc));
-    float lo, hi;
-    upk(add2(s0, s1), lo, hi);
-    s = lo + hi;
+    if ((n & 7) != 0 && tid == nf % CL_THREADS) {
+        f2 T[4];
+        (void)group8<E>(base, nf, n, T);
+        acc_group(T, c, mc, s, fl, bit);
+    }
 }
 
 // Residual coefficients of the position a sequence ended at, in log2 units:
@@ -572,6 +635,31 @@ __device__ __forceinline__ void cl_emit(const ClusterParams &P, int b, int j, in
     P.out_len[b] = j;
 }
 
+// Send lane 0's record to every CTA of the cluster (lane l writes CTA l's
+// copy): `slot` is this CTA's own receive slot for the sender (the same offset
+// in every CTA), `bar` the round's mbarrier.
+__device__ __forceinline__ void send_rec_to(Rec *slot, unsigned long long *bar, uint32_t C, const Rec &r0, int lane)
+{
+    Rec r;
+    r.a0 = __shfl_sync(0xffffffffu, r0.a0, 0);
+    r.a1 = __shfl_sync(0xffffffffu, r0.a1, 0);
+    r.a2 = __shfl_sync(0xffffffffu, r0.a2, 0);
+    r.i0 = __shfl_sync(0xffffffffu, r0.i0, 0);
+    r.b0 = __shfl_sync(0xffffffffu, r0.b0, 0);
+    r.b1 = __shfl_sync(0xffffffffu, r0.b1, 0);
+    r.b2 = __shfl_sync(0xffffffffu, r0.b2, 0);
+    r.i1 = __shfl_sync(0xffffffffu, r0.i1, 0);
+    if ((uint32_t)lane < C) {
+        const uint32_t dst = cl_map(saddr(slot), (uint32_t)lane);
+        const uint32_t rb = cl_map(saddr(bar), (uint32_t)lane);
+        st_async16(dst, make_uint4(__float_as_uint(r.a0), __float_as_uint(r.a1), __float_as_uint(r.a2), (uint32_t)r.i0),
+                   rb);
+        st_async16(dst + 16,
+                   make_uint4(__float_as_uint(r.b0), __float_as_uint(r.b1), __float_as_uint(r.b2), (uint32_t)r.i1),
+                   rb);
+    }
+}
+
 // Send lane 0's record of the round with parity `par` to every CTA (lane l
 // writes CTA l's copy).
 __device__ __forceinline__ void send_rec(ClShared &S, uint32_t par, uint32_t me, uint32_t C, const Rec &r0, int lane)
@@ -661,7 +749,7 @@ __global__ void __launch_bounds__(CL_THREADS, 3) cluster_kernel(const __grid_con
             // ---- reduce the slice
             bool ok = true;
             if (n > 0) {
-                ok = warp_wait(&S.full, loads & 1u, P.spin_limit, nullptr, lane);
+                ok = ring_wait_warp(&S.full, loads & 1u, P.spin_limit, lane);
                 ok = __syncthreads_and(ok);
                 if (ok) {
                     ++loads;

@@ -24,6 +24,14 @@ struct ClusterEntry {
 ClusterEntry entry_cluster(int tdt, bool greedy);
 uint32_t cluster_header_bytes();   // shared memory ahead of the row slices
 
+// The sweep kernel: (position, sequence, part) items over persistent CTAs.
+struct SweepEntry {
+    cudaError_t (*launch)(const SweepParams &P, int grid, cudaStream_t stream);
+    cudaError_t (*occupancy)(int *ctas_per_sm);
+    int max_v;   // largest vocabulary it accepts (a row streamed by one CTA)
+};
+SweepEntry entry_sweep(int tdt);
+
 cudaError_t launch_philox_words(uint32_t k0, uint32_t k1, uint32_t tag, int B, int P, uint32_t *out,
                                 cudaStream_t stream);
 

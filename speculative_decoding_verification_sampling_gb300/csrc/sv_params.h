@@ -115,10 +115,63 @@ struct ClusterParams {
     uint32_t spin_limit;       // bound on every on-device wait loop
 };
 
+// Sweep kernel (sv_sweep.cuh): per-sequence decision state (in the region a
+// call must find zeroed) and per-(sequence, position) statistics.
+struct SwSeq {
+    uint32_t lock;     // 1 while a CTA advances the decisions
+    uint32_t front;    // next undecided position
+    uint32_t end;      // 0 while undecided; 1 + j once the sequence ended at position j; 0x80000000 | code on error
+    uint32_t fin;      // 1 once the outputs are written
+};
+// Statistics of one part of one (sequence, position), or of the whole row
+// pair once merged: stochastic: target reference and sum, draft reference
+// and sum (log2 units, sums as float pairs); greedy: mt = maximum, st_hi holds
+// its index's bits.  flags: bit 0 target NaN/+inf, bit 1 draft NaN/+inf.
+struct alignas(16) SwStat {
+    float mt, st_hi, st_lo, md, sd_hi, sd_lo;
+    int flags, pad;
+};
+constexpr int SW_SMAX = 16;   // largest number of parts per row pair
+constexpr uint32_t SW_READY = 0x80000000u;   // sw_cnt bit: merged statistics written
+
+// Parts per row pair for a batch of B sequences: enough (position, sequence,
+// part) items to cover the GPU at position 0.
+inline int sweep_parts(int B)
+{
+    int S = 1;
+    while (S < SW_SMAX && (long long)B * S < 512)
+        S <<= 1;
+    return S;
+}
+
+struct SweepParams {
+    const void *target;        // [B][K+1][V]
+    const void *draft;         // [B][K][V] draft logits; nullptr for greedy
+    const int32_t *tokens;     // [B][K]
+    int32_t *out_tokens;       // [B][K+1]
+    int32_t *out_len;          // [B]
+    float *aux_R;              // [B] or nullptr
+    int32_t *aux_status;       // [1] or nullptr
+    uint32_t *ctl;             // [CTL_WORDS] at the start of the workspace
+    uint32_t reset_words;      // 32-bit words from ctl a call leaves zeroed
+    SwSeq *seq;                // [B]
+    uint32_t *cnt;             // [B][K+1] parts done (| SW_READY once merged)
+    SwStat *part;              // [B][K+1][S]
+    SwStat *stat;              // [B][K+1]
+    int B, K, V;
+    int S;                     // parts per row pair
+    int span;                  // tokens per part (a multiple of 8)
+    int greedy;
+    float c;                   // log2(e) / T
+    uint32_t key0, key1;       // Philox key (seed low, seed high)
+    uint32_t spin_limit;
+    uint32_t n_items;          // (K + 1) * B * S
+};
+
 // Workspace layout for (B, K, V, S); every array starts 256-byte aligned.
 struct WsLayout {
-    size_t ctl, state, res_rec, pair_cnt, res_cnt, fin, errres, errcode, terminal, gtok, dec, part,
-        seg, sl_lb, total;
+    size_t ctl, state, res_rec, pair_cnt, res_cnt, fin, errres, sw_seq, sw_cnt, errcode, terminal, gtok, dec,
+        part, seg, sl_lb, sw_part, sw_stat, total;
     size_t reset_end;   // [ctl, reset_end) holds what a call must find zeroed
     int npt_max, nseg;
 };
@@ -142,6 +195,8 @@ inline WsLayout ws_layout(int B, int K, int V, int S)
     w.res_cnt = o;  o = align256(o + Bz * 4);
     w.fin = o;      o = align256(o + Bz * 4);
     w.errres = o;   o = align256(o + Bz * 4);
+    w.sw_seq = o;   o = align256(o + Bz * sizeof(SwSeq));
+    w.sw_cnt = o;   o = align256(o + Bz * P * 4);
     w.reset_end = o;
     w.errcode = o;  o = align256(o + Bz * P * 4);
     w.terminal = o; o = align256(o + Bz * 4);
@@ -150,6 +205,8 @@ inline WsLayout ws_layout(int B, int K, int V, int S)
     w.part = o;     o = align256(o + Bz * P * (size_t)w.npt_max * sizeof(Partial));
     w.seg = o;      o = align256(o + Bz * (size_t)w.nseg * sizeof(SegMass));
     w.sl_lb = o;    o = align256(o + (S > 0 ? Bz * (size_t)(w.nseg + 1) * 4 : 0));
+    w.sw_part = o;  o = align256(o + Bz * P * (size_t)sweep_parts(B) * sizeof(SwStat));
+    w.sw_stat = o;  o = align256(o + Bz * P * sizeof(SwStat));
     w.total = o;
     return w;
 }

@@ -27,12 +27,13 @@ def _device():
     sv.load()
 
 
-@pytest.fixture(scope="module", autouse=True, params=["cluster", "general"])
+@pytest.fixture(scope="module", autouse=True, params=["cluster", "sweep", "general"])
 def kernel(request):
-    """Every case runs twice: with the default dispatch (the cluster kernel
-    wherever it applies) and with the chunk-scheduled kernel forced."""
+    """Every case runs under each kernel: the default dispatch (the cluster
+    kernel wherever it applies), the sweep kernel, and the chunk-scheduled
+    kernel."""
     old = os.environ.get("SPECVERIFY_KERNEL")
-    os.environ["SPECVERIFY_KERNEL"] = "auto" if request.param == "cluster" else "general"
+    os.environ["SPECVERIFY_KERNEL"] = "auto" if request.param == "cluster" else request.param
     yield request.param
     if old is None:
         os.environ.pop("SPECVERIFY_KERNEL", None)
