@@ -133,6 +133,30 @@ spec_status_t spec_verify_shortlist(const void *target_logits, spec_dtype_t tdt,
                                     void *workspace, size_t workspace_bytes,
                                     const spec_aux_t *aux, void *stream);
 
+/* Verification with no caller workspace (the pages have no counterpart: this
+ * is an interface for callers that cannot allocate device memory, or cannot
+ * hold a workspace per call, e.g. code with a fixed memory plan).  Arguments
+ * and results are those of spec_verify (T == 0: greedy, draft_logits may be
+ * NULL) with draft logits only.
+ *   Scratch: a 256-byte device array inside the library holds the kernel's
+ *   control words.  It is zero when the library loads, and every call that
+ *   completes leaves it zero.  The call allocates nothing; it is served by
+ *   the cluster kernel alone.
+ *   Limits: rows 16-byte aligned (V * element size a multiple of 16, aligned
+ *   bases), one CTA's slice of a position within that kernel's shared-memory
+ *   budget (about V <= 289280 bfloat16 / 144640 float32 logits with draft
+ *   rows, twice that for greedy), and no q_draft / p_draft / row_lse outputs.
+ *   Any other call returns SPEC_ERR_UNSUPPORTED without launching;
+ *   spec_verify serves it.
+ *   Overlapping calls race: all calls on a device share the scratch, so they
+ *   must be ordered on the GPU (one stream, or events between streams).
+ *   The first call on each device looks up the scratch address with a CUDA
+ *   runtime call; make that first call outside any stream capture.          */
+spec_status_t spec_verify_static(const void *target_logits, spec_dtype_t tdt, const void *draft_logits,
+                                 const int32_t *draft_tokens, int B, int K, int V, float T, uint64_t seed,
+                                 int32_t *out_tokens, int32_t *out_accept_len, const spec_aux_t *aux,
+                                 void *stream);
+
 /* Philox4x32-10 words as the verification kernels draw them, for checking:
  * out[(b * P + pos) * 4 + w] = word w of Philox(counter (pos, b, tag, 0),
  * key (seed low, seed high)) for b < B, pos < P.  `out` is a device pointer of

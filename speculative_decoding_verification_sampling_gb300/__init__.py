@@ -22,7 +22,7 @@ from .build import LIB as _LIB_PATH
 
 __all__ = [
     "SpecVerifyError", "Aux", "spec_verify", "spec_verify_greedy", "spec_verify_shortlist",
-    "spec_workspace_bytes", "spec_philox_words", "spec_status_string", "spec_launch_count", "library_path", "load",
+    "spec_workspace_bytes", "spec_philox_words", "spec_status_string", "spec_launch_count", "spec_verify_static", "library_path", "load",
 ]
 
 SPEC_F32, SPEC_BF16 = 0, 1
@@ -73,6 +73,8 @@ def load():
             lib.spec_philox_words.restype = I
             lib.spec_status_string.argtypes = [I]
             lib.spec_status_string.restype = ctypes.c_char_p
+            lib.spec_verify_static.argtypes = [P, I, P, P, I, I, I, F, U64, P, P, P, P]
+            lib.spec_verify_static.restype = I
             lib.spec_launch_count.argtypes = []
             lib.spec_launch_count.restype = U64
             _lib = lib
@@ -227,6 +229,31 @@ def spec_verify_greedy(target: torch.Tensor, draft_tokens: torch.Tensor, *, out_
                                    ctypes.byref(ax) if ax is not None else None, st)
     if rc:
         raise SpecVerifyError(rc, "spec_verify_greedy")
+    return out_tokens, out_accept_len
+
+
+def spec_verify_static(target: torch.Tensor, draft: torch.Tensor | None, draft_tokens: torch.Tensor, T: float,
+                       seed: int, *, out_tokens=None, out_accept_len=None, aux: Aux | None = None, stream=None):
+    """spec_verify without a workspace: the library's own 256-byte scratch
+    (see include/specverify.h).  Draft logits only; T == 0 is greedy (draft
+    may be None).  Raises SpecVerifyError (SPEC_ERR_UNSUPPORTED) for shapes
+    that need a workspace.  Calls must not overlap on the GPU."""
+    B, K1, V = target.shape
+    K = K1 - 1
+    _check(target, (B, K + 1, V), (torch.float32, torch.bfloat16), "target")
+    if T > 0:
+        _check(draft, (B, K, V), (target.dtype,), "draft")
+    _check(draft_tokens, (B, K), (torch.int32,), "draft_tokens")
+    dev = target.device
+    out_tokens, out_accept_len = _outs(B, K, dev, out_tokens, out_accept_len)
+    st = _stream(dev, stream)
+    ax = aux._struct(B, K) if aux is not None else None
+    rc = load().spec_verify_static(target.data_ptr(), _dt(target), draft.data_ptr() if (draft is not None and T > 0)
+                                   else None, draft_tokens.data_ptr(), B, K, V, float(T), int(seed),
+                                   out_tokens.data_ptr(), out_accept_len.data_ptr(),
+                                   ctypes.byref(ax) if ax is not None else None, st)
+    if rc:
+        raise SpecVerifyError(rc, "spec_verify_static")
     return out_tokens, out_accept_len
 
 

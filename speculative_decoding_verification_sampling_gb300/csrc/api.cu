@@ -117,6 +117,10 @@ bool debug_enabled()
 // Co-resident clusters for (kernel, cluster size, shared memory), per device.
 std::map<std::tuple<int, int, int, uint32_t>, int> g_max_clusters;
 
+// Address of the static scratch of spec_verify_static, looked up once per
+// device (with that device current) on its first call there.
+uint32_t *g_static_scratch[kMaxDevices] = {};
+
 uint32_t spin_limit()
 {
     const char *s = std::getenv("SPECVERIFY_SPIN_LIMIT");
@@ -230,9 +234,9 @@ spec_status_t run_sweep(bool greedy, const void *target, spec_dtype_t tdt, const
 spec_status_t run_cluster(bool greedy, const void *target, spec_dtype_t tdt, const void *draft,
                           const int32_t *tokens, int B, int K, int V, float T, uint64_t seed,
                           int32_t *out_tokens, int32_t *out_len, uint32_t *ctl, const spec_aux_t *aux,
-                          void *stream)
+                          void *stream, bool any_choice = false)
 {
-    if (cluster_disabled())
+    if (!any_choice && cluster_disabled())
         return SPEC_ERR_UNSUPPORTED;
     if (aux && (aux->q_draft || aux->p_draft || aux->row_lse) && !greedy)
         return SPEC_ERR_UNSUPPORTED;
@@ -485,6 +489,58 @@ spec_status_t spec_verify_shortlist(const void *target_logits, spec_dtype_t tdt,
     return run(sv::MODE_SHORT, target_logits, tdt, draft_sl, ddt, draft_is_probs, shortlist_idx, S,
                draft_tokens, B, K, V, T, seed, out_tokens, out_accept_len, workspace, workspace_bytes, aux,
                stream);
+}
+
+// Verification without a caller workspace.  Callers that cannot allocate, or
+// cannot hold a workspace per call in flight, use it. Examples: code that
+// runs where device allocation is not allowed, or that keeps a fixed memory
+// plan.  Its scratch is the 256-byte static array in k_cluster.cu (the
+// cluster kernel's control block), so calls share it and must not overlap on
+// the GPU.  Only the cluster kernel's shapes are served; any other shape
+// returns SPEC_ERR_UNSUPPORTED without launching.
+spec_status_t spec_verify_static(const void *target_logits, spec_dtype_t tdt, const void *draft_logits,
+                                 const int32_t *draft_tokens, int B, int K, int V, float T, uint64_t seed,
+                                 int32_t *out_tokens, int32_t *out_accept_len, const spec_aux_t *aux,
+                                 void *stream)
+{
+    if (!sizes_ok(B, K, V, 0) || !target_logits || !draft_tokens || !out_tokens || !out_accept_len)
+        return SPEC_ERR_INVALID_ARG;
+    if (tdt != SPEC_F32 && tdt != SPEC_BF16)
+        return SPEC_ERR_INVALID_ARG;
+    if (!std::isfinite(T) || T < 0.0f)
+        return SPEC_ERR_INVALID_ARG;
+    const bool greedy = T == 0.0f;
+    if (!greedy) {
+        if (!draft_logits)
+            return SPEC_ERR_INVALID_ARG;
+        const double c = 1.4426950408889634 / (double)T;
+        if (!std::isfinite((float)c))
+            return SPEC_ERR_INVALID_ARG;
+    }
+    if (aux && (aux->q_draft || aux->p_draft || aux->row_lse))
+        return SPEC_ERR_UNSUPPORTED;   // per-position outputs need the chunk-scheduled kernel and its workspace
+    int sms = 0, occ = 0;
+    sv::KernelEntry entry{};
+    spec_status_t st = device_setup(&sms, greedy ? sv::MODE_GREEDY : sv::MODE_STOCH,
+                                    tdt == SPEC_BF16 ? 1 : 0, false, &entry, &occ);
+    if (st != SPEC_OK)
+        return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    uint32_t *ctl = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!g_static_scratch[dev]) {
+            uint32_t *p = nullptr;
+            if (sv::static_scratch_address(&p) != cudaSuccess || !p)
+                return SPEC_ERR_CUDA;
+            g_static_scratch[dev] = p;
+        }
+        ctl = g_static_scratch[dev];
+    }
+    return run_cluster(greedy, target_logits, tdt, draft_logits, draft_tokens, B, K, V, T, seed, out_tokens,
+                       out_accept_len, ctl, aux, stream, true);
 }
 
 spec_status_t spec_philox_words(uint64_t seed, uint32_t tag, int B, int P, uint32_t *out, void *stream)

@@ -74,6 +74,20 @@ ClusterEntry make_cluster_entry()
 
 uint32_t cluster_header_bytes() { return CL_HDR; }
 
+// Scratch of spec_verify_static: the cluster kernel's control block lives in
+// this module-scope array instead of a caller workspace.  Zero at load, and
+// left zero by every call that completes.
+static __device__ __align__(256) uint32_t g_static_scratch[STATIC_SCRATCH_WORDS];
+static_assert(STATIC_SCRATCH_WORDS >= CTL_WORDS, "the control block must fit the static scratch");
+
+cudaError_t static_scratch_address(uint32_t **addr)
+{
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    *addr = static_cast<uint32_t *>(p);
+    return e;
+}
+
 ClusterEntry entry_cluster(int tdt, bool greedy)
 {
     if (tdt == 0)

@@ -24,6 +24,11 @@ struct ClusterEntry {
 ClusterEntry entry_cluster(int tdt, bool greedy);
 uint32_t cluster_header_bytes();   // shared memory ahead of the row slices
 
+// Device scratch that needs no caller workspace: 64 words (256 bytes), of
+// which the cluster kernel uses the CTL_WORDS control words.
+constexpr int STATIC_SCRATCH_WORDS = 64;
+cudaError_t static_scratch_address(uint32_t **addr);   // current device
+
 // The sweep kernel: (position, sequence, part) items over persistent CTAs.
 struct SweepEntry {
     cudaError_t (*launch)(const SweepParams &P, int grid, cudaStream_t stream);
