@@ -87,6 +87,11 @@ spec_status_t device_setup(int *sms, int mode, int tdt, bool probs, sv::KernelEn
     return SPEC_OK;
 }
 
+// Batches from this size on go to the sweep kernel first (measured: B=512 K=8
+// 395 us against 462 us for the cluster kernel; B=256 K=4 is faster on the
+// cluster kernel).
+constexpr int kSweepMinB = 512;
+
 // Largest shared-memory footprint per CTA for the cluster kernel: three CTAs
 // (three sequences in flight) per SM at V = 128256 bf16 with clusters of 8.
 constexpr uint32_t kClusterSmemMax = 72 * 1024;
@@ -200,15 +205,27 @@ spec_status_t run_sweep(bool greedy, const void *target, spec_dtype_t tdt, const
     }
     P.ctl = reinterpret_cast<uint32_t *>(w + L.ctl);
     P.reset_words = (uint32_t)((L.reset_end - L.ctl) / 4);
+    P.swc = reinterpret_cast<uint32_t *>(w + L.sw_ctl);
     P.seq = reinterpret_cast<sv::SwSeq *>(w + L.sw_seq);
     P.cnt = reinterpret_cast<uint32_t *>(w + L.sw_cnt);
     P.part = reinterpret_cast<sv::SwStat *>(w + L.sw_part);
     P.stat = reinterpret_cast<sv::SwStat *>(w + L.sw_stat);
+    P.res = reinterpret_cast<sv::SwRes *>(w + L.sw_res);
+    P.res_ready = reinterpret_cast<uint32_t *>(w + L.sw_res_ready);
+    P.res_done = reinterpret_cast<uint32_t *>(w + L.sw_res_done);
+    P.resm = reinterpret_cast<sv::DF2 *>(w + L.sw_resm);
     P.B = B;
     P.K = K;
     P.V = V;
     P.S = S;
     P.span = cdiv(cdiv(V, S), 8) * 8;
+    // sampling jobs in parts of whole stages: about SW_RPARTS of them
+    const int st_tokens = 8192 / es;
+    int rparts = sv::SW_RPARTS;
+    if (const char *e = std::getenv("SPECVERIFY_SWEEP_RPARTS"))
+        rparts = std::max(1, std::atoi(e));
+    P.rspan = cdiv(cdiv(V, rparts), st_tokens) * st_tokens;
+    P.RS = cdiv(V, P.rspan);
     P.greedy = greedy ? 1 : 0;
     P.c = greedy ? 1.0f : (float)(1.4426950408889634 / (double)T);
     P.key0 = (uint32_t)(seed & 0xffffffffu);
@@ -355,6 +372,13 @@ spec_status_t run(int mode, const void *target, spec_dtype_t tdt, const void *dr
         const bool full = aux && (aux->q_draft || aux->p_draft || aux->row_lse);
         if (!(full && mode != sv::MODE_GREEDY)) {
             uint32_t *ctl = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + L.ctl);
+            // large batches: the sweep keeps HBM busier than one sequence per cluster
+            if (B >= kSweepMinB) {
+                const spec_status_t ss = run_sweep(mode == sv::MODE_GREEDY, target, tdt, draft, tokens, B, K, V, T,
+                                                   seed, out_tokens, out_len, workspace, L, aux, stream);
+                if (ss != SPEC_ERR_UNSUPPORTED)
+                    return ss;
+            }
             const spec_status_t cs = run_cluster(mode == sv::MODE_GREEDY, target, tdt, draft, tokens, B, K, V, T,
                                                  seed, out_tokens, out_len, ctl, aux, stream);
             if (cs != SPEC_ERR_UNSUPPORTED)

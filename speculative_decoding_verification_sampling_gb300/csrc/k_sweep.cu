@@ -40,8 +40,8 @@ cudaError_t occupancy_sweep(int *ctas_per_sm)
 SweepEntry entry_sweep(int tdt)
 {
     if (tdt == 0)
-        return SweepEntry{&launch_sweep<F32>, &occupancy_sweep<F32>, WSBH / 4 * WMAXST};
-    return SweepEntry{&launch_sweep<BF16>, &occupancy_sweep<BF16>, WSBH / 2 * WMAXST};
+        return SweepEntry{&launch_sweep<F32>, &occupancy_sweep<F32>, WSBH / 4 * SW_MAXST};
+    return SweepEntry{&launch_sweep<BF16>, &occupancy_sweep<BF16>, WSBH / 2 * SW_MAXST};
 }
 
 }  // namespace sv

@@ -444,10 +444,12 @@ struct ResK {
 // inverse CDF):
 //   q'(x) = 2^(xt c - Mt),
 //   delta = log2(p(x) / q(x)) = (xd - xt) c - dL,
-//   r'(x) = q'(x) (1 - 2^delta) for delta < 0, else 0,
-// with 1 - 2^delta = -expm1(delta ln 2) from its Taylor series on (-1, 0)
-// (no cancellation as delta -> 0; terms to t^8/8!, truncation below 2e-7
-// relative) and from 1 - ex2(delta) below -1.  Tokens with xt = -inf give 0.
+//   r'(x) = q'(x) (1 - 2^delta) for delta < 0, else 0.
+// 1 - 2^delta has no cancellation on [-1, 0) in the form
+// -2 * 2^(delta/2) * sinh(delta ln2 / 2), where sinh is its odd Taylor series
+// to y^9 (|y| <= ln2/2: truncation below 3e-10 relative; about 5e-7 relative
+// with ex2.approx).  Below -1 it is 1 - ex2(delta), where 2^delta < 1/2.  One
+// ex2 serves both branches.  Tokens with xt = -inf give 0.
 template <class E>
 __device__ __forceinline__ void res_group(const uint8_t *bt, const uint8_t *bd, int n, int g, const ResK &k,
                                           bool bonus, bool useq, float *v)
@@ -466,29 +468,29 @@ __device__ __forceinline__ void res_group(const uint8_t *bt, const uint8_t *bd, 
         return;
     }
     (void)group8<E>(bd, g, n, XD);
-    const f2 ndh = pk(-k.dLhi, -k.dLhi), ndl = pk(-k.dLlo, -k.dLlo), ln2 = pk(0.69314718055994531f, 0.69314718055994531f);
+    const f2 ndh = pk(-k.dLhi, -k.dLhi), ndl = pk(-k.dLlo, -k.dLlo);
+    const f2 hl = pk(0.34657359027997264f, 0.34657359027997264f);   // ln2 / 2
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        const f2 dd = fma2(XT[p], pk(-1.0f, -1.0f), XD[p]);          // xd - xt (exact for bf16 inputs)
+        const f2 dd = fma2(XT[p], pk(-1.0f, -1.0f), XD[p]);           // xd - xt (exact for bf16 inputs)
         float d0, d1;
         upk(add2(fma2(dd, cc, ndh), ndl), d0, d1);                    // delta
         d0 = fminf(d0, 0.0f);                                         // also maps NaN (both -inf) to 0
         d1 = fminf(d1, 0.0f);
-        const f2 t = mul2(pk(fmaxf(d0, -1.0f), fmaxf(d1, -1.0f)), ln2);
-        f2 e = pk(-1.0f / 40320.0f, -1.0f / 40320.0f);
-        e = fma2(e, t, pk(-1.0f / 5040.0f, -1.0f / 5040.0f));
-        e = fma2(e, t, pk(-1.0f / 720.0f, -1.0f / 720.0f));
-        e = fma2(e, t, pk(-1.0f / 120.0f, -1.0f / 120.0f));
-        e = fma2(e, t, pk(-1.0f / 24.0f, -1.0f / 24.0f));
-        e = fma2(e, t, pk(-1.0f / 6.0f, -1.0f / 6.0f));
-        e = fma2(e, t, pk(-0.5f, -0.5f));
-        e = fma2(e, t, pk(-1.0f, -1.0f));
-        float o0, o1;
-        upk(mul2(t, e), o0, o1);                                      // 1 - 2^delta on [-1, 0]
-        if (d0 <= -1.0f)
-            o0 = 1.0f - ex2a(d0);
-        if (d1 <= -1.0f)
-            o1 = 1.0f - ex2a(d1);
+        const bool far0 = d0 < -1.0f, far1 = d1 < -1.0f;
+        float e0, e1;
+        upk(ex2x2(pk(far0 ? d0 : 0.5f * d0, far1 ? d1 : 0.5f * d1)), e0, e1);
+        const f2 y = mul2(pk(d0, d1), hl);
+        const f2 y2 = mul2(y, y);
+        f2 sp = pk(1.0f / 362880.0f, 1.0f / 362880.0f);
+        sp = fma2(sp, y2, pk(1.0f / 5040.0f, 1.0f / 5040.0f));
+        sp = fma2(sp, y2, pk(1.0f / 120.0f, 1.0f / 120.0f));
+        sp = fma2(sp, y2, pk(1.0f / 6.0f, 1.0f / 6.0f));
+        sp = fma2(sp, y2, pk(1.0f, 1.0f));
+        float s0, s1;
+        upk(mul2(y, sp), s0, s1);                                     // sinh(delta ln2 / 2)
+        const float o0 = far0 ? 1.0f - e0 : -2.0f * e0 * s0;
+        const float o1 = far1 ? 1.0f - e1 : -2.0f * e1 * s1;
         upk(mul2(Q[p], pk(o0, o1)), v[2 * p], v[2 * p + 1]);
     }
 }
@@ -510,8 +512,8 @@ __device__ __forceinline__ float lane_seg(const uint8_t *bt, const uint8_t *bd, 
     return tree8(v);
 }
 
-// Mass of groups [g0, g1) in token order: 256-token segments, each the sum
-// of its lanes' sums (a float-pair butterfly), accumulated in order.
+// Mass of groups [g0, g1): each lane sums its groups (one per 256-token
+// segment) as a float pair, then one float-pair butterfly over the lanes.
 template <class E>
 __device__ DF warp_mass(const uint8_t *bt, const uint8_t *bd, int n, int g0, int g1, const ResK &k, bool bonus,
                         bool useq, int lane)
@@ -525,10 +527,9 @@ __device__ DF warp_mass(const uint8_t *bt, const uint8_t *bd, int n, int g0, int
             ls[i] = sb + i < nseg ? lane_seg<E>(bt, bd, n, g0, g1, sb + i, k, bonus, useq, lane) : 0.0f;
 #pragma unroll
         for (int i = 0; i < SEGB; ++i)
-            if (sb + i < nseg)
-                W = df_add(W, warp_sum_df(DF{ls[i], 0.0f}));
+            W = df_add(W, DF{ls[i], 0.0f});
     }
-    return W;
+    return warp_sum_df(W);
 }
 
 // Largest token in groups [g0, g1) with positive mass (-1 if none).
