@@ -157,6 +157,31 @@ spec_status_t spec_verify_static(const void *target_logits, spec_dtype_t tdt, co
                                  int32_t *out_tokens, int32_t *out_accept_len, const spec_aux_t *aux,
                                  void *stream);
 
+/* Fused draft-token sampler: the drafting step that precedes verification
+ * (nextadmin.net lesson "Speculative Decoding", § Core algorithm step 2 and
+ * § Build it, spec_step: each drafted token is drawn from the draft
+ * distribution and its probability p_dist[d] is kept for the acceptance test;
+ * aiengineeringfromscratch.com lesson 25, § Build it: softmax of the logits
+ * divided by the temperature).
+ *   draft_logits  [B][K][V]  dtype `ddt`; row (b, i) is the drafter's output at
+ *                            position i of sequence b (already conditioned on
+ *                            the earlier drafts)
+ *   out_tokens    [B][K]     int32: d_i = the smallest x whose running sum of
+ *                            softmax(z / T) in ascending token order exceeds
+ *                            v * R (R the total), v = word 0 of Philox4x32-10
+ *                            with counter (i, b, 1, 0) and key (seed low, seed
+ *                            high), mapped by ((w >> 8) + 0.5) * 2^-24
+ *   out_prob      [B][K]     float: p_i(d_i) (may be NULL)
+ *   device_status [1]        set to 0, or SPEC_ERR_NONFINITE when some row has a
+ *                            NaN or +inf logit or is -inf everywhere (that row
+ *                            gets token -1 and probability NaN); may be NULL
+ * T == 0 drafts greedily: the first index of the largest logit, probability 1.
+ * Limits: B, K, V >= 1, B * K <= 2^30, V <= 2093056, T finite and >= 0.
+ * No workspace; the call is asynchronous on `stream`.                         */
+spec_status_t spec_draft_sample(const void *draft_logits, spec_dtype_t ddt, int B, int K, int V, float T,
+                                uint64_t seed, int32_t *out_tokens, float *out_prob, int32_t *device_status,
+                                void *stream);
+
 /* Philox4x32-10 words as the verification kernels draw them, for checking:
  * out[(b * P + pos) * 4 + w] = word w of Philox(counter (pos, b, tag, 0),
  * key (seed low, seed high)) for b < B, pos < P.  `out` is a device pointer of

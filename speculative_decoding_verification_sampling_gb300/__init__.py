@@ -22,7 +22,7 @@ from .build import LIB as _LIB_PATH
 
 __all__ = [
     "SpecVerifyError", "Aux", "spec_verify", "spec_verify_greedy", "spec_verify_shortlist",
-    "spec_workspace_bytes", "spec_philox_words", "spec_status_string", "spec_launch_count", "spec_verify_static", "library_path", "load",
+    "spec_workspace_bytes", "spec_philox_words", "spec_draft_sample", "spec_status_string", "spec_launch_count", "spec_verify_static", "library_path", "load",
 ]
 
 SPEC_F32, SPEC_BF16 = 0, 1
@@ -75,6 +75,8 @@ def load():
             lib.spec_status_string.restype = ctypes.c_char_p
             lib.spec_verify_static.argtypes = [P, I, P, P, I, I, I, F, U64, P, P, P, P]
             lib.spec_verify_static.restype = I
+            lib.spec_draft_sample.argtypes = [P, I, I, I, I, F, U64, P, P, P, P]
+            lib.spec_draft_sample.restype = I
             lib.spec_launch_count.argtypes = []
             lib.spec_launch_count.restype = U64
             _lib = lib
@@ -296,3 +298,29 @@ def spec_philox_words(seed: int, tag: int, B: int, P: int, device=None, stream=N
     if rc:
         raise SpecVerifyError(rc, "spec_philox_words")
     return out
+
+
+def spec_draft_sample(draft: torch.Tensor, T: float, seed: int, *, out_tokens=None, out_prob=None,
+                      device_status=None, stream=None):
+    """Draft tokens d_i ~ softmax(draft[b][i] / T) by inverse CDF on Philox
+    uniforms (counter (i, b, 1, 0)), with p_i(d_i).  draft [B][K][V] float32 or
+    bfloat16 logits.  T == 0 takes the first argmax (probability 1).  Returns
+    (out_tokens [B][K] int32, out_prob [B][K] float32) on the device."""
+    B, K, V = draft.shape
+    _check(draft, (B, K, V), (torch.float32, torch.bfloat16), "draft")
+    dev = draft.device
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K), dtype=torch.int32, device=dev)
+    if out_prob is None:
+        out_prob = torch.empty((B, K), dtype=torch.float32, device=dev)
+    _check(out_tokens, (B, K), (torch.int32,), "out_tokens")
+    _check(out_prob, (B, K), (torch.float32,), "out_prob")
+    if device_status is not None:
+        _check(device_status, (1,), (torch.int32,), "device_status")
+    st = _stream(dev, stream)
+    rc = load().spec_draft_sample(draft.data_ptr(), _dt(draft), B, K, V, float(T), int(seed) & (2**64 - 1),
+                                  out_tokens.data_ptr(), out_prob.data_ptr(),
+                                  device_status.data_ptr() if device_status is not None else None, st)
+    if rc:
+        raise SpecVerifyError(rc, "spec_draft_sample")
+    return out_tokens, out_prob

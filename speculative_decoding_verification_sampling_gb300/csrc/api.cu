@@ -578,6 +578,23 @@ spec_status_t spec_philox_words(uint64_t seed, uint32_t tag, int B, int P, uint3
     return SPEC_OK;
 }
 
+spec_status_t spec_draft_sample(const void *draft_logits, spec_dtype_t ddt, int B, int K, int V, float T,
+                                uint64_t seed, int32_t *out_tokens, float *out_prob, int32_t *device_status,
+                                void *stream)
+{
+    if (!draft_logits || !out_tokens || B < 1 || K < 1 || V < 1 || (ddt != SPEC_F32 && ddt != SPEC_BF16))
+        return SPEC_ERR_INVALID_ARG;
+    if (!(T >= 0.0f) || !std::isfinite(T) || (long long)B * K > (1LL << 30))
+        return SPEC_ERR_INVALID_ARG;
+    if (V > sv::draft_max_v())
+        return SPEC_ERR_UNSUPPORTED;
+    if (sv::launch_draft_sample(draft_logits, ddt == SPEC_BF16 ? 1 : 0, B, K, V, T, seed, out_tokens, out_prob,
+                                device_status, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return SPEC_OK;
+}
+
 uint64_t spec_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char *spec_status_string(spec_status_t status)

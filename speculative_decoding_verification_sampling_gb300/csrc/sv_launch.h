@@ -37,6 +37,11 @@ struct SweepEntry {
 };
 SweepEntry entry_sweep(int tdt);
 
+// The fused draft-token sampler (k_draft.cu): one CTA per row of draft logits.
+int draft_max_v();
+cudaError_t launch_draft_sample(const void *draft, int tdt, int B, int K, int V, float T, uint64_t seed,
+                                int32_t *out_tokens, float *out_prob, int32_t *status, cudaStream_t stream);
+
 cudaError_t launch_philox_words(uint32_t k0, uint32_t k1, uint32_t tag, int B, int P, uint32_t *out,
                                 cudaStream_t stream);
 

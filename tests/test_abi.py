@@ -99,3 +99,20 @@ def test_binding_rejects_cpu_tensors():
     t = torch.zeros(1, 5, 16)
     with pytest.raises(TypeError):
         sv.spec_verify(t, t[:, :4].contiguous(), torch.zeros(1, 4, dtype=torch.int32), 1.0, 0)
+
+
+def test_draft_sample_rejects_bad_arguments():
+    """Argument errors come back before anything is launched."""
+    lib = sv.load()
+    p = ctypes.c_void_p(256)
+    n0 = sv.spec_launch_count()
+    assert lib.spec_draft_sample(None, 1, 1, 1, 8, 1.0, 0, p, None, None, None) == 1
+    assert lib.spec_draft_sample(p, 1, 0, 1, 8, 1.0, 0, p, None, None, None) == 1
+    assert lib.spec_draft_sample(p, 1, 1, 0, 8, 1.0, 0, p, None, None, None) == 1
+    assert lib.spec_draft_sample(p, 1, 1, 1, 0, 1.0, 0, p, None, None, None) == 1
+    assert lib.spec_draft_sample(p, 1, 1, 1, 8, -1.0, 0, p, None, None, None) == 1
+    assert lib.spec_draft_sample(p, 1, 1, 1, 8, float("nan"), 0, p, None, None, None) == 1
+    assert lib.spec_draft_sample(p, 1, 1, 1, 8, float("inf"), 0, p, None, None, None) == 1
+    assert lib.spec_draft_sample(p, 7, 1, 1, 8, 1.0, 0, p, None, None, None) == 1
+    assert lib.spec_draft_sample(p, 1, 1, 1, 1 << 22, 1.0, 0, p, None, None, None) == 5
+    assert sv.spec_launch_count() == n0
