@@ -20,10 +20,12 @@ Besides the device-timed value the JSON line carries:
   e2e          - the same metric through the public call with host buffers:
                  every step copies its inputs from pinned host memory and
                  reads its outputs back;
-  roofline     - HBM roofline of the verification kernel: the logits the
-                 left-to-right rule must read (rows up to the first rejection,
-                 or all 2K+1 rows when every draft is accepted) over the mean
-                 kernel duration, against the measured copy bandwidth;
+  roofline     - HBM roofline of the verification call (its four kernels,
+                 timed together with CUDA events around each call): the logits
+                 the left-to-right rule must read (rows up to the first
+                 rejection, or all 2K+1 rows when every draft is accepted) over
+                 the mean call duration, against the measured copy bandwidth;
+                 `traffic` is the DRAM bytes of all four kernels of one call;
   cpu_baseline - the float64 CPU oracle on this host's cores, on a bounded
                  sample of the same batch (rank 0, one GPU only);
   clocks       - SM clocks and throttle reasons sampled during the run.
@@ -57,7 +59,10 @@ TEMPERATURE = 1.0
 DATA_SEED = 5          # seed of the synthetic batch on rank 0 (rank r uses DATA_SEED + r)
 VERIFY_SEED = 7        # Philox key of the verification uniforms
 CSRC = os.path.join(_ROOT, "speculative_decoding_verification_sampling_gb300", "csrc")
-TRAFFIC_RECORD = os.path.join(_ROOT, "profiles", "cluster_kernel_stoch_b256_k4.md")
+TRAFFIC_RECORD = os.path.join(_ROOT, "profiles", "rows_kernels_stoch_b256_k4.md")
+# What one call launches at this workload (the library's dispatch): the
+# row-parallel kernels, two statistics launches, the residual masses, the sampling.
+PATH_KERNELS = "vr_stats x2 + vr_residual + vr_sample (row-parallel verification, stochastic, bf16)"
 REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
 
@@ -127,10 +132,10 @@ def kernel_sources_digest() -> str:
 
 
 def recorded_traffic(path: str = TRAFFIC_RECORD, digest: str | None = None):
-    """DRAM bytes per launch from a committed ncu summary, or None when the
-    summary is missing or was taken on other kernel sources.  The summary
-    holds the lines `traffic_bytes_per_launch: <int>` and
-    `kernel_sources_sha256: <hex>`."""
+    """DRAM bytes per verification call from a committed ncu summary, or None
+    when the summary is missing or was taken on other kernel sources.  The
+    summary holds the lines `traffic_bytes_per_launch: <int>` (per call, all
+    its kernels) and `kernel_sources_sha256: <hex>`."""
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -442,7 +447,7 @@ def run_gb300(args) -> int:
         line["roofline"] = {
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": recorded_traffic(digest=digest), "peak_source": src,
-            "kernel": "cluster_kernel (stochastic, bf16)",
+            "kernel": PATH_KERNELS, "scope": "the whole verification call (all its kernels)",
             "algorithmic_bytes_per_launch": alg_bytes, "mean_kernel_us": mean_kernel_s * 1e6,
             "all_rows_bytes_per_launch": all_rows_bytes,
             "all_rows_gbs": all_rows_bytes / mean_kernel_s / 1e9,

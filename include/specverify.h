@@ -190,8 +190,10 @@ spec_status_t spec_philox_words(uint64_t seed, uint32_t tag, int B, int P, uint3
                                 void *stream);
 
 /* Number of kernels this library has launched in this process, over every
- * entry point and device (one per successful spec_verify* call, one per
- * spec_philox_words call).  For accounting; thread-safe.                      */
+ * entry point and device: a successful spec_verify* call launches one kernel,
+ * or three or four when the row-parallel kernels serve it (large stochastic
+ * batches); spec_draft_sample and spec_philox_words launch one each.  For
+ * accounting; thread-safe.                                                   */
 uint64_t spec_launch_count(void);
 
 /* A static description of a status code. */

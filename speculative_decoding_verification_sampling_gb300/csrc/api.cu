@@ -96,11 +96,16 @@ constexpr int kSweepMinB = 512;
 // (three sequences in flight) per SM at V = 128256 bf16 with clusters of 8.
 constexpr uint32_t kClusterSmemMax = 72 * 1024;
 
-// Kernel choice (SPECVERIFY_KERNEL).  By default the cluster kernel (which
-// holds its slices in shared memory) serves every call it applies to, then
-// the sweep kernel, then the chunk-scheduled kernel.  "sweep" skips the
-// cluster kernel; "general" forces the chunk-scheduled kernel.
-enum KernelChoice { KC_AUTO = 0, KC_SWEEP = 1, KC_GENERAL = 2 };
+// Stochastic calls with at least this many logit rows (B (2K + 1)) go to the
+// row-parallel kernels: measured faster than the cluster and sweep kernels
+// from B = 32, K = 7 and B = 64, K = 4 up (B = 256, K = 4: 160 us against
+// 202 us); smaller calls cannot fill the GPU with rows.
+constexpr long long kRowsMinRows = 256;
+
+// Kernel choice (SPECVERIFY_KERNEL), for measurement and tests.  By default
+// the dispatch in run() picks the kernel; "cluster", "sweep" and "rows" skip
+// the others of those three; "general" forces the chunk-scheduled kernel.
+enum KernelChoice { KC_AUTO = 0, KC_SWEEP = 1, KC_GENERAL = 2, KC_ROWS = 3, KC_CLUSTER = 4 };
 KernelChoice kernel_choice()
 {
     const char *s = std::getenv("SPECVERIFY_KERNEL");
@@ -108,9 +113,13 @@ KernelChoice kernel_choice()
         return KC_GENERAL;
     if (s && std::strcmp(s, "sweep") == 0)
         return KC_SWEEP;
+    if (s && std::strcmp(s, "rows") == 0)
+        return KC_ROWS;
+    if (s && std::strcmp(s, "cluster") == 0)
+        return KC_CLUSTER;
     return KC_AUTO;
 }
-bool cluster_disabled() { return kernel_choice() != KC_AUTO; }
+bool cluster_disabled() { return kernel_choice() != KC_AUTO && kernel_choice() != KC_CLUSTER; }
 
 // SPECVERIFY_DEBUG=1 prints each launch's geometry to stderr.
 bool debug_enabled()
@@ -243,6 +252,57 @@ spec_status_t run_sweep(bool greedy, const void *target, spec_dtype_t tdt, const
     return SPEC_OK;
 }
 
+// Row-parallel verification (k_rows.cu): logit draft rows (or greedy), no
+// shortlist.  Serves the per-position outputs too (then every row is read).
+spec_status_t run_rows(bool greedy, const void *target, spec_dtype_t tdt, const void *draft, const int32_t *tokens,
+                       int B, int K, int V, float T, uint64_t seed, int32_t *out_tokens, int32_t *out_len,
+                       void *workspace, const sv::WsLayout &L, const spec_aux_t *aux, void *stream)
+{
+    if ((long long)B * (2 * K + 1) > INT32_MAX || (long long)B * sv::rows_chunks() > INT32_MAX)
+        return SPEC_ERR_UNSUPPORTED;
+    const int es = tdt == SPEC_F32 ? 4 : 2;
+    char *w = static_cast<char *>(workspace);
+    sv::RowsParams P{};
+    P.target = target;
+    P.draft = greedy ? nullptr : draft;
+    P.tokens = tokens;
+    P.out_tokens = out_tokens;
+    P.out_len = out_len;
+    if (aux) {
+        P.aux_q = aux->q_draft;
+        P.aux_p = aux->p_draft;
+        P.aux_R = aux->residual_mass;
+        P.aux_lse = aux->row_lse;
+        P.aux_status = aux->device_status;
+    }
+    P.stat = reinterpret_cast<sv::VrStat *>(w + L.vr_stat);
+    P.pair = reinterpret_cast<uint32_t *>(w + L.vr_pair);
+    P.rej = reinterpret_cast<uint32_t *>(w + L.vr_rej);
+    P.errc = reinterpret_cast<int32_t *>(w + L.vr_errc);
+    P.rowcnt = reinterpret_cast<uint32_t *>(w + L.vr_rowcnt);
+    P.vpart = reinterpret_cast<sv::VrStat *>(w + L.vr_part);
+    P.segm = reinterpret_cast<sv::VrSeg *>(w + L.vr_segm);
+    P.B = B;
+    P.K = K;
+    P.V = V;
+    P.nseg = (V + sv::rows_segment_tokens() - 1) / sv::rows_segment_tokens();
+    P.nch = sv::rows_chunks();
+    P.greedy = greedy ? 1 : 0;
+    P.skip = (P.aux_q || P.aux_p || P.aux_lse) ? 0 : 1;
+    P.vec = ((long long)V * es) % 16 == 0 && reinterpret_cast<uintptr_t>(target) % 16 == 0 &&
+            (greedy || reinterpret_cast<uintptr_t>(draft) % 16 == 0);
+    P.c = greedy ? 1.0f : (float)(1.4426950408889634 / (double)T);
+    P.key0 = (uint32_t)(seed & 0xffffffffu);
+    P.key1 = (uint32_t)(seed >> 32);
+    if (debug_enabled())
+        std::fprintf(stderr, "specverify: rows kernels %s %s B=%d K=%d V=%d skip=%d vec=%d\n",
+                     greedy ? "greedy" : "stochastic", tdt == SPEC_BF16 ? "bf16" : "f32", B, K, V, P.skip, P.vec);
+    if (sv::launch_rows(P, tdt == SPEC_BF16 ? 1 : 0, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    g_launches.fetch_add((uint64_t)sv::rows_launches(K, greedy), std::memory_order_relaxed);
+    return SPEC_OK;
+}
+
 // One sequence per cluster (sv_cluster.cuh).  Applies to stochastic
 // verification with draft logits and to greedy verification, when no
 // per-position output is requested, rows start 16-byte aligned and one CTA's
@@ -370,10 +430,25 @@ spec_status_t run(int mode, const void *target, spec_dtype_t tdt, const void *dr
 
     if (mode == sv::MODE_GREEDY || (mode == sv::MODE_STOCH && !probs)) {
         const bool full = aux && (aux->q_draft || aux->p_draft || aux->row_lse);
+        const KernelChoice kc = kernel_choice();
+        if (kc == KC_ROWS) {
+            const spec_status_t rs = run_rows(mode == sv::MODE_GREEDY, target, tdt, draft, tokens, B, K, V, T, seed,
+                                              out_tokens, out_len, workspace, L, aux, stream);
+            if (rs != SPEC_ERR_UNSUPPORTED)
+                return rs;
+        }
+        // stochastic calls with enough rows to fill the GPU: the row-parallel kernels
+        // (they also serve the per-position outputs)
+        if (kc == KC_AUTO && mode == sv::MODE_STOCH && (long long)B * (2 * K + 1) >= kRowsMinRows) {
+            const spec_status_t rs = run_rows(false, target, tdt, draft, tokens, B, K, V, T, seed, out_tokens,
+                                              out_len, workspace, L, aux, stream);
+            if (rs != SPEC_ERR_UNSUPPORTED)
+                return rs;
+        }
         if (!(full && mode != sv::MODE_GREEDY)) {
             uint32_t *ctl = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + L.ctl);
             // large batches: the sweep keeps HBM busier than one sequence per cluster
-            if (B >= kSweepMinB) {
+            if (kc == KC_AUTO && B >= kSweepMinB) {
                 const spec_status_t ss = run_sweep(mode == sv::MODE_GREEDY, target, tdt, draft, tokens, B, K, V, T,
                                                    seed, out_tokens, out_len, workspace, L, aux, stream);
                 if (ss != SPEC_ERR_UNSUPPORTED)

@@ -1,0 +1,778 @@
+// k_rows.cu -- row-parallel verification: three kernels in stream order.
+//
+// The rule is that of the other kernels (nextadmin.net lesson "Speculative
+// Decoding", § Core algorithm steps 4-6; aiengineeringfromscratch.com lesson
+// 25, § The exact rule and § Greedy case; q = target, p = draft).  Here the
+// work is cut by rows instead of by sequences, so that every SM streams
+// independent rows at full bandwidth:
+//   1. vr_stats: one launch per position, one CTA per logit row of that
+//      position.  It streams the row once (16-byte loads, four in flight per
+//      thread) into its reference and sum (greedy: its argmax) and keeps the
+//      logit at the drafted token.  The CTA completing the second row of a
+//      position decides it; a rejection (or an error) sets the position's bit
+//      in the sequence's mask.  Rows of a sequence with a bit below their
+//      position skip their reads, so only the rows the left-to-right rule
+//      examines are streamed.
+//   2. vr_residual: eight CTAs per sequence.  The mask gives the position j
+//      where the sequence ends; each CTA streams its eighth of row pair j into
+//      residual masses r' = q' (1 - 2^delta)_+ and target masses q' per
+//      256-token segment, in token order.
+//   3. vr_sample: one CTA per sequence.  It scans the segment masses for the
+//      one crossing v * R, reads that segment again and locates the token
+//      (inverse CDF in ascending token order); it writes the outputs and
+//      re-zeroes the sequence's control words.
+// Greedy verification runs kernels 1 and 3 only.
+#include "sv_cluster.cuh"
+#include "sv_launch.h"
+
+#include <algorithm>
+
+namespace sv {
+namespace {
+
+constexpr int VR_NCH = 8;      // vr_residual CTAs per sequence
+constexpr int VRT = 256;       // threads of a vr_residual CTA
+constexpr int VST = 128;       // threads of a vr_sample CTA
+constexpr int VSEG = 256;      // tokens per residual segment (one per lane-unit of a warp)
+
+// Tokens [x0, x0 + 8) of a row as four float pairs (-inf at or past V).
+template <class E>
+struct Unit {
+    uint4 a, b;   // raw 16-byte loads (b only for float32)
+};
+template <class E>
+__device__ __forceinline__ Unit<E> fetch_unit(const uint8_t *row, int x0, int V, bool vec)
+{
+    Unit<E> u{};
+    if (vec && x0 + 8 <= V) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(row + (size_t)x0 * E::ES);
+        u.a = __ldg(p);
+        if constexpr (E::ES == 4)
+            u.b = __ldg(p + 1);
+        return u;
+    }
+    uint32_t w[8];
+    if constexpr (E::ES == 2) {
+        const uint16_t *h = reinterpret_cast<const uint16_t *>(row);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t lo = x0 + 2 * k < V ? (uint32_t)__ldg(h + x0 + 2 * k) : 0xff80u;
+            const uint32_t hi = x0 + 2 * k + 1 < V ? (uint32_t)__ldg(h + x0 + 2 * k + 1) : 0xff80u;
+            w[k] = lo | (hi << 16);
+        }
+        u.a = make_uint4(w[0], w[1], w[2], w[3]);
+    } else {
+        const uint32_t *f = reinterpret_cast<const uint32_t *>(row);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            w[k] = x0 + k < V ? __ldg(f + x0 + k) : 0xff800000u;
+        u.a = make_uint4(w[0], w[1], w[2], w[3]);
+        u.b = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+    return u;
+}
+template <class E>
+__device__ __forceinline__ void unit_pairs(const Unit<E> &u, f2 *X)
+{
+    if constexpr (E::ES == 2) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+            X[p] = E::pair(u.a, p);
+    } else {
+        X[0] = E::pair(u.a, 0);
+        X[1] = E::pair(u.a, 1);
+        X[2] = E::pair(u.b, 0);
+        X[3] = E::pair(u.b, 1);
+    }
+}
+
+__device__ __forceinline__ VrStat ld_vrstat(const VrStat *p)
+{
+    const float4 a = __ldcg(reinterpret_cast<const float4 *>(p));
+    const float4 b = __ldcg(reinterpret_cast<const float4 *>(p) + 1);
+    return VrStat{a.x, a.y, a.z, __float_as_int(a.w), b.x, 0, 0, 0};
+}
+__device__ __forceinline__ uint32_t vr_atom_add(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// Decide position i of sequence b from the statistics of its target row t and
+// draft row d (the drafted token dt).  Returns 0 and sets accept, or a status
+// code.  Checks in the oracle's order: token, target row, draft row.
+__device__ __forceinline__ int vr_decide(const RowsParams &P, int b, int i, int dt, const VrStat &t,
+                                         const VrStat &d, bool &accept)
+{
+    accept = false;
+    if (i < P.K && !(dt >= 0 && dt < P.V))
+        return ST_TOKEN;
+    if (P.greedy) {
+        const int g = __float_as_int(t.s_hi);
+        if ((t.flags & VR_BAD) || !(t.m > -F_INF) || g < 0)
+            return ST_NONFINITE;
+        accept = i < P.K && g == dt;
+        return 0;
+    }
+    if ((t.flags & VR_BAD) || !(t.m > -F_INF) || !(t.s_hi > 0.0f))
+        return ST_NONFINITE;
+    if (i == P.K)
+        return 0;
+    if ((d.flags & VR_BAD) || !(d.m > -F_INF) || !(d.s_hi > 0.0f))
+        return ST_NONFINITE;
+    int et, ed;
+    float ft, fd;
+    log2_split(DF{t.s_hi, t.s_lo}, et, ft);
+    log2_split(DF{d.s_hi, d.s_lo}, ed, fd);
+    const float zt = t.zd, zd = d.zd;
+    // p(d) == 0 (or below the float64 range) accepts
+    const float lp = zd * P.c - d.m - ((float)ed + fd);
+    if (zd == -F_INF || lp < -1074.5f) {
+        accept = true;
+        return 0;
+    }
+    // log2(q(d) / p(d)) = (zt - zd) c - (Mt - Md) - (log2 St - log2 Sd)
+    const float X = (zt - zd) * P.c - ((t.m - d.m) + ((float)(et - ed) + (ft - fd)));
+    const uint4 w = philox10((uint32_t)i, (uint32_t)b, 0u, 0u, P.key0, P.key1);
+    const float u = ((float)(w.x >> 8) + 0.5f) * (1.0f / 16777216.0f);
+    accept = X >= 0.0f || u < ex2a(X);
+    return 0;
+}
+
+// Where sequence b ends, from the decisions of the row kernels: the first
+// position decided against (its status in errc; 0 for a plain rejection), or
+// K when all K drafts were accepted (errc[K] if the bonus row is in error).
+// Every position before it was computed and accepted: none of its rows could
+// skip, and the second of its rows to finish decided it.
+__device__ __forceinline__ int vr_end(const RowsParams &P, int b, int &j)
+{
+    const uint32_t m = __ldcg(P.rej + b);
+    j = m ? __ffs(m) - 1 : P.K;
+    return (m >> j) & 1u ? __ldcg(P.errc + (size_t)b * (P.K + 1) + j) : 0;
+}
+
+// ---------------------------------------------------------------- 1. row statistics
+template <class E, int VT>
+__global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParams P)
+{
+    constexpr int NW = VT / 32;
+    __shared__ float sm_m[NW], sm_hi[NW], sm_lo[NW];
+    __shared__ int sm_i[NW], sm_f[NW];
+    __shared__ float sm_zd;
+    __shared__ int sm_skip;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int K = P.K, V = P.V;
+    // this launch's rows, position-major over [P.pos, P.pos + P.npos): the
+    // target and draft rows of each sequence side by side (the target row
+    // alone for greedy and at position K), each cut into P.parts parts of
+    // P.span tokens, one CTA each
+    const int rpp = P.greedy ? P.B : 2 * P.B;   // rows of a position below K
+    const int rg = (int)blockIdx.x / P.parts, part = (int)blockIdx.x % P.parts;
+    const int i = P.pos + rg / rpp;
+    const int rl = rg % rpp;
+    const bool pairs = !P.greedy && i < K;
+    const int b = P.greedy ? rl : rl >> 1;
+    const int kind = P.greedy ? 0 : rl & 1;
+    if (kind && i == K)
+        return;   // position K has no draft row
+    const size_t ridx = (size_t)b * (2 * K + 1) + (kind ? K + 1 + i : i);
+    if (P.skip && i > 0) {
+        // a rejection (or error) decided at an earlier position makes this row unneeded
+        if (tid == 0) {
+            const uint32_t m = __ldcg(P.rej + b);
+            sm_skip = (m & ((1u << i) - 1u)) != 0u;
+        }
+        __syncthreads();
+        if (sm_skip) {
+            if (tid == 0 && part == 0)
+                P.stat[ridx] = VrStat{-F_INF, 0.0f, 0.0f, VR_SKIP, 0.0f, 0, 0, 0};
+            return;
+        }
+    }
+    const uint8_t *row = kind ? static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + i) * (size_t)V * E::ES
+                              : static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + i) * (size_t)V * E::ES;
+    const int dt = i < K ? __ldg(P.tokens + (size_t)b * K + i) : -1;
+    const int t0 = min(V, part * P.span), t1 = min(V, t0 + P.span);
+    const int u0 = t0 / 8, nu = (t1 - t0 + 7) / 8;   // this part's units of 8 tokens
+    const float c = P.c;
+    float mc = -F_INF, s = 0.0f, bv = -F_INF, zd = 0.0f;
+    int fl = 0, bi = -1;
+    bool hz = false;
+    // four units in flight per thread; each buffer is refilled right after its use
+    Unit<E> u[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        if (tid + k * VT < nu)
+            u[k] = fetch_unit<E>(row, (u0 + tid + k * VT) * 8, t1, P.vec);
+    for (int g0 = tid; g0 < nu; g0 += 4 * VT) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int g = g0 + k * VT;
+            if (g < nu) {
+                f2 X[4];
+                unit_pairs<E>(u[k], X);
+                if (g + 4 * VT < nu)
+                    u[k] = fetch_unit<E>(row, (u0 + g + 4 * VT) * 8, t1, P.vec);
+                const int x0 = (u0 + g) * 8;
+                if ((unsigned)(dt - x0) < 8u || P.greedy) {
+                    float x[8];
+#pragma unroll
+                    for (int p = 0; p < 4; ++p)
+                        upk(X[p], x[2 * p], x[2 * p + 1]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        if (dt == x0 + e) {
+                            zd = x[e];
+                            hz = true;
+                        }
+                        if (P.greedy) {
+                            if (!(x[e] == x[e]) || x[e] == F_INF)
+                                fl |= VR_BAD;
+                            else if (x[e] > bv)
+                                bv = x[e], bi = x0 + e;
+                        }
+                    }
+                }
+                if (!P.greedy)
+                    acc_group(X, c, mc, s, fl, VR_BAD);
+            }
+        }
+    }
+    fl = warp_or(fl);
+    if (hz)
+        sm_zd = zd;
+    if (P.greedy) {
+#pragma unroll
+        for (int o = 16; o; o >>= 1)
+            argmax_merge(bv, bi, __shfl_xor_sync(0xffffffffu, bv, o), __shfl_xor_sync(0xffffffffu, bi, o));
+        if (lane == 0) {
+            sm_m[warp] = bv;
+            sm_i[warp] = bi;
+            sm_f[warp] = fl;
+        }
+    } else {
+        float M;
+        DF S;
+        merge_ms<32>(mc, DF{s, 0.0f}, c, M, S);
+        if (lane == 0) {
+            sm_m[warp] = M;
+            sm_hi[warp] = S.hi;
+            sm_lo[warp] = S.lo;
+            sm_f[warp] = fl;
+        }
+    }
+    __syncthreads();
+    if (warp != 0)
+        return;
+    const bool in = lane < NW;
+    VrStat st{};
+    st.flags = warp_or(in ? sm_f[lane] : 0);
+    if ((unsigned)(dt - t0) < (unsigned)(t1 - t0)) {
+        st.zd = sm_zd;
+        st.flags |= VR_HASD;
+    }
+    if (P.greedy) {
+        float v = in ? sm_m[lane] : -F_INF;
+        int ix = in ? sm_i[lane] : -1;
+        warp_merge_argmax<NW>(v, ix);
+        st.m = v;
+        st.s_hi = __int_as_float(ix);
+    } else {
+        float M;
+        DF S;
+        merge_ms<NW>(in ? sm_m[lane] : -F_INF, in ? DF{sm_hi[lane], sm_lo[lane]} : DF{0.0f, 0.0f}, c, M, S);
+        st.m = M;
+        st.s_hi = S.hi;
+        st.s_lo = S.lo;
+    }
+    if (lane != 0)
+        return;
+    if (P.parts > 1) {
+        // the last part of the row to finish merges the parts, in part order
+        VrStat *pp = P.vpart + ridx * VR_SMAX;
+        pp[part] = st;
+        if (vr_atom_add(P.rowcnt + ridx, 1u) != (uint32_t)(P.parts - 1))
+            return;
+        VrStat m{};
+        float Mx = -F_INF;
+        for (int h = 0; h < P.parts; ++h) {
+            const VrStat q = ld_vrstat(pp + h);
+            m.flags |= q.flags;
+            if (q.flags & VR_HASD)
+                m.zd = q.zd;
+            if (P.greedy) {
+                if (h == 0) {
+                    m.m = q.m;
+                    m.s_hi = q.s_hi;
+                } else {
+                    int ix = __float_as_int(m.s_hi);
+                    argmax_merge(m.m, ix, q.m, __float_as_int(q.s_hi));
+                    m.s_hi = __int_as_float(ix);
+                }
+            } else {
+                Mx = fmaxf(Mx, q.m);
+            }
+        }
+        if (!P.greedy) {
+            DF S{0.0f, 0.0f};
+            for (int h = 0; h < P.parts; ++h) {
+                const VrStat q = ld_vrstat(pp + h);
+                if (q.m > -F_INF)
+                    S = df_add(S, df_scale_pow2(DF{q.s_hi, q.s_lo}, q.m - Mx));
+            }
+            m.m = Mx;
+            m.s_hi = S.hi;
+            m.s_lo = S.lo;
+        }
+        st = m;
+    }
+    P.stat[ridx] = st;
+    // the second row of a position to finish decides it (greedy and position K:
+    // the only row); a rejection or an error sets the position's bit
+    VrStat t = st, d{};
+    if (pairs) {
+        if (vr_atom_add(P.pair + (size_t)b * (K + 1) + i, 1u) != 1u)
+            return;
+        const VrStat o = ld_vrstat(P.stat + (size_t)b * (2 * K + 1) + (kind ? i : K + 1 + i));
+        t = kind ? o : st;
+        d = kind ? st : o;
+    }
+    bool acc = false;
+    const int code = vr_decide(P, b, i, dt, t, d, acc);
+    if (code || (!acc && i < K)) {
+        P.errc[(size_t)b * (K + 1) + i] = code;
+        atomicOr(P.rej + b, 1u << i);
+    }
+}
+
+// ---------------------------------------------------------------- 2. residual masses
+// q'(x) = 2^(xt c - Mt) and r'(x) = q'(x) (1 - 2^delta)_+ for 8 tokens, delta =
+// (xd - xt) c - dL (both scaled by the target's normaliser, which cancels in
+// the inverse CDF).  1 - 2^delta on [-1, 0) is -2 * 2^(delta/2) * sinh(delta
+// ln2 / 2) with sinh as its odd Taylor series to y^9, so nothing cancels as
+// q -> p; below -1 it is 1 - 2^delta.  With qonly (the bonus row) r' = q'.
+__device__ __forceinline__ void vr_res8(const f2 *XT, const f2 *XD, const ResK &k, bool qonly, float *r, float *q)
+{
+    const f2 cc = pk(k.c, k.c), nMt = pk(-k.Mt, -k.Mt);
+    f2 Q[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        Q[p] = ex2x2(fma2(XT[p], cc, nMt));
+        upk(Q[p], q[2 * p], q[2 * p + 1]);
+    }
+    if (qonly) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            r[e] = q[e];
+        return;
+    }
+    const f2 ndh = pk(-k.dLhi, -k.dLhi), ndl = pk(-k.dLlo, -k.dLlo);
+    const f2 hl = pk(0.34657359027997264f, 0.34657359027997264f);   // ln2 / 2
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const f2 dd = fma2(XT[p], pk(-1.0f, -1.0f), XD[p]);           // xd - xt
+        float d0, d1;
+        upk(add2(fma2(dd, cc, ndh), ndl), d0, d1);                    // delta
+        d0 = fminf(d0, 0.0f);                                         // also maps NaN (both -inf) to 0
+        d1 = fminf(d1, 0.0f);
+        const bool far0 = d0 < -1.0f, far1 = d1 < -1.0f;
+        float e0, e1;
+        upk(ex2x2(pk(far0 ? d0 : 0.5f * d0, far1 ? d1 : 0.5f * d1)), e0, e1);
+        const f2 y = mul2(pk(d0, d1), hl);
+        const f2 y2 = mul2(y, y);
+        f2 sp = pk(1.0f / 362880.0f, 1.0f / 362880.0f);
+        sp = fma2(sp, y2, pk(1.0f / 5040.0f, 1.0f / 5040.0f));
+        sp = fma2(sp, y2, pk(1.0f / 120.0f, 1.0f / 120.0f));
+        sp = fma2(sp, y2, pk(1.0f / 6.0f, 1.0f / 6.0f));
+        sp = fma2(sp, y2, pk(1.0f, 1.0f));
+        float s0, s1;
+        upk(mul2(y, sp), s0, s1);                                     // sinh(delta ln2 / 2)
+        const float o0 = far0 ? 1.0f - e0 : -2.0f * e0 * s0;
+        const float o1 = far1 ? 1.0f - e1 : -2.0f * e1 * s1;
+        upk(mul2(Q[p], pk(o0, o1)), r[2 * p], r[2 * p + 1]);
+    }
+}
+// Lane sums of one unit, in a fixed order (the locate pass repeats it).
+__device__ __forceinline__ float sum8f(const float *v)
+{
+    return ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+}
+
+// The coefficients of the distribution sequence b samples at its end j.
+__device__ __forceinline__ ResK vr_coef(const RowsParams &P, int b, int j)
+{
+    const VrStat *st = P.stat + (size_t)b * (2 * P.K + 1);
+    const VrStat t = ld_vrstat(st + j);
+    ResK k;
+    k.Mt = t.m;
+    k.c = P.c;
+    k.dLhi = k.dLlo = 0.0f;
+    if (j < P.K) {
+        // dL = (Md - Mt) + log2 Sd - log2 St as a float pair
+        const VrStat d = ld_vrstat(st + P.K + 1 + j);
+        int et, ed;
+        float ft, fd;
+        log2_split(DF{t.s_hi, t.s_lo}, et, ft);
+        log2_split(DF{d.s_hi, d.s_lo}, ed, fd);
+        DF dl = two_sum(d.m, -t.m);
+        dl = df_add(dl, DF{(float)(ed - et), 0.0f});
+        dl = df_add(dl, DF{fd - ft, 0.0f});
+        k.dLhi = dl.hi;
+        k.dLlo = dl.lo;
+    }
+    return k;
+}
+
+template <class E>
+__global__ void __launch_bounds__(VRT) vr_residual(const __grid_constant__ RowsParams P)
+{
+    constexpr int NW = VRT / 32;
+    constexpr int UPS = VSEG / 8;   // units per segment (one per lane)
+    __shared__ int sm_j, sm_code;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.x / P.nch, ch = blockIdx.x % P.nch;
+    const int K = P.K, V = P.V;
+    if (tid == 0) {
+        int j = 0;
+        sm_code = vr_end(P, b, j);
+        sm_j = j;
+    }
+    __syncthreads();
+    if (sm_code)
+        return;
+    const int j = sm_j;
+    const bool qonly = j == K;
+    const ResK k = vr_coef(P, b, j);
+    const uint8_t *trow = static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + j) * (size_t)V * E::ES;
+    const uint8_t *drow =
+        qonly ? trow : static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + j) * (size_t)V * E::ES;
+    // this chunk's segments [s_lo, s_hi); at step t warp w takes segment
+    // s_lo + t * NW + w, lane l its unit l (tokens seg * VSEG + 8 l ..)
+    const int spc = (P.nseg + P.nch - 1) / P.nch;
+    const int s_lo = ch * spc, s_hi = min(P.nseg, s_lo + spc);
+    const int nsteps = (s_hi - s_lo + NW - 1) / NW;
+    VrSeg *out = P.segm + (size_t)b * P.nseg;
+    auto unit_x0 = [&](int t) { return ((s_lo + t * NW + warp) * UPS + lane) * 8; };
+    // four steps in flight; each buffer is refilled right after its use
+    Unit<E> ut[4], ud[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        if (q < nsteps) {
+            ut[q] = fetch_unit<E>(trow, unit_x0(q), V, P.vec);
+            if (!qonly)
+                ud[q] = fetch_unit<E>(drow, unit_x0(q), V, P.vec);
+        }
+    for (int t0 = 0; t0 < nsteps; t0 += 4) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int t = t0 + q;
+            if (t < nsteps) {
+                f2 XT[4], XD[4];
+                unit_pairs<E>(ut[q], XT);
+                if (!qonly)
+                    unit_pairs<E>(ud[q], XD);
+                if (t + 4 < nsteps) {
+                    ut[q] = fetch_unit<E>(trow, unit_x0(t + 4), V, P.vec);
+                    if (!qonly)
+                        ud[q] = fetch_unit<E>(drow, unit_x0(t + 4), V, P.vec);
+                }
+                float r[8], qv[8];
+                vr_res8(XT, XD, k, qonly, r, qv);
+                const float rs = warp_sumf(sum8f(r)), qs = warp_sumf(sum8f(qv));
+                const int seg = s_lo + t * NW + warp;
+                if (lane == 0 && seg < s_hi)
+                    out[seg] = VrSeg{rs, qs};
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- 3. sampling and outputs
+// Accepted drafts 0..j-1, then x at j, -1 after.
+__device__ __forceinline__ void vr_emit(const RowsParams &P, int b, int j, int x)
+{
+    int32_t *o = P.out_tokens + (size_t)b * (P.K + 1);
+    for (int i = 0; i < j; ++i)
+        o[i] = __ldg(P.tokens + (size_t)b * P.K + i);
+    o[j] = x;
+    for (int i = j + 1; i <= P.K; ++i)
+        o[i] = -1;
+    P.out_len[b] = j;
+}
+
+template <class E>
+__global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsParams P)
+{
+    constexpr int NW = VST / 32;
+    __shared__ int sm_j, sm_code, sm_seg, sm_last[NW];
+    __shared__ DF sm_r[NW], sm_q[NW], sm_before;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int b = blockIdx.x;
+    const int K = P.K, V = P.V;
+    if (tid == 0) {
+        int j = 0;
+        sm_code = vr_end(P, b, j);
+        sm_j = j;
+    }
+    __syncthreads();
+    const int j = sm_j, code = sm_code;
+    const VrStat *st = P.stat + (size_t)b * (2 * K + 1);
+
+    // per-position outputs (every row was computed when they are asked for)
+    if (P.aux_q || P.aux_p || P.aux_lse) {
+        for (int i = tid; i < 2 * K + 1; i += VST) {
+            const VrStat s = ld_vrstat(st + i);
+            const bool ok = !(s.flags & (VR_BAD | VR_SKIP)) && s.m > -F_INF && s.s_hi > 0.0f;
+            int e;
+            float f;
+            log2_split(DF{s.s_hi, s.s_lo}, e, f);
+            const float l2 = s.m + ((float)e + f);   // log2 sum 2^(x c)
+            if (P.aux_lse)
+                P.aux_lse[(size_t)b * (2 * K + 1) + i] = ok ? l2 * 0.6931471805599453f : __int_as_float(0x7fc00000);
+            const int pos = i <= K ? i : i - K - 1;
+            if (pos < K && (i <= K ? P.aux_q : P.aux_p)) {
+                const int dt = __ldg(P.tokens + (size_t)b * K + pos);
+                const bool tok_ok = dt >= 0 && dt < V;
+                const float v = ok && tok_ok ? ex2a(fmaf(s.zd, P.c, -l2)) : __int_as_float(0x7fc00000);
+                (i <= K ? P.aux_q : P.aux_p)[(size_t)b * K + pos] = v;
+            }
+        }
+    }
+    if (code) {
+        if (tid == 0) {
+            int32_t *o = P.out_tokens + (size_t)b * (K + 1);
+            for (int i = 0; i <= K; ++i)
+                o[i] = -1;
+            P.out_len[b] = -code;
+            if (P.aux_R)
+                P.aux_R[b] = __int_as_float(0x7fc00000);
+            if (P.aux_status)
+                atomicCAS(P.aux_status, 0, code);
+        }
+    } else if (P.greedy) {
+        if (tid == 0) {
+            vr_emit(P, b, j, __float_as_int(ld_vrstat(st + j).s_hi));
+            if (P.aux_R)
+                P.aux_R[b] = __int_as_float(0x7fc00000);
+        }
+    } else {
+        // totals of the residual and target masses of row pair j
+        const int nseg = P.nseg;
+        const VrSeg *sg = P.segm + (size_t)b * nseg;
+        const int per = (nseg + VST - 1) / VST;
+        const int s0 = min(nseg, tid * per), s1 = min(nseg, s0 + per);
+        DF ownr{0.0f, 0.0f}, ownq{0.0f, 0.0f};
+        for (int s = s0; s < s1; ++s) {
+            const float2 g = __ldcg(reinterpret_cast<const float2 *>(sg + s));
+            ownr = df_add(ownr, DF{g.x, 0.0f});
+            ownq = df_add(ownq, DF{g.y, 0.0f});
+        }
+        const DF ir = warp_incl_scan_df(ownr, lane), iq = warp_incl_scan_df(ownq, lane);
+        if (lane == 31) {
+            sm_r[warp] = ir;
+            sm_q[warp] = iq;
+        }
+        if (tid == 0)
+            sm_seg = -1;
+        __syncthreads();
+        DF tr{0.0f, 0.0f}, tq{0.0f, 0.0f}, pr{0.0f, 0.0f}, pq{0.0f, 0.0f};
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            if (w == warp) {
+                pr = tr;
+                pq = tq;
+            }
+            tr = df_add(tr, sm_r[w]);
+            tq = df_add(tq, sm_q[w]);
+        }
+        // R <= 0 (q == p up to rounding): sample q_j itself
+        const bool useq = j < K && !(tr.hi > 0.0f);
+        const DF F = useq ? tq : tr;
+        const DF winc = useq ? iq : ir;
+        DF wexc{__shfl_up_sync(0xffffffffu, winc.hi, 1), __shfl_up_sync(0xffffffffu, winc.lo, 1)};
+        if (lane == 0)
+            wexc = DF{0.0f, 0.0f};
+        const DF incl = df_add(useq ? pq : pr, winc), excl = df_add(useq ? pq : pr, wexc);
+        const uint4 wd = philox10((uint32_t)j, (uint32_t)b, 0u, 0u, P.key0, P.key1);
+        const float v = ((float)(wd.y >> 8) + 0.5f) * (1.0f / 16777216.0f);
+        const float th = v * F.hi;
+        const DF thr = df_add(DF{th, fmaf(v, F.hi, -th)}, DF{v * F.lo, 0.0f});
+        if (df_gt(incl, thr) && !df_gt(excl, thr)) {
+            DF G = excl;
+            for (int s = s0; s < s1; ++s) {
+                const float2 g = __ldcg(reinterpret_cast<const float2 *>(sg + s));
+                const float m = useq ? g.y : g.x;
+                const DF nG = df_add(G, DF{m, 0.0f});
+                if (df_gt(nG, thr) && m > 0.0f) {
+                    sm_seg = s;
+                    sm_before = G;
+                    break;
+                }
+                G = nG;
+            }
+        }
+        __syncthreads();
+        if (sm_seg < 0) {
+            // rounding left no crossing: the last segment with mass
+            int last = -1;
+            for (int s = tid; s < nseg; s += VST) {
+                const float2 g = __ldcg(reinterpret_cast<const float2 *>(sg + s));
+                if ((useq ? g.y : g.x) > 0.0f)
+                    last = s;
+            }
+            last = warp_maxi(last);
+            if (lane == 0)
+                sm_last[warp] = last;
+            __syncthreads();
+        }
+        if (warp == 0) {
+            // the token inside the segment: lane l holds tokens [s*256 + 8l, +8)
+            int seg = sm_seg, fb = 0;
+            if (seg < 0) {
+                seg = -1;
+                for (int w = 0; w < NW; ++w)
+                    seg = max(seg, sm_last[w]);
+                fb = 1;
+            }
+            int x = -1;
+            if (seg >= 0) {
+                const ResK k = vr_coef(P, b, j);
+                const bool qonly = j == K || useq;
+                const uint8_t *trow =
+                    static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + j) * (size_t)V * E::ES;
+                const uint8_t *drow = static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + j) * (size_t)V * E::ES;
+                const int x0 = seg * VSEG + lane * 8;
+                const Unit<E> ut = fetch_unit<E>(trow, x0, V, P.vec);
+                Unit<E> ud{};
+                if (!qonly)
+                    ud = fetch_unit<E>(drow, x0, V, P.vec);
+                f2 XT[4], XD[4];
+                unit_pairs<E>(ut, XT);
+                if (!qonly)
+                    unit_pairs<E>(ud, XD);
+                float r[8], q[8];
+                vr_res8(XT, XD, k, qonly, r, q);
+                const float ls = sum8f(r);
+                if (!fb) {
+                    const DF rel = df_add(thr, DF{-sm_before.hi, -sm_before.lo});
+                    const float t = rel.hi + rel.lo;
+                    float in = ls;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float u = __shfl_up_sync(0xffffffffu, in, o);
+                        if (lane >= o)
+                            in += u;
+                    }
+                    float ex = __shfl_up_sync(0xffffffffu, in, 1);
+                    if (lane == 0)
+                        ex = 0.0f;
+                    const unsigned bal = __ballot_sync(0xffffffffu, in > t && ls > 0.0f);
+                    if (bal) {
+                        const int L = __ffs(bal) - 1;
+                        if (lane == L) {
+                            float cum = ex;
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                cum += r[e];
+                                if (x < 0 && cum > t && r[e] > 0.0f)
+                                    x = x0 + e;
+                            }
+                        }
+                        x = __shfl_sync(0xffffffffu, x, L);
+                    }
+                }
+                if (x < 0) {
+                    // the last token of the segment with a positive weight
+                    int lk = -1;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        if (r[e] > 0.0f)
+                            lk = x0 + e;
+                    x = warp_maxi(lk);
+                }
+            }
+            if (lane == 0) {
+                vr_emit(P, b, j, x);
+                if (P.aux_R) {
+                    // R of the distribution drawn from (for q_j itself: the residual's, about 0)
+                    const VrStat t = ld_vrstat(st + j);
+                    const DF Rr = useq ? tr : F;
+                    P.aux_R[b] = (Rr.hi + Rr.lo) / (t.s_hi + t.s_lo);
+                }
+            }
+        }
+    }
+    // the sequence's control words, for the next call
+    __syncthreads();
+    for (int i = tid; i <= K; i += VST)
+        P.pair[(size_t)b * (K + 1) + i] = 0u;
+    for (int i = tid; i < 2 * K + 1; i += VST)
+        P.rowcnt[(size_t)b * (2 * K + 1) + i] = 0u;
+    if (tid == 0)
+        P.rej[b] = 0u;
+}
+
+// A vr_stats launch over `rows` rows: each row is cut into parts so that the
+// launch brings about as many threads as the GPU holds (the bytes in flight
+// grow with them), with parts of at least 4096 tokens.
+constexpr int VST_T = 256;   // threads of a vr_stats CTA
+template <class E>
+cudaError_t launch_stats(RowsParams P, int pos, int npos, int sms, cudaStream_t stream)
+{
+    const int rpp = P.greedy ? P.B : 2 * P.B;
+    // position K has the target row alone (B rows): launch it as rpp rows, the
+    // draft half returning at once, to keep one row mapping
+    const int rows = rpp * npos;
+    const long long want = (long long)sms * 2048;
+    int S = (int)std::min<long long>(VR_SMAX, (want + (long long)rows * VST_T - 1) / ((long long)rows * VST_T));
+    S = std::max(1, std::min(S, P.V / 4096));
+    P.pos = pos;
+    P.npos = npos;
+    P.span = ((P.V + S - 1) / S + 7) / 8 * 8;
+    P.parts = (P.V + P.span - 1) / P.span;
+    vr_stats<E, VST_T><<<rows * P.parts, VST_T, 0, stream>>>(P);
+    return cudaGetLastError();
+}
+
+template <class E>
+cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream)
+{
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess)
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+        return e;
+    // positions 0 and 1 first, then the rest: the second launch sees every
+    // decision of the first (most of what skipping saves), at the cost of one
+    // launch boundary
+    const int first = std::min(2, P.K + 1);
+    e = launch_stats<E>(P, 0, first, sms, stream);
+    if (e == cudaSuccess && first <= P.K)
+        e = launch_stats<E>(P, first, P.K + 1 - first, sms, stream);
+    if (e != cudaSuccess)
+        return e;
+    if (!P.greedy)
+        vr_residual<E><<<P.B * P.nch, VRT, 0, stream>>>(P);
+    vr_sample<E><<<P.B, VST, 0, stream>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int rows_chunks() { return VR_NCH; }
+int rows_segment_tokens() { return VSEG; }
+int rows_launches(int K, bool greedy) { return (K + 1 > 2 ? 2 : 1) + (greedy ? 1 : 2); }
+
+cudaError_t launch_rows(const RowsParams &P, int tdt, cudaStream_t stream)
+{
+    if (P.aux_status) {
+        cudaError_t e = cudaMemsetAsync(P.aux_status, 0, sizeof(int32_t), stream);
+        if (e != cudaSuccess)
+            return e;
+    }
+    return tdt == 0 ? launch_rows_t<F32>(P, stream) : launch_rows_t<BF16>(P, stream);
+}
+
+}  // namespace sv

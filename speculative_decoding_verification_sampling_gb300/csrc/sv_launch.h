@@ -37,6 +37,13 @@ struct SweepEntry {
 };
 SweepEntry entry_sweep(int tdt);
 
+// Row-parallel verification (k_rows.cu): statistics per row, residual masses
+// per sequence chunk, then sampling per sequence (greedy: no residual kernel).
+int rows_chunks();
+int rows_segment_tokens();
+int rows_launches(int K, bool greedy);   // kernels one call launches
+cudaError_t launch_rows(const RowsParams &P, int tdt, cudaStream_t stream);
+
 // The fused draft-token sampler (k_draft.cu): one CTA per row of draft logits.
 int draft_max_v();
 cudaError_t launch_draft_sample(const void *draft, int tdt, int B, int K, int V, float T, uint64_t seed,

@@ -198,9 +198,52 @@ struct SweepParams {
 };
 
 // Workspace layout for (B, K, V, S); every array starts 256-byte aligned.
+// Row-parallel verification (k_rows.cu): the statistics of one logit row.
+//   m        reference floor(max * c) in log2 units (greedy: the maximum)
+//   s_hi/lo  sum of 2^(x c - m) as a float pair (greedy: s_hi holds the
+//            argmax index's bits)
+//   flags    VR_BAD (NaN or +inf seen), VR_SKIP (not computed: not needed)
+//   zd       the logit at the drafted token of the row's position
+struct alignas(16) VrStat {
+    float m, s_hi, s_lo;
+    int flags;
+    float zd;
+    int pad0, pad1, pad2;
+};
+enum { VR_BAD = 1, VR_SKIP = 2, VR_HASD = 4 };
+constexpr int VR_SMAX = 16;   // most parts a row is split into
+struct VrSeg {
+    float r, q;   // residual and target masses of one 256-token segment, relative to 2^Mt
+};
+
+struct RowsParams {
+    const void *target;        // [B][K+1][V]
+    const void *draft;         // [B][K][V] logits; nullptr for greedy
+    const int32_t *tokens;     // [B][K]
+    int32_t *out_tokens;       // [B][K+1]
+    int32_t *out_len;          // [B]
+    float *aux_q, *aux_p, *aux_R, *aux_lse;
+    int32_t *aux_status;
+    uint32_t *ctl;             // control words (status)
+    VrStat *stat;              // [B][2K+1]: target rows 0..K, then draft rows 0..K-1
+    uint32_t *pair;            // [B][K+1] rows of a position done
+    uint32_t *rowcnt;          // [B][2K+1] parts of a row done
+    VrStat *vpart;             // [B][2K+1][VR_SMAX] statistics of the parts of a row
+    uint32_t *rej;             // [B] bit i: position i decided against (or in error)
+    int32_t *errc;             // [B][K+1] status of a decision in error (valid where rej is set)
+    VrSeg *segm;             // [B][nseg]
+    int B, K, V, nseg, nch;
+    int pos, npos;             // vr_stats: the positions [pos, pos + npos) this launch streams
+    int parts, span;           // vr_stats: parts per row, tokens per part (a multiple of 8)
+    int greedy, skip, vec;
+    float c;
+    uint32_t key0, key1;
+};
+
 struct WsLayout {
     size_t ctl, state, res_rec, pair_cnt, res_cnt, fin, errres, sw_ctl, sw_seq, sw_cnt, sw_res_ready, sw_res_done,
-        errcode, terminal, gtok, dec, part, seg, sl_lb, sw_part, sw_stat, sw_res, sw_resm, total;
+        vr_pair, vr_rej, vr_rowcnt, errcode, terminal, gtok, dec, part, seg, sl_lb, sw_part, sw_stat, sw_res, sw_resm,
+        vr_stat, vr_errc, vr_part, vr_segm, total;
     size_t reset_end;   // [ctl, reset_end) holds what a call must find zeroed
     int npt_max, nseg;
 };
@@ -229,6 +272,9 @@ inline WsLayout ws_layout(int B, int K, int V, int S)
     w.sw_cnt = o;   o = align256(o + Bz * P * 4);
     w.sw_res_ready = o; o = align256(o + 2 * Bz * 4);
     w.sw_res_done = o;  o = align256(o + 2 * Bz * 4);
+    w.vr_pair = o;  o = align256(o + Bz * P * 4);
+    w.vr_rej = o;   o = align256(o + Bz * 4);
+    w.vr_rowcnt = o; o = align256(o + Bz * (2 * P - 1) * 4);
     w.reset_end = o;
     w.errcode = o;  o = align256(o + Bz * P * 4);
     w.terminal = o; o = align256(o + Bz * 4);
@@ -241,6 +287,10 @@ inline WsLayout ws_layout(int B, int K, int V, int S)
     w.sw_stat = o;  o = align256(o + Bz * P * sizeof(SwStat));
     w.sw_res = o;   o = align256(o + 2 * Bz * sizeof(SwRes));
     w.sw_resm = o;  o = align256(o + 2 * Bz * (size_t)SW_MAXST * SW_WARPS * sizeof(DF2));
+    w.vr_stat = o;  o = align256(o + Bz * (2 * P - 1) * sizeof(VrStat));
+    w.vr_errc = o;  o = align256(o + Bz * P * 4);
+    w.vr_part = o;  o = align256(o + Bz * (2 * P - 1) * (size_t)VR_SMAX * sizeof(VrStat));
+    w.vr_segm = o;  o = align256(o + Bz * (size_t)w.nseg * sizeof(VrSeg));
     w.total = o;
     return w;
 }

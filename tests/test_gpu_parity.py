@@ -27,13 +27,14 @@ def _device():
     sv.load()
 
 
-@pytest.fixture(scope="module", autouse=True, params=["cluster", "sweep", "general"])
+@pytest.fixture(scope="module", autouse=True, params=["auto", "cluster", "sweep", "rows", "general"])
 def kernel(request):
-    """Every case runs under each kernel: the default dispatch (the cluster
-    kernel wherever it applies), the sweep kernel, and the chunk-scheduled
-    kernel."""
+    """Every case runs under the default dispatch and under each kernel forced
+    in turn: the cluster kernel, the sweep kernel, the row-parallel kernels
+    and the chunk-scheduled kernel (each falls back to the next for shapes it
+    does not serve)."""
     old = os.environ.get("SPECVERIFY_KERNEL")
-    os.environ["SPECVERIFY_KERNEL"] = "auto" if request.param == "cluster" else request.param
+    os.environ["SPECVERIFY_KERNEL"] = request.param
     yield request.param
     if old is None:
         os.environ.pop("SPECVERIFY_KERNEL", None)
