@@ -471,6 +471,220 @@ def run_gb300(args) -> int:
     return 0
 
 
+# --------------------------------------------------------------------------
+# further workloads of the library (`--workload`), one JSON line each, same keys
+# --------------------------------------------------------------------------
+def _draft_sample_workload(B: int, K: int, dev):
+    """The fused draft-token sampler over the throughput workload's draft rows:
+    [B][K][V] bf16 logits, T = 1."""
+    import torch
+    import oracle.draft_sample as ods
+    import speculative_decoding_verification_sampling_gb300 as sv
+    from speculative_decoding_verification_sampling_gb300 import synth
+    cfg = synth.throughput(B=B, K=K, seed=DATA_SEED)
+    host = cfg["draft"]
+    nbytes = host.numel() * host.element_size()
+
+    def make_sets(n):
+        d0 = host.to(dev)
+        return [(d0 if i == 0 else d0.clone(),
+                 torch.empty(B, K, dtype=torch.int32, device=dev),
+                 torch.empty(B, K, dtype=torch.float32, device=dev)) for i in range(n)]
+
+    def call(st, stream):
+        d, ot, op = st
+        sv.spec_draft_sample(d, TEMPERATURE, VERIFY_SEED, out_tokens=ot, out_prob=op, stream=stream)
+
+    def result(st):
+        return st[1].cpu()
+
+    def oracle_run(i):
+        """The oracle on sequence i of the batch: returns the tokens it drew."""
+        b = i % B
+        ods.draft_sample(host[b:b + 1], TEMPERATURE, VERIFY_SEED, seq_ids=[b])
+        return K
+
+    return dict(metric="sampled draft tokens/s at V=128256 bf16 (fused draft-token sampler); achieved HBM GB/s",
+                unit="tokens/s", units=B * K, alg_bytes=nbytes + B * K * 8, h2d=nbytes, d2h=B * K * 8,
+                make_sets=make_sets, call=call, result=result, host_inputs=[host],
+                upload=lambda st: [st[0]], oracle_run=oracle_run,
+                kernel="draft_sample_kernel (bf16, T=1)",
+                workload=f"draft-token sampling B={B} K={K} V={V} bf16 T=1; draft logits = "
+                         f"N(0, 2^2) target + N(0, 0.5^2) (the verification workload's draft rows)",
+                l2=f"inputs larger than L2: device copies of the {nbytes / 1e6:.0f} MB draft rows, rotated")
+
+
+def _kv_commit_workload(B: int, K: int, dev):
+    """KV-cache commit after the verification step: a cache shaped like a
+    Llama-3-8B one (32 layers, 8 KV heads of 128 dims, keys and values, bf16:
+    4096 bytes per entry and layer), capacity 512 entries per sequence, the K
+    staged entries of the verification pass, and the accept lengths that the
+    verification of the throughput batch returns.  Every step commits at its
+    own offsets, so the written entries move through the cache."""
+    import numpy as np
+    import torch
+    import oracle.kv_commit as okv
+    import speculative_decoding_verification_sampling_gb300 as sv
+    from speculative_decoding_verification_sampling_gb300 import synth
+    NL, L, EW = 32, 512, 2048          # EW bf16 elements per entry and layer
+    W = EW * 2
+    cfg = synth.throughput(B=B, K=K, seed=DATA_SEED)
+    _, acc = sv.spec_verify(cfg["target"].to(dev), cfg["draft"].to(dev), cfg["draft_tokens"].to(dev),
+                            TEMPERATURE, VERIFY_SEED)
+    del cfg
+    torch.cuda.synchronize(dev)
+    acc_h = acc.cpu()
+    committed = int(acc_h.clamp(min=0).sum())
+    gen = torch.Generator(device="cpu").manual_seed(DATA_SEED)
+    host = torch.randn((NL, B, K, EW), generator=gen).to(torch.bfloat16)
+    cache = torch.zeros((NL, B, L, EW), dtype=torch.bfloat16, device=dev)
+    # one length array per call (the commit advances it in place): step i
+    # commits sequence b at entry (7 b + 11 i) mod (L - K)
+    n_calls = 4096
+    steps = torch.arange(n_calls)[:, None]
+    lens = ((torch.arange(B)[None, :] * 7 + 11 * steps) % (L - K)).to(torch.int32).to(dev)
+    state = {"step": 0}
+
+    def make_sets(n):
+        s0 = host.to(dev)
+        return [s0 if i == 0 else s0.clone() for i in range(n)]
+
+    def call(st, stream):
+        i = state["step"] % n_calls
+        state["step"] += 1
+        sv.spec_kv_commit(cache, st, acc, lens[i], stream=stream)
+
+    def result(st):
+        return torch.zeros(1)
+
+    cache_h = np.zeros((NL, 1, L, W), dtype=np.uint8)
+    staged_h = host.view(torch.uint8).numpy()
+
+    def oracle_run(i):
+        b = i % B
+        okv.kv_commit(cache_h, staged_h[:, b:b + 1], [0], [int(acc_h[b])])
+        return max(0, int(acc_h[b])) * NL
+
+    return dict(metric="committed KV entries/s (entries x layers; 4096-byte bf16 entries, 32 layers, "
+                       "accept lengths of the B=256 K=4 verification); achieved HBM GB/s",
+                unit="entries/s", units=committed * NL, alg_bytes=2 * committed * NL * W + 2 * B * 4,
+                h2d=host.numel() * 2, d2h=4 * B, make_sets=make_sets, call=call, result=result,
+                host_inputs=[host], upload=lambda st: [st], oracle_run=oracle_run,
+                kernel="kv_copy + kv_len",
+                workload=f"KV-cache commit B={B} K={K}: cache [32][{B}][{L}][4096 B] bf16, staged "
+                         f"[32][{B}][{K}][4096 B], accept lengths of the verification step "
+                         f"(mean {float(acc_h.double().mean()):.2f})",
+                l2="staged entries rotated over device copies; each step commits at new offsets")
+
+
+EXTRA_WORKLOADS = {"draft_sample": _draft_sample_workload, "kv_commit": _kv_commit_workload}
+
+
+def run_extra(args) -> int:
+    """A further workload of the library, timed like the verification step."""
+    import torch
+    import torch.distributed as dist
+    import speculative_decoding_verification_sampling_gb300 as sv
+
+    rank, world, local_rank = dist_env()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU path)")
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    sv.load()
+    w = EXTRA_WORKLOADS[args.workload](args.batch, args.k, dev)
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        sets = w["make_sets"](args.rotate)
+    stream.synchronize()
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    uuid = f"GPU-{uuid}" if uuid is not None and not str(uuid).startswith("GPU-") else (str(uuid) if uuid else None)
+    with ClockSampler(uuid) as clocks:
+        with torch.cuda.stream(stream):
+            for i in range(max(args.warmup, len(sets))):
+                w["call"](sets[i % len(sets)], stream)
+        stream.synchronize()
+        ref = w["result"](sets[0])
+        for st in sets[1:]:
+            if not torch.equal(w["result"](st), ref):
+                raise RuntimeError("copies of one input set gave different results")
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        launches0 = sv.spec_launch_count()
+        barrier(dev)
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for i in range(args.steps):
+                w["call"](sets[i % len(sets)], stream)
+            stop.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(dev)
+        launches = sv.spec_launch_count() - launches0
+        clock_samples = clocks.samples()
+    elapsed_ms = max_over_ranks(start.elapsed_time(stop), dev)
+    mean_s = elapsed_ms / args.steps / 1e3
+    value = world * w["units"] * args.steps / (elapsed_ms / 1e3)
+
+    # end to end: inputs copied in from pinned host memory, results read back, every step
+    pinned = [h.pin_memory() for h in w["host_inputs"]]
+    st0 = sets[0]
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for dst, src in zip(w["upload"](st0), pinned):
+                dst.copy_(src, non_blocking=True)
+            w["call"](st0, stream)
+            out = w["result"](st0)
+        stream.synchronize()
+        return out
+
+    for _ in range(3):
+        e2e_step()
+    e2e_steps = max(3, min(args.steps, 100))
+    barrier(dev)
+    h0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        last = e2e_step()
+    e2e_s = max_over_ranks(time.perf_counter() - h0, dev)
+    if not torch.equal(last, ref):
+        raise RuntimeError("end-to-end results differ from the device-resident run")
+    if rank == 0:
+        peak, src = hbm_peak()
+        achieved = w["alg_bytes"] / mean_s / 1e9
+        line = {
+            "metric": w["metric"], "value": value, "unit": w["unit"], "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w["workload"], "B": args.batch, "K": args.k, "V": V,
+                       "parallelism": f"replicas x{world}", "l2": w["l2"]},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_source": src, "kernel": w["kernel"],
+                         "algorithmic_bytes_per_launch": w["alg_bytes"], "mean_kernel_us": mean_s * 1e6},
+            "e2e": {"value": world * w["units"] * e2e_steps / e2e_s, "unit": w["unit"],
+                    "h2d_bytes_per_step": w["h2d"], "d2h_bytes_per_step": w["d2h"], "steps": e2e_steps},
+            "gpu_launches": int(launches),
+            "clocks": summarize_clocks(clock_samples),
+        }
+        if world == 1 and args.cpu_seconds > 0:
+            t0, n, i = time.perf_counter(), 0, 0
+            while time.perf_counter() - t0 < args.cpu_seconds:
+                n += w["oracle_run"](i)
+                i += 1
+            el = time.perf_counter() - t0
+            line["cpu_baseline"] = {"value": n / el, "unit": w["unit"], "cores": 1, "kind": "oracle",
+                                    "sample": f"{n} units of the same workload through the float64 oracle "
+                                              f"(one thread), {el:.1f} s"}
+        else:
+            line["cpu_baseline"] = None
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -481,6 +695,8 @@ def main(argv=None) -> int:
     ap.add_argument("--k", type=int, default=4, help="drafted tokens per sequence")
     ap.add_argument("--rotate", type=int, default=4, help="device copies of the input set")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="length of the oracle sample")
+    ap.add_argument("--workload", choices=("verify",) + tuple(EXTRA_WORKLOADS), default="verify",
+                    help="the verification step (default), or a further workload of the library")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -492,6 +708,8 @@ def main(argv=None) -> int:
             ap.error("--gpus N > 1 runs under torchrun with N processes")
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload != "verify":
+        return run_extra(args)
     return run_gb300(args)
 
 

@@ -182,6 +182,34 @@ spec_status_t spec_draft_sample(const void *draft_logits, spec_dtype_t ddt, int 
                                 uint64_t seed, int32_t *out_tokens, float *out_prob, int32_t *device_status,
                                 void *stream);
 
+/* KV-cache commit (and rollback) after verification (nextadmin.net lesson
+ * "Speculative Decoding", § KV cache management: the verification pass
+ * appends the K drafts' entries; when drafts are rejected the cache returns
+ * to the accepted prefix, production systems staging the K entries and
+ * committing the accepted ones; § Exercises item 4 fixes the outcome).
+ *   cache       [NL][B][L][entry_bytes]  the KV cache: NL layers, capacity L
+ *                                        entries per sequence, entry_bytes
+ *                                        bytes per entry and layer (keys and
+ *                                        values of all heads, any dtype)
+ *   staged      [NL][B][K][entry_bytes]  the K new entries of the verification
+ *                                        pass, or NULL when they were written in
+ *                                        place at [seq_len[b], seq_len[b] + K)
+ *   accept_len  [B]   spec_verify's out_accept_len (accepted drafts, or < 0
+ *                     for a sequence in error)
+ *   seq_len     [B]   in/out: cache lengths
+ * For a = accept_len[b] >= 0: entries 0..a-1 of staged[l][b] are copied to
+ * cache[l][b][seq_len[b]..] for every layer and seq_len[b] += a; the drafts'
+ * other entries are dropped (rolled back).  a < 0 changes nothing.  a > K, or
+ * seq_len[b] + a > L, changes nothing and sets *device_status to
+ * SPEC_ERR_INVALID_ARG (device_status is set to 0 first; it may be NULL).
+ * Device pointers; staged must not overlap cache.  16-byte aligned buffers
+ * with entry_bytes a multiple of 16 take the vector path.  Asynchronous on
+ * `stream`; two launches (one in place).  The token emitted at the rejection
+ * (or the bonus token) has no entry yet: it is the next round's input.       */
+spec_status_t spec_kv_commit(void *cache, const void *staged, int NL, int B, int K, int L, size_t entry_bytes,
+                             const int32_t *accept_len, int32_t *seq_len, int32_t *device_status,
+                             void *stream);
+
 /* Philox4x32-10 words as the verification kernels draw them, for checking:
  * out[(b * P + pos) * 4 + w] = word w of Philox(counter (pos, b, tag, 0),
  * key (seed low, seed high)) for b < B, pos < P.  `out` is a device pointer of
@@ -192,7 +220,8 @@ spec_status_t spec_philox_words(uint64_t seed, uint32_t tag, int B, int P, uint3
 /* Number of kernels this library has launched in this process, over every
  * entry point and device: a successful spec_verify* call launches one kernel,
  * or three or four when the row-parallel kernels serve it (large stochastic
- * batches); spec_draft_sample and spec_philox_words launch one each.  For
+ * batches); spec_draft_sample and spec_philox_words launch one each,
+ * spec_kv_commit two (one in place).  For
  * accounting; thread-safe.                                                   */
 uint64_t spec_launch_count(void);
 

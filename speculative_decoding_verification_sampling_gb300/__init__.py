@@ -22,7 +22,7 @@ from .build import LIB as _LIB_PATH
 
 __all__ = [
     "SpecVerifyError", "Aux", "spec_verify", "spec_verify_greedy", "spec_verify_shortlist",
-    "spec_workspace_bytes", "spec_philox_words", "spec_draft_sample", "spec_status_string", "spec_launch_count", "spec_verify_static", "library_path", "load",
+    "spec_workspace_bytes", "spec_philox_words", "spec_draft_sample", "spec_kv_commit", "spec_status_string", "spec_launch_count", "spec_verify_static", "library_path", "load",
 ]
 
 SPEC_F32, SPEC_BF16 = 0, 1
@@ -75,6 +75,8 @@ def load():
             lib.spec_status_string.restype = ctypes.c_char_p
             lib.spec_verify_static.argtypes = [P, I, P, P, I, I, I, F, U64, P, P, P, P]
             lib.spec_verify_static.restype = I
+            lib.spec_kv_commit.argtypes = [P, P, I, I, I, I, Z, P, P, P, P]
+            lib.spec_kv_commit.restype = I
             lib.spec_draft_sample.argtypes = [P, I, I, I, I, F, U64, P, P, P, P]
             lib.spec_draft_sample.restype = I
             lib.spec_launch_count.argtypes = []
@@ -324,3 +326,32 @@ def spec_draft_sample(draft: torch.Tensor, T: float, seed: int, *, out_tokens=No
     if rc:
         raise SpecVerifyError(rc, "spec_draft_sample")
     return out_tokens, out_prob
+
+
+def spec_kv_commit(cache: torch.Tensor, staged: torch.Tensor | None, accept_len: torch.Tensor,
+                   seq_len: torch.Tensor, *, K: int | None = None, device_status=None, stream=None):
+    """Commit the accepted drafts' KV entries: cache [NL][B][L][...] (any
+    dtype), staged [NL][B][K][...] of the same dtype and entry shape (None:
+    entries written in place, then K must be given), accept_len [B] int32 (as
+    spec_verify returns it), seq_len [B] int32 updated in place."""
+    if not isinstance(cache, torch.Tensor) or not cache.is_cuda or cache.dim() < 4 or not cache.is_contiguous():
+        raise TypeError("cache must be a contiguous CUDA tensor [NL][B][L][...]")
+    NL, B, L = cache.shape[:3]
+    entry = cache[0, 0, 0]
+    W = entry.numel() * cache.element_size()
+    if staged is not None:
+        K = staged.shape[2]
+        _check(staged, (NL, B, K) + tuple(cache.shape[3:]), (cache.dtype,), "staged")
+    elif K is None:
+        raise ValueError("K is needed when the entries were written in place")
+    _check(accept_len, (B,), (torch.int32,), "accept_len")
+    _check(seq_len, (B,), (torch.int32,), "seq_len")
+    if device_status is not None:
+        _check(device_status, (1,), (torch.int32,), "device_status")
+    st = _stream(cache.device, stream)
+    rc = load().spec_kv_commit(cache.data_ptr(), staged.data_ptr() if staged is not None else None, NL, B, int(K), L,
+                               W, accept_len.data_ptr(), seq_len.data_ptr(),
+                               device_status.data_ptr() if device_status is not None else None, st)
+    if rc:
+        raise SpecVerifyError(rc, "spec_kv_commit")
+    return seq_len

@@ -670,6 +670,26 @@ spec_status_t spec_draft_sample(const void *draft_logits, spec_dtype_t ddt, int 
     return SPEC_OK;
 }
 
+spec_status_t spec_kv_commit(void *cache, const void *staged, int NL, int B, int K, int L, size_t entry_bytes,
+                             const int32_t *accept_len, int32_t *seq_len, int32_t *device_status, void *stream)
+{
+    if (!cache || !accept_len || !seq_len || NL < 1 || B < 1 || K < 1 || L < 1 || entry_bytes < 1)
+        return SPEC_ERR_INVALID_ARG;
+    const unsigned long long W = entry_bytes;
+    // the cache (NL B L W bytes) within 2^48 bytes, so every offset fits 64 bits
+    if ((double)NL * (double)B * (double)L * (double)W > 281474976710656.0)
+        return SPEC_ERR_INVALID_ARG;
+    const unsigned long long per = 256ULL * 64ULL;
+    if ((unsigned long long)NL * B * ((K * W + per - 1) / per) > 0x7fffffffULL)
+        return SPEC_ERR_UNSUPPORTED;
+    int launches = 0;
+    if (sv::launch_kv_commit(cache, staged, NL, B, K, L, (long long)W, accept_len, seq_len, device_status,
+                             static_cast<cudaStream_t>(stream), &launches) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    g_launches.fetch_add((uint64_t)launches, std::memory_order_relaxed);
+    return SPEC_OK;
+}
+
 uint64_t spec_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char *spec_status_string(spec_status_t status)

@@ -44,6 +44,10 @@ int rows_segment_tokens();
 int rows_launches(int K, bool greedy);   // kernels one call launches
 cudaError_t launch_rows(const RowsParams &P, int tdt, cudaStream_t stream);
 
+// KV-cache commit after verification (k_kv.cu): copy, then the length update.
+cudaError_t launch_kv_commit(void *cache, const void *staged, int NL, int B, int K, int L, long long W,
+                             const int32_t *acc, int32_t *len, int32_t *status, cudaStream_t stream, int *launches);
+
 // The fused draft-token sampler (k_draft.cu): one CTA per row of draft logits.
 int draft_max_v();
 cudaError_t launch_draft_sample(const void *draft, int tdt, int B, int K, int V, float T, uint64_t seed,

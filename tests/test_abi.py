@@ -116,3 +116,19 @@ def test_draft_sample_rejects_bad_arguments():
     assert lib.spec_draft_sample(p, 7, 1, 1, 8, 1.0, 0, p, None, None, None) == 1
     assert lib.spec_draft_sample(p, 1, 1, 1, 1 << 22, 1.0, 0, p, None, None, None) == 5
     assert sv.spec_launch_count() == n0
+
+
+def test_kv_commit_rejects_bad_arguments():
+    lib = sv.load()
+    p = ctypes.c_void_p(256)
+    n0 = sv.spec_launch_count()
+    assert lib.spec_kv_commit(None, p, 1, 1, 1, 1, 16, p, p, None, None) == 1
+    assert lib.spec_kv_commit(p, p, 0, 1, 1, 1, 16, p, p, None, None) == 1
+    assert lib.spec_kv_commit(p, p, 1, 0, 1, 1, 16, p, p, None, None) == 1
+    assert lib.spec_kv_commit(p, p, 1, 1, 0, 1, 16, p, p, None, None) == 1
+    assert lib.spec_kv_commit(p, p, 1, 1, 1, 0, 16, p, p, None, None) == 1
+    assert lib.spec_kv_commit(p, p, 1, 1, 1, 1, 0, p, p, None, None) == 1
+    assert lib.spec_kv_commit(p, p, 1, 1, 1, 1, 16, None, p, None, None) == 1
+    assert lib.spec_kv_commit(p, p, 1, 1, 1, 1, 16, p, None, None, None) == 1
+    assert lib.spec_kv_commit(p, p, 1 << 20, 1 << 20, 1, 1 << 20, 1 << 20, p, p, None, None) == 1
+    assert sv.spec_launch_count() == n0
