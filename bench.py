@@ -577,7 +577,50 @@ def _kv_commit_workload(B: int, K: int, dev):
                 l2="staged entries rotated over device copies; each step commits at new offsets")
 
 
-EXTRA_WORKLOADS = {"draft_sample": _draft_sample_workload, "kv_commit": _kv_commit_workload}
+def _tree_greedy_workload(B: int, K: int, dev):
+    """Greedy verification of an EAGLE-style draft tree: 32 sequences, top-k
+    branches (4, 2, 2, 1, 1) per depth (61 nodes), V=128256 bf16 target rows
+    ~ N(0, 3^2); every node row is read (500 MB per call).  K is not used."""
+    import torch
+    import oracle.tree as otr
+    import speculative_decoding_verification_sampling_gb300 as sv
+    from speculative_decoding_verification_sampling_gb300 import synth
+    Bt = 32
+    cfg = synth.tree_greedy(B=Bt, V=V, seed=DATA_SEED)
+    host_t, host_k, host_p = cfg["target"], cfg["tree_tokens"], cfg["parent"]
+    N = cfg["N"]
+    nbytes = host_t.numel() * host_t.element_size()
+    ws = torch.empty(sv.load().spec_tree_workspace_bytes(Bt, N, V), dtype=torch.uint8, device=dev)
+
+    def make_sets(n):
+        t0, k0, p0 = host_t.to(dev), host_k.to(dev), host_p.to(dev)
+        return [((t0, k0, p0) if i == 0 else (t0.clone(), k0.clone(), p0.clone())) + ([None],) for i in range(n)]
+
+    def call(st, stream):
+        t, k, p, out = st
+        out[0] = sv.spec_verify_tree_greedy(t, k, p, workspace=ws, stream=stream)
+
+    def result(st):
+        return st[3][0][2].cpu()
+
+    def oracle_run(i):
+        b = i % Bt
+        otr.tree_verify_greedy(host_t[b:b + 1], host_k[b:b + 1].numpy(), host_p[b:b + 1].numpy())
+        return N - 1
+
+    return dict(metric="verified draft-tree nodes/s (greedy tree verification, 61-node trees, V=128256 bf16); "
+                       "achieved HBM GB/s", unit="nodes/s", units=Bt * (N - 1),
+                alg_bytes=nbytes + Bt * N * 8 + Bt * N * 8 + Bt * 4, h2d=nbytes + Bt * N * 8, d2h=Bt * (2 * N + 1) * 4,
+                make_sets=make_sets, call=call, result=result, host_inputs=[host_t, host_k, host_p],
+                upload=lambda st: [st[0], st[1], st[2]], oracle_run=oracle_run,
+                kernel="draft_sample_kernel (greedy, node rows) + tree_walk", B=Bt, K=N - 1,
+                workload=f"greedy tree verification B={Bt} N={N} (branching 4,2,2,1,1) V={V} bf16; target "
+                         f"N(0, 3^2); first children hold the argmax with probability 0.7",
+                l2=f"inputs larger than L2: device copies of the {nbytes / 1e6:.0f} MB node rows, rotated")
+
+
+EXTRA_WORKLOADS = {"draft_sample": _draft_sample_workload, "kv_commit": _kv_commit_workload,
+                   "tree_greedy": _tree_greedy_workload}
 
 
 def run_extra(args) -> int:
@@ -658,7 +701,7 @@ def run_extra(args) -> int:
             "metric": w["metric"], "value": value, "unit": w["unit"], "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w["workload"], "B": args.batch, "K": args.k, "V": V,
+            "config": {"workload": w["workload"], "B": w.get("B", args.batch), "K": w.get("K", args.k), "V": V,
                        "parallelism": f"replicas x{world}", "l2": w["l2"]},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": None, "peak_source": src, "kernel": w["kernel"],

@@ -210,6 +210,46 @@ spec_status_t spec_kv_commit(void *cache, const void *staged, int NL, int B, int
                              const int32_t *accept_len, int32_t *seq_len, int32_t *device_status,
                              void *stream);
 
+/* Greedy tree verification (aiengineeringfromscratch.com Phase 10 lesson 25,
+ * § Tree attention verification: one target pass over a draft tree under a
+ * mask where each token sees only its ancestors; the output is the longest
+ * accepted prefix along any path; § Greedy case: a draft is accepted when it
+ * is the target's argmax).  The stochastic multi-branch rule is not on the
+ * pages and is not offered.
+ *   target_logits  [B][N][V]  dtype `tdt`; row n: the target's prediction after
+ *                             node n's token
+ *   tree_tokens    [B][N]     int32: node n's drafted token (node 0, the root,
+ *                             is the last accepted token and is not read)
+ *   parent         [B][N]     int32: parent[0] == -1, parent[n] in [0, n)
+ *   out_tokens     [B][N]     int32: the accepted path's drafts, then the
+ *                             argmax of its last node's row; -1 after
+ *   out_nodes      [B][N]     int32: the path's node indices (root excluded); -1 after
+ *   out_accept_len [B]        int32: accepted drafts (the path's depth), or
+ *                             -code on a data error in an examined place:
+ *                             1 malformed parent array, 2 NaN / +inf / all -inf
+ *                             row of an accepted node, 3 token outside [0, V)
+ *                             at a child of an accepted node
+ * A child is accepted iff its parent is accepted and its token equals the
+ * first index of the maximum of the parent's row.  The path ends at the
+ * deepest accepted node, the lowest node index among equally deep ones.
+ *   workspace      device scratch of spec_tree_workspace_bytes(B, N, V) bytes
+ *                  (no zero-fill needed), 16-byte aligned
+ *   device_status  [1] set to 0, or the code of one failing sequence; may be NULL
+ * Limits: B, N, V >= 1, N <= 2048, B * N <= 2^30, V <= 2093056.  Two launches,
+ * asynchronous on `stream`.                                                   */
+size_t spec_tree_workspace_bytes(int B, int N, int V);
+spec_status_t spec_verify_tree_greedy(const void *target_logits, spec_dtype_t tdt, const int32_t *tree_tokens,
+                                      const int32_t *parent, int B, int N, int V, int32_t *out_tokens,
+                                      int32_t *out_nodes, int32_t *out_accept_len, void *workspace,
+                                      size_t workspace_bytes, int32_t *device_status, void *stream);
+
+/* Tree attention mask (the same section): mask[b][i][j] = 1 iff node j is
+ * node i or one of its ancestors, else 0; uint8 [B][N][N], device pointers.
+ * A malformed parent array sets *device_status to 1 (it is set to 0 first;
+ * may be NULL) and leaves that row's walk cut short.  One launch.            */
+spec_status_t spec_tree_mask(const int32_t *parent, int B, int N, uint8_t *mask, int32_t *device_status,
+                             void *stream);
+
 /* Philox4x32-10 words as the verification kernels draw them, for checking:
  * out[(b * P + pos) * 4 + w] = word w of Philox(counter (pos, b, tag, 0),
  * key (seed low, seed high)) for b < B, pos < P.  `out` is a device pointer of

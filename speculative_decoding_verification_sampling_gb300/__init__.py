@@ -22,7 +22,7 @@ from .build import LIB as _LIB_PATH
 
 __all__ = [
     "SpecVerifyError", "Aux", "spec_verify", "spec_verify_greedy", "spec_verify_shortlist",
-    "spec_workspace_bytes", "spec_philox_words", "spec_draft_sample", "spec_kv_commit", "spec_status_string", "spec_launch_count", "spec_verify_static", "library_path", "load",
+    "spec_workspace_bytes", "spec_philox_words", "spec_draft_sample", "spec_kv_commit", "spec_verify_tree_greedy", "spec_tree_mask", "spec_status_string", "spec_launch_count", "spec_verify_static", "library_path", "load",
 ]
 
 SPEC_F32, SPEC_BF16 = 0, 1
@@ -75,6 +75,12 @@ def load():
             lib.spec_status_string.restype = ctypes.c_char_p
             lib.spec_verify_static.argtypes = [P, I, P, P, I, I, I, F, U64, P, P, P, P]
             lib.spec_verify_static.restype = I
+            lib.spec_tree_workspace_bytes.argtypes = [I, I, I]
+            lib.spec_tree_workspace_bytes.restype = Z
+            lib.spec_verify_tree_greedy.argtypes = [P, I, P, P, I, I, I, P, P, P, P, Z, P, P]
+            lib.spec_verify_tree_greedy.restype = I
+            lib.spec_tree_mask.argtypes = [P, I, I, P, P, P]
+            lib.spec_tree_mask.restype = I
             lib.spec_kv_commit.argtypes = [P, P, I, I, I, I, Z, P, P, P, P]
             lib.spec_kv_commit.restype = I
             lib.spec_draft_sample.argtypes = [P, I, I, I, I, F, U64, P, P, P, P]
@@ -355,3 +361,51 @@ def spec_kv_commit(cache: torch.Tensor, staged: torch.Tensor | None, accept_len:
     if rc:
         raise SpecVerifyError(rc, "spec_kv_commit")
     return seq_len
+
+
+def spec_verify_tree_greedy(target: torch.Tensor, tree_tokens: torch.Tensor, parent: torch.Tensor, *,
+                            workspace=None, device_status=None, stream=None):
+    """Greedy verification of a draft tree: target [B][N][V] logits (row n: the
+    prediction after node n), tree_tokens and parent [B][N] int32 (parent[0]
+    == -1, parent[n] < n).  Returns (out_tokens [B][N], out_nodes [B][N],
+    out_accept_len [B])."""
+    B, N, V = target.shape
+    _check(target, (B, N, V), (torch.float32, torch.bfloat16), "target")
+    _check(tree_tokens, (B, N), (torch.int32,), "tree_tokens")
+    _check(parent, (B, N), (torch.int32,), "parent")
+    dev = target.device
+    nbytes = int(load().spec_tree_workspace_bytes(B, N, V))
+    if nbytes == 0:
+        raise SpecVerifyError(1, "spec_verify_tree_greedy")
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    out_t = torch.empty((B, N), dtype=torch.int32, device=dev)
+    out_n = torch.empty((B, N), dtype=torch.int32, device=dev)
+    out_l = torch.empty((B,), dtype=torch.int32, device=dev)
+    if device_status is not None:
+        _check(device_status, (1,), (torch.int32,), "device_status")
+    st = _stream(dev, stream)
+    rc = load().spec_verify_tree_greedy(target.data_ptr(), _dt(target), tree_tokens.data_ptr(), parent.data_ptr(),
+                                        B, N, V, out_t.data_ptr(), out_n.data_ptr(), out_l.data_ptr(),
+                                        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                        device_status.data_ptr() if device_status is not None else None, st)
+    if rc:
+        raise SpecVerifyError(rc, "spec_verify_tree_greedy")
+    return out_t, out_n, out_l
+
+
+def spec_tree_mask(parent: torch.Tensor, *, out=None, device_status=None, stream=None) -> torch.Tensor:
+    """Tree attention mask: uint8 [B][N][N], 1 where node j is node i or an ancestor of it."""
+    B, N = parent.shape
+    _check(parent, (B, N), (torch.int32,), "parent")
+    if out is None:
+        out = torch.empty((B, N, N), dtype=torch.uint8, device=parent.device)
+    _check(out, (B, N, N), (torch.uint8,), "out")
+    if device_status is not None:
+        _check(device_status, (1,), (torch.int32,), "device_status")
+    rc = load().spec_tree_mask(parent.data_ptr(), B, N, out.data_ptr(),
+                               device_status.data_ptr() if device_status is not None else None,
+                               _stream(parent.device, stream))
+    if rc:
+        raise SpecVerifyError(rc, "spec_tree_mask")
+    return out

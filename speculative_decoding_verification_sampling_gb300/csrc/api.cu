@@ -690,6 +690,55 @@ spec_status_t spec_kv_commit(void *cache, const void *staged, int NL, int B, int
     return SPEC_OK;
 }
 
+size_t spec_tree_workspace_bytes(int B, int N, int V)
+{
+    if (B < 1 || N < 1 || V < 1 || N > sv::tree_max_nodes() || (long long)B * N > (1LL << 30))
+        return 0;
+    return ((size_t)B * N * 4 + 255) & ~(size_t)255;
+}
+
+spec_status_t spec_verify_tree_greedy(const void *target_logits, spec_dtype_t tdt, const int32_t *tree_tokens,
+                                      const int32_t *parent, int B, int N, int V, int32_t *out_tokens,
+                                      int32_t *out_nodes, int32_t *out_accept_len, void *workspace,
+                                      size_t workspace_bytes, int32_t *device_status, void *stream)
+{
+    if (!target_logits || !tree_tokens || !parent || !out_tokens || !out_nodes || !out_accept_len || !workspace)
+        return SPEC_ERR_INVALID_ARG;
+    if (tdt != SPEC_F32 && tdt != SPEC_BF16)
+        return SPEC_ERR_INVALID_ARG;
+    const size_t need = spec_tree_workspace_bytes(B, N, V);
+    if (need == 0 || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 15u))
+        return SPEC_ERR_INVALID_ARG;
+    if (V > sv::draft_max_v())
+        return SPEC_ERR_UNSUPPORTED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (device_status && cudaMemsetAsync(device_status, 0, sizeof(int32_t), st) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    int32_t *g = static_cast<int32_t *>(workspace);
+    // the argmax of every node row: the draft sampler's greedy kernel over B * N rows
+    if (sv::launch_draft_sample(target_logits, tdt == SPEC_BF16 ? 1 : 0, B, N, V, 0.0f, 0, g, nullptr, nullptr,
+                                st) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    if (sv::launch_tree_walk(tree_tokens, parent, g, B, N, V, out_tokens, out_nodes, out_accept_len, device_status,
+                             st) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return SPEC_OK;
+}
+
+spec_status_t spec_tree_mask(const int32_t *parent, int B, int N, uint8_t *mask, int32_t *device_status,
+                             void *stream)
+{
+    if (!parent || !mask || B < 1 || N < 1 || (long long)B * N > 0x7fffffffLL ||
+        (double)B * (double)N * (double)N > 281474976710656.0)
+        return SPEC_ERR_INVALID_ARG;
+    if (sv::launch_tree_mask(parent, B, N, mask, device_status, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    g_launches.fetch_add(1, std::memory_order_relaxed);
+    return SPEC_OK;
+}
+
 uint64_t spec_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char *spec_status_string(spec_status_t status)

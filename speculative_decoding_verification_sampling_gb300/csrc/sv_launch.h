@@ -48,6 +48,13 @@ cudaError_t launch_rows(const RowsParams &P, int tdt, cudaStream_t stream);
 cudaError_t launch_kv_commit(void *cache, const void *staged, int NL, int B, int K, int L, long long W,
                              const int32_t *acc, int32_t *len, int32_t *status, cudaStream_t stream, int *launches);
 
+// Greedy tree verification and the tree mask (k_tree.cu).
+int tree_max_nodes();
+cudaError_t launch_tree_walk(const int32_t *tokens, const int32_t *parent, const int32_t *g, int B, int N, int V,
+                             int32_t *out_tokens, int32_t *out_nodes, int32_t *out_len, int32_t *status,
+                             cudaStream_t stream);
+cudaError_t launch_tree_mask(const int32_t *parent, int B, int N, uint8_t *mask, int32_t *status, cudaStream_t stream);
+
 // The fused draft-token sampler (k_draft.cu): one CTA per row of draft logits.
 int draft_max_v();
 cudaError_t launch_draft_sample(const void *draft, int tdt, int B, int K, int V, float T, uint64_t seed,

@@ -178,3 +178,46 @@ def controlled_alpha_pair(V: int, alpha: float, gen: torch.Generator):
     q[:half] = wq / wq.sum()
     r[half:] = wr / wr.sum()
     return q, alpha * q + (1.0 - alpha) * r
+
+
+def tree_topology(branching=(4, 2, 2, 1, 1)) -> list[int]:
+    """Parents of a draft tree in breadth-first order: the root, then
+    `branching[0]` children, each with `branching[1]` children, and so on
+    (EAGLE-style top-k branches per depth).  Node 0 is the root (parent -1)."""
+    parent, level = [-1], [0]
+    for k in branching:
+        nxt = []
+        for p in level:
+            for _ in range(k):
+                parent.append(p)
+                nxt.append(len(parent) - 1)
+        level = nxt
+    return parent
+
+
+def tree_greedy(B: int = 32, V: int = 128256, branching=(4, 2, 2, 1, 1), dtype=torch.bfloat16, seed: int = 6,
+                match_prob: float = 0.7, target_std: float = 3.0, device="cpu") -> dict:
+    """Greedy tree verification inputs: target ~ N(0, target_std^2) [B][N][V];
+    the first child of every node holds the target's argmax after its parent
+    with probability `match_prob` (else a uniform token), the other children
+    uniform tokens; node 0's token is unused (0)."""
+    g = _gen(seed, device)
+    parent = tree_topology(branching)
+    N = len(parent)
+    target = _normal((B, N, V), target_std, g, device).to(dtype)
+    best = torch.argmax(target.float(), dim=-1)
+    rand_tok = torch.randint(0, V, (B, N), generator=g, device=device)
+    keep = torch.rand((B, N), generator=g, device=device) < match_prob
+    tokens = torch.zeros((B, N), dtype=torch.int64, device=device)
+    first = {}
+    for n in range(1, N):
+        p = parent[n]
+        is_first = p not in first
+        first.setdefault(p, n)
+        if is_first:
+            tokens[:, n] = torch.where(keep[:, n], best[:, p], rand_tok[:, n])
+        else:
+            tokens[:, n] = rand_tok[:, n]
+    par = torch.tensor(parent, dtype=torch.int32, device=device).expand(B, N).contiguous()
+    return dict(name=f"tree greedy B={B} N={N} V={V} branching={tuple(branching)}", target=target,
+                tree_tokens=tokens.to(torch.int32), parent=par, B=B, N=N, V=V)
