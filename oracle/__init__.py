@@ -70,6 +70,12 @@ def _load():
                                           ctypes.c_double, ctypes.c_uint64,
                                           P, P, P, P, P, P, P, P, P, P, ctypes.c_int]
             lib.oracle_verify.restype = ctypes.c_int
+            lib.oracle_verify_sl.argtypes = [P, ctypes.c_int, P, ctypes.c_int, ctypes.c_int,
+                                             P, ctypes.c_int, ctypes.c_longlong, ctypes.c_longlong, P, P,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_double, ctypes.c_uint64,
+                                             P, P, P, P, P, P, P, P, P, P, ctypes.c_int]
+            lib.oracle_verify_sl.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -164,11 +170,14 @@ def _i32(t):
 
 
 def verify(target, draft, draft_tokens, T: float, seed: int, *, draft_is_probs: bool = False,
-           shortlist=None, full: bool = False, threads: int | None = None, seq_ids=None) -> dict:
+           shortlist=None, shortlist_len=None, full: bool = False, threads: int | None = None,
+           seq_ids=None) -> dict:
     """One verification round for every sequence of the batch.
 
     target: [B][K+1][V] float32 or bfloat16 logits; draft: [B][K][V] logits or
-    float32 probabilities ([B][K][S] with ``shortlist`` of shape [B][S]);
+    float32 probabilities ([B][K][S] with a ``shortlist``: [B][S] one list per
+    sequence, [B][K][S] one list per position, or [S] one list shared by all;
+    ``shortlist_len`` [K] the entries of each position's list, default S);
     draft_tokens: [B][K].  T == 0 selects greedy verification.  ``full`` also
     returns q_i(d_i), p_i(d_i) and the log-sum-exp of every row.
     Returns numpy arrays: tokens [B][K+1], accept_len [B], terminal [B],
@@ -189,9 +198,17 @@ def verify(target, draft, draft_tokens, T: float, seed: int, *, draft_is_probs: 
     tok = _i32(draft_tokens).reshape(B, K)
     sl = None
     S = 0
+    sl_seq = sl_pos = 0
+    sl_len = None
     if shortlist is not None:
         sl = _i32(shortlist)
-        S = sl.shape[1]
+        S = sl.shape[-1]
+        if sl.ndim == 3:
+            sl_seq, sl_pos = K * S, S
+        elif sl.ndim == 2:
+            sl_seq, sl_pos = S, 0
+        if shortlist_len is not None:
+            sl_len = np.ascontiguousarray(np.asarray(shortlist_len, dtype=np.int32))
     out_tokens = np.zeros((B, K + 1), dtype=np.int32)
     out_len = np.zeros(B, dtype=np.int32)
     terminal = np.zeros(B, dtype=np.int32)
@@ -206,8 +223,9 @@ def verify(target, draft, draft_tokens, T: float, seed: int, *, draft_is_probs: 
     if threads is None:
         threads = os.cpu_count() or 1
     sid = None if seq_ids is None else np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int32))
-    st = _load().oracle_verify(_ptr(tgt), tdt, _ptr(drf), ddt, int(bool(draft_is_probs)),
-                               _ptr(sl), S, _ptr(tok), B, K, V, float(T), int(seed) & (2**64 - 1),
+    st = _load().oracle_verify_sl(_ptr(tgt), tdt, _ptr(drf), ddt, int(bool(draft_is_probs)),
+                               _ptr(sl), S, sl_seq, sl_pos, _ptr(sl_len), _ptr(tok), B, K, V, float(T),
+                               int(seed) & (2**64 - 1),
                                _ptr(out_tokens), _ptr(out_len), _ptr(q_draft), _ptr(p_draft),
                                _ptr(res_mass), _ptr(row_lse), _ptr(acc_margin), _ptr(smp_margin),
                                _ptr(terminal), _ptr(sid), int(threads))

@@ -46,9 +46,10 @@
  *     ([SD-EN] § Greedy case); when all K match, the bonus is argmax q_{K+1}
  *     ([SD-FA] § Core algorithm step 6);
  *   - data errors (NaN / +inf logits, an all -inf row, a token outside
- *     [0, V), a shortlist that is not ascending and unique inside [0, V),
+ *     [0, V), a shortlist that is not ascending and unique inside [0, V)
+ *     (or whose length is outside [1, S]),
  *     negative or non-finite draft probabilities) are checked at the positions
- *     the left-to-right rule examines, in the order: shortlist (position 0),
+ *     the left-to-right rule examines, in the order: the position's shortlist,
  *     token, target row, draft row.  Logit rows are checked whole (their
  *     softmax needs every entry); given draft probabilities are checked where
  *     the rule reads them: p_i(d_i) at each examined position, and the whole
@@ -227,7 +228,9 @@ struct job {
     const void *target; int tdt;        /* [B][K+1][V]                          */
     const void *draft; int ddt;         /* [B][K][V], or [B][K][S] on a shortlist */
     int draft_is_probs;                 /* draft holds probabilities (float32)  */
-    const int32_t *shortlist; int S;    /* [B][S] ascending, or NULL            */
+    const int32_t *shortlist; int S;    /* index lists (ascending), or NULL; S = draft row stride */
+    long long sl_seq, sl_pos;           /* list of (b, i) at shortlist + b sl_seq + i sl_pos */
+    const int32_t *sl_len;              /* [K] entries of the list at position i, or NULL (S) */
     const int32_t *tokens;              /* [B][K]                               */
     int B, K, V;
     double T;
@@ -252,6 +255,18 @@ static int seq_of(const struct job *J, int b)
     return J->seq_ids ? J->seq_ids[b] : b;
 }
 
+/* The shortlist of position i of sequence b and its length ([DYNA] § Method 3:
+ * the budget, hence the list, may depend on the position; a list shared by
+ * every position or every sequence is the same layout with stride 0).        */
+static const int32_t *sl_row(const struct job *J, int b, int i)
+{
+    return J->shortlist + (long long)b * J->sl_seq + (long long)i * J->sl_pos;
+}
+static int sl_n(const struct job *J, int i)
+{
+    return J->sl_len ? J->sl_len[i] : J->S;
+}
+
 /* q_i: softmax of target row (b, i). */
 static int target_dist(const struct job *J, int b, int i, struct scratch *w, double *lse)
 {
@@ -268,8 +283,8 @@ static int target_dist(const struct job *J, int b, int i, struct scratch *w, dou
  * softmax over the S shortlisted logits, 0 for every other token.             */
 static int draft_dist(const struct job *J, int b, int i, struct scratch *w, double *lse)
 {
-    int n = J->shortlist ? J->S : J->V;
-    size_t off = ((size_t)b * J->K + i) * (size_t)n;
+    int n = J->shortlist ? sl_n(J, i) : J->V;
+    size_t off = ((size_t)b * J->K + i) * (size_t)(J->shortlist ? J->S : J->V);
     if (lse)
         *lse = NAN;
     if (J->draft_is_probs) {
@@ -285,10 +300,10 @@ static int draft_dist(const struct job *J, int b, int i, struct scratch *w, doub
     if (!J->shortlist) {
         memcpy(w->p, w->r, sizeof(double) * (size_t)n);
     } else {
-        const int32_t *idx = J->shortlist + (size_t)b * J->S;
+        const int32_t *idx = sl_row(J, b, i);
         for (int x = 0; x < J->V; ++x)
             w->p[x] = 0.0;
-        for (int s = 0; s < J->S; ++s)
+        for (int s = 0; s < n; ++s)
             w->p[idx[s]] = w->r[s];
     }
     return OR_OK;
@@ -303,18 +318,21 @@ static int prob_ok(double v)
 /* Every entry of draft probability row (b, i) usable. */
 static int prob_row_ok(const struct job *J, int b, int i)
 {
-    int n = J->shortlist ? J->S : J->V;
-    size_t off = ((size_t)b * J->K + i) * (size_t)n;
+    int n = J->shortlist ? sl_n(J, i) : J->V;
+    size_t off = ((size_t)b * J->K + i) * (size_t)(J->shortlist ? J->S : J->V);
     for (int x = 0; x < n; ++x)
         if (!prob_ok(elem(J->draft, OR_F32, off + x)))
             return 0;
     return 1;
 }
 
-static int shortlist_ok(const struct job *J, int b)
+static int shortlist_ok(const struct job *J, int b, int i)
 {
-    const int32_t *idx = J->shortlist + (size_t)b * J->S;
-    for (int s = 0; s < J->S; ++s) {
+    const int32_t *idx = sl_row(J, b, i);
+    const int n = sl_n(J, i);
+    if (n < 1 || n > J->S)
+        return 0;
+    for (int s = 0; s < n; ++s) {
         if (idx[s] < 0 || idx[s] >= J->V)
             return 0;
         if (s > 0 && idx[s] <= idx[s - 1])
@@ -353,11 +371,12 @@ static void verify_stochastic(const struct job *J, int b, struct scratch *w)
     if (J->residual_mass)
         J->residual_mass[b] = NAN;
 
-    if (J->shortlist && !shortlist_ok(J, b)) {
-        emit_error(J, b, OR_ERR_SHORTLIST);
-        return;
-    }
     for (int i = 0; i < K; ++i) {
+        /* the shortlist this position's draft uses, before its token */
+        if (J->shortlist && !shortlist_ok(J, b, i)) {
+            emit_error(J, b, OR_ERR_SHORTLIST);
+            return;
+        }
         int d = J->tokens[(size_t)b * K + i];
         if (d < 0 || d >= V) {
             emit_error(J, b, OR_ERR_TOKEN_RANGE);
@@ -428,8 +447,8 @@ static void verify_stochastic(const struct job *J, int b, struct scratch *w)
 static void all_positions(const struct job *J, int b, struct scratch *w)
 {
     const int K = J->K;
-    int sl_bad = J->shortlist && !shortlist_ok(J, b);
     for (int i = 0; i <= K; ++i) {
+        int sl_bad = i < K && J->shortlist && !shortlist_ok(J, b, i);
         double lse_t = NAN, lse_d = NAN;
         int bad_t = target_dist(J, b, i, w, &lse_t);
         if (J->row_lse)
@@ -519,15 +538,17 @@ static void *run_worker(void *arg)
 
 /* Batched entry point: one verification round for each of B independent
  * sequences, split over `nthreads` host threads (one sequence at a time per
- * thread).  Host pointers; the same argument order as the library.
- * Returns 0, or 1 for arguments that are out of range.                        */
-int oracle_verify(const void *target, int tdt, const void *draft, int ddt, int draft_is_probs,
-                  const int32_t *shortlist, int S, const int32_t *tokens,
-                  int B, int K, int V, double T, uint64_t seed,
-                  int32_t *out_tokens, int32_t *out_accept_len,
-                  double *q_draft, double *p_draft, double *residual_mass, double *row_lse,
-                  double *accept_margin, double *sample_margin, int32_t *terminal,
-                  const int32_t *seq_ids, int nthreads)
+ * thread).  Host pointers.  The shortlist of position i of sequence b is the
+ * sl_len[i] (all S when sl_len is NULL) entries at shortlist + b sl_seq +
+ * i sl_pos; draft rows are [B][K][S].  Returns 0, or 1 for arguments that are
+ * out of range.                                                               */
+int oracle_verify_sl(const void *target, int tdt, const void *draft, int ddt, int draft_is_probs,
+                     const int32_t *shortlist, int S, long long sl_seq, long long sl_pos, const int32_t *sl_len,
+                     const int32_t *tokens, int B, int K, int V, double T, uint64_t seed,
+                     int32_t *out_tokens, int32_t *out_accept_len,
+                     double *q_draft, double *p_draft, double *residual_mass, double *row_lse,
+                     double *accept_margin, double *sample_margin, int32_t *terminal,
+                     const int32_t *seq_ids, int nthreads)
 {
     if (B < 1 || K < 1 || V < 1 || !(T >= 0.0) || !target || !tokens || !out_tokens || !out_accept_len)
         return 1;
@@ -539,8 +560,8 @@ int oracle_verify(const void *target, int tdt, const void *draft, int ddt, int d
         nthreads = 1;
     if (nthreads > B)
         nthreads = B;
-    struct job J = { target, tdt, draft, ddt, draft_is_probs, shortlist, S, tokens, B, K, V, T, seed,
-                     out_tokens, out_accept_len, q_draft, p_draft, residual_mass, row_lse,
+    struct job J = { target, tdt, draft, ddt, draft_is_probs, shortlist, S, sl_seq, sl_pos, sl_len, tokens, B, K, V,
+                     T, seed, out_tokens, out_accept_len, q_draft, p_draft, residual_mass, row_lse,
                      accept_margin, sample_margin, terminal, seq_ids, nthreads };
     pthread_t *th = malloc(sizeof(pthread_t) * (size_t)nthreads);
     struct worker *wk = malloc(sizeof(struct worker) * (size_t)nthreads);
@@ -554,4 +575,18 @@ int oracle_verify(const void *target, int tdt, const void *draft, int ddt, int d
     free(th);
     free(wk);
     return 0;
+}
+
+/* The per-sequence shortlist form: list b at shortlist + b S, all S entries. */
+int oracle_verify(const void *target, int tdt, const void *draft, int ddt, int draft_is_probs,
+                  const int32_t *shortlist, int S, const int32_t *tokens,
+                  int B, int K, int V, double T, uint64_t seed,
+                  int32_t *out_tokens, int32_t *out_accept_len,
+                  double *q_draft, double *p_draft, double *residual_mass, double *row_lse,
+                  double *accept_margin, double *sample_margin, int32_t *terminal,
+                  const int32_t *seq_ids, int nthreads)
+{
+    return oracle_verify_sl(target, tdt, draft, ddt, draft_is_probs, shortlist, S, (long long)S, 0, NULL, tokens, B,
+                            K, V, T, seed, out_tokens, out_accept_len, q_draft, p_draft, residual_mass, row_lse,
+                            accept_margin, sample_margin, terminal, seq_ids, nthreads);
 }
