@@ -133,6 +133,33 @@ spec_status_t spec_verify_shortlist(const void *target_logits, spec_dtype_t tdt,
                                     void *workspace, size_t workspace_bytes,
                                     const spec_aux_t *aux, void *stream);
 
+/* Verification with a shortlisted draft whose list may depend on the position
+ * (DynaSpec summary, § Method 3: the position-aware budget k_c(t) sets how
+ * many clusters, hence tokens, the drafter uses at draft step t; a static
+ * list shared by every sequence and position, as in FR-Spec, is the same
+ * layout with both strides 0).
+ *   draft_sl       [B][K][S]  draft logits of dtype `tdt` (ddt == tdt); row (b, i)
+ *                             holds shortlist_len[i] logits, for the tokens of
+ *                             list (b, i)
+ *   shortlist_idx  list (b, i) starts at shortlist_idx + b * sl_seq_stride +
+ *                  i * sl_pos_stride (entries): strictly ascending, each in [0, V)
+ *                  (per position: strides K*S and S; per sequence: S and 0;
+ *                  shared: 0 and 0)
+ *   shortlist_len  HOST array of K entry counts, each in [1, S], or NULL (all S)
+ * p_i is 0 off list (b, i); the target and the residual stay over the full
+ * vocabulary; a drafted token off its list has p_i(d_i) = 0 and is accepted.
+ * A list that is not strictly ascending inside [0, V) is an error
+ * (SPEC_ERR_SHORTLIST) at the position that uses it, found only if the rule
+ * reaches that position.  Draft probabilities are not accepted here.
+ * The workspace is spec_workspace_bytes(B, K, V, S).  T == 0 runs the greedy
+ * rule (the draft is not read).  Served by the row-parallel kernels.         */
+spec_status_t spec_verify_shortlist_pos(const void *target_logits, spec_dtype_t tdt, const void *draft_sl,
+                                        spec_dtype_t ddt, const int32_t *shortlist_idx, long long sl_seq_stride,
+                                        long long sl_pos_stride, const int32_t *shortlist_len, int S,
+                                        const int32_t *draft_tokens, int B, int K, int V, float T, uint64_t seed,
+                                        int32_t *out_tokens, int32_t *out_accept_len, void *workspace,
+                                        size_t workspace_bytes, const spec_aux_t *aux, void *stream);
+
 /* Verification with no caller workspace (the pages have no counterpart: this
  * is an interface for callers that cannot allocate device memory, or cannot
  * hold a workspace per call, e.g. code with a fixed memory plan).  Arguments

@@ -22,7 +22,8 @@ from .build import LIB as _LIB_PATH
 
 __all__ = [
     "SpecVerifyError", "Aux", "spec_verify", "spec_verify_greedy", "spec_verify_shortlist",
-    "spec_workspace_bytes", "spec_philox_words", "spec_draft_sample", "spec_kv_commit", "spec_verify_tree_greedy", "spec_tree_mask", "spec_status_string", "spec_launch_count", "spec_verify_static", "library_path", "load",
+    "spec_workspace_bytes", "spec_philox_words", "spec_draft_sample", "spec_kv_commit", "spec_verify_tree_greedy", "spec_tree_mask",
+    "spec_verify_shortlist_pos", "dynaspec_budget", "spec_status_string", "spec_launch_count", "spec_verify_static", "library_path", "load",
 ]
 
 SPEC_F32, SPEC_BF16 = 0, 1
@@ -75,6 +76,10 @@ def load():
             lib.spec_status_string.restype = ctypes.c_char_p
             lib.spec_verify_static.argtypes = [P, I, P, P, I, I, I, F, U64, P, P, P, P]
             lib.spec_verify_static.restype = I
+            L64 = ctypes.c_longlong
+            lib.spec_verify_shortlist_pos.argtypes = [P, I, P, I, P, L64, L64, P, I, P, I, I, I, F, U64, P, P, P,
+                                                      Z, P, P]
+            lib.spec_verify_shortlist_pos.restype = I
             lib.spec_tree_workspace_bytes.argtypes = [I, I, I]
             lib.spec_tree_workspace_bytes.restype = Z
             lib.spec_verify_tree_greedy.argtypes = [P, I, P, P, I, I, I, P, P, P, P, Z, P, P]
@@ -409,3 +414,52 @@ def spec_tree_mask(parent: torch.Tensor, *, out=None, device_status=None, stream
     if rc:
         raise SpecVerifyError(rc, "spec_tree_mask")
     return out
+
+
+def dynaspec_budget(kmax: int, K: int) -> list[int]:
+    """Clusters the drafter uses at draft step t = 0..K-1 under DynaSpec's
+    position-aware budget (DynaSpec summary, § Method 3): kmax for t in {0, 1},
+    floor(kmax / ((t + 1) * 2)) for t >= 2, taken as printed, and at least one
+    cluster (an empty shortlist would leave the drafter nothing to propose)."""
+    return [kmax if t < 2 else max(1, kmax // ((t + 1) * 2)) for t in range(K)]
+
+
+def spec_verify_shortlist_pos(target: torch.Tensor, draft_sl: torch.Tensor, shortlist_idx: torch.Tensor,
+                              draft_tokens: torch.Tensor, T: float, seed: int, *, shortlist_len=None,
+                              out_tokens=None, out_accept_len=None, workspace=None, aux: Aux | None = None,
+                              stream=None):
+    """Verification with per-position shortlists: shortlist_idx [B][K][S] (one
+    list per position), [B][S] (one per sequence) or [S] (one shared list), int32
+    strictly ascending; draft_sl [B][K][S] logits of the target's dtype, row
+    (b, i) holding shortlist_len[i] entries (a host sequence of K ints; default S)."""
+    B, K1, V = target.shape
+    K = K1 - 1
+    S = shortlist_idx.shape[-1]
+    _check(target, (B, K + 1, V), (torch.float32, torch.bfloat16), "target")
+    _check(draft_sl, (B, K, S), (target.dtype,), "draft_sl")
+    _check(draft_tokens, (B, K), (torch.int32,), "draft_tokens")
+    if shortlist_idx.dim() == 3:
+        _check(shortlist_idx, (B, K, S), (torch.int32,), "shortlist_idx")
+        seq, pos = K * S, S
+    elif shortlist_idx.dim() == 2:
+        _check(shortlist_idx, (B, S), (torch.int32,), "shortlist_idx")
+        seq, pos = S, 0
+    else:
+        _check(shortlist_idx, (S,), (torch.int32,), "shortlist_idx")
+        seq, pos = 0, 0
+    lens = None
+    if shortlist_len is not None:
+        lens = (ctypes.c_int32 * K)(*[int(x) for x in shortlist_len])
+    dev = target.device
+    out_tokens, out_accept_len = _outs(B, K, dev, out_tokens, out_accept_len)
+    st = _stream(dev, stream)
+    workspace, wsb = _ws_args(dev, st, spec_workspace_bytes(B, K, V, S), workspace, (B, K, V, S))
+    ax = aux._struct(B, K) if aux is not None else None
+    rc = load().spec_verify_shortlist_pos(target.data_ptr(), _dt(target), draft_sl.data_ptr(), _dt(draft_sl),
+                                          shortlist_idx.data_ptr(), seq, pos, lens, S, draft_tokens.data_ptr(),
+                                          B, K, V, float(T), int(seed) & (2**64 - 1), out_tokens.data_ptr(),
+                                          out_accept_len.data_ptr(), workspace.data_ptr(), wsb,
+                                          ctypes.byref(ax) if ax is not None else None, st)
+    if rc:
+        raise SpecVerifyError(rc, "spec_verify_shortlist_pos")
+    return out_tokens, out_accept_len

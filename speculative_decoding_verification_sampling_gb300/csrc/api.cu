@@ -254,9 +254,19 @@ spec_status_t run_sweep(bool greedy, const void *target, spec_dtype_t tdt, const
 
 // Row-parallel verification (k_rows.cu): logit draft rows (or greedy), no
 // shortlist.  Serves the per-position outputs too (then every row is read).
+// A shortlisted draft for run_rows: the list of (b, i) is the len[i] entries at
+// idx + b seq + i pos (len: host array of K entries), draft rows [B][K][S].
+struct RowsShortlist {
+    const int32_t *idx = nullptr;
+    long long seq = 0, pos = 0;
+    const int32_t *len = nullptr;
+    int S = 0;
+};
+
 spec_status_t run_rows(bool greedy, const void *target, spec_dtype_t tdt, const void *draft, const int32_t *tokens,
                        int B, int K, int V, float T, uint64_t seed, int32_t *out_tokens, int32_t *out_len,
-                       void *workspace, const sv::WsLayout &L, const spec_aux_t *aux, void *stream)
+                       void *workspace, const sv::WsLayout &L, const spec_aux_t *aux, void *stream,
+                       const RowsShortlist &sl = RowsShortlist())
 {
     if ((long long)B * (2 * K + 1) > INT32_MAX || (long long)B * sv::rows_chunks() > INT32_MAX)
         return SPEC_ERR_UNSUPPORTED;
@@ -291,6 +301,16 @@ spec_status_t run_rows(bool greedy, const void *target, spec_dtype_t tdt, const 
     P.skip = (P.aux_q || P.aux_p || P.aux_lse) ? 0 : 1;
     P.vec = ((long long)V * es) % 16 == 0 && reinterpret_cast<uintptr_t>(target) % 16 == 0 &&
             (greedy || reinterpret_cast<uintptr_t>(draft) % 16 == 0);
+    if (sl.idx && !greedy) {
+        P.sl = sl.idx;
+        P.sl_seq = sl.seq;
+        P.sl_pos = sl.pos;
+        P.S = sl.S;
+        for (int i = 0; i < K; ++i)
+            P.sl_len[i] = sl.len ? sl.len[i] : sl.S;
+        P.lb = reinterpret_cast<int32_t *>(w + L.vr_lb);
+        P.vec = P.vec && ((long long)sl.S * es) % 16 == 0;
+    }
     P.c = greedy ? 1.0f : (float)(1.4426950408889634 / (double)T);
     P.key0 = (uint32_t)(seed & 0xffffffffu);
     P.key1 = (uint32_t)(seed >> 32);
@@ -428,6 +448,22 @@ spec_status_t run(int mode, const void *target, spec_dtype_t tdt, const void *dr
     if (st != SPEC_OK)
         return st;
 
+    // shortlisted draft logits with enough rows to fill the GPU: the row-parallel
+    // kernels, every position using the sequence's list
+    if (mode == sv::MODE_SHORT && !probs) {
+        const KernelChoice kc = kernel_choice();
+        if (kc == KC_ROWS || (kc == KC_AUTO && (long long)B * (2 * K + 1) >= kRowsMinRows)) {
+            RowsShortlist sl;
+            sl.idx = shortlist;
+            sl.seq = S;
+            sl.pos = 0;
+            sl.S = S;
+            const spec_status_t rs = run_rows(false, target, tdt, draft, tokens, B, K, V, T, seed, out_tokens,
+                                              out_len, workspace, L, aux, stream, sl);
+            if (rs != SPEC_ERR_UNSUPPORTED)
+                return rs;
+        }
+    }
     if (mode == sv::MODE_GREEDY || (mode == sv::MODE_STOCH && !probs)) {
         const bool full = aux && (aux->q_draft || aux->p_draft || aux->row_lse);
         const KernelChoice kc = kernel_choice();
@@ -588,6 +624,42 @@ spec_status_t spec_verify_shortlist(const void *target_logits, spec_dtype_t tdt,
     return run(sv::MODE_SHORT, target_logits, tdt, draft_sl, ddt, draft_is_probs, shortlist_idx, S,
                draft_tokens, B, K, V, T, seed, out_tokens, out_accept_len, workspace, workspace_bytes, aux,
                stream);
+}
+
+spec_status_t spec_verify_shortlist_pos(const void *target_logits, spec_dtype_t tdt, const void *draft_sl,
+                                        spec_dtype_t ddt, const int32_t *shortlist_idx, long long sl_seq_stride,
+                                        long long sl_pos_stride, const int32_t *shortlist_len, int S,
+                                        const int32_t *draft_tokens, int B, int K, int V, float T, uint64_t seed,
+                                        int32_t *out_tokens, int32_t *out_accept_len, void *workspace,
+                                        size_t workspace_bytes, const spec_aux_t *aux, void *stream)
+{
+    if (!sizes_ok(B, K, V, S) || S < 1 || S > V || sl_seq_stride < 0 || sl_pos_stride < 0)
+        return SPEC_ERR_INVALID_ARG;
+    if (!target_logits || !draft_sl || !shortlist_idx || !draft_tokens || !out_tokens || !out_accept_len ||
+        !workspace)
+        return SPEC_ERR_INVALID_ARG;
+    if ((tdt != SPEC_F32 && tdt != SPEC_BF16) || ddt != tdt || !std::isfinite(T) || T < 0.0f)
+        return SPEC_ERR_INVALID_ARG;
+    if (shortlist_len)
+        for (int i = 0; i < K; ++i)
+            if (shortlist_len[i] < 1 || shortlist_len[i] > S)
+                return SPEC_ERR_INVALID_ARG;
+    if (T == 0.0f)   // greedy: the draft is not read
+        return run(sv::MODE_GREEDY, target_logits, tdt, nullptr, tdt, 0, nullptr, 0, draft_tokens, B, K, V, T,
+                   seed, out_tokens, out_accept_len, workspace, workspace_bytes, aux, stream);
+    if (!std::isfinite((float)(1.4426950408889634 / (double)T)))
+        return SPEC_ERR_INVALID_ARG;
+    const sv::WsLayout L = sv::ws_layout(B, K, V, S);
+    if (workspace_bytes < L.total || (reinterpret_cast<uintptr_t>(workspace) & 15u))
+        return SPEC_ERR_INVALID_ARG;
+    RowsShortlist sl;
+    sl.idx = shortlist_idx;
+    sl.seq = sl_seq_stride;
+    sl.pos = sl_pos_stride;
+    sl.len = shortlist_len;
+    sl.S = S;
+    return run_rows(false, target_logits, tdt, draft_sl, draft_tokens, B, K, V, T, seed, out_tokens,
+                    out_accept_len, workspace, L, aux, stream, sl);
 }
 
 // Verification without a caller workspace.  Callers that cannot allocate, or

@@ -106,6 +106,8 @@ __device__ __forceinline__ int vr_decide(const RowsParams &P, int b, int i, int 
                                          const VrStat &d, bool &accept)
 {
     accept = false;
+    if (i < P.K && (d.flags & VR_SLBAD))
+        return ST_SHORTLIST;   // the position's shortlist, before its token
     if (i < P.K && !(dt >= 0 && dt < P.V))
         return ST_TOKEN;
     if (P.greedy) {
@@ -190,10 +192,15 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
             return;
         }
     }
-    const uint8_t *row = kind ? static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + i) * (size_t)V * E::ES
-                              : static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + i) * (size_t)V * E::ES;
+    // a shortlisted draft row holds sl_len[i] logits, for the listed tokens
+    const bool slrow = kind && P.sl;
+    const int nrow = slrow ? P.sl_len[i] : V;
+    const uint8_t *row =
+        kind ? static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + i) * (size_t)(P.sl ? P.S : V) * E::ES
+             : static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + i) * (size_t)V * E::ES;
+    const int32_t *lst = slrow ? P.sl + b * P.sl_seq + i * P.sl_pos : nullptr;
     const int dt = i < K ? __ldg(P.tokens + (size_t)b * K + i) : -1;
-    const int t0 = min(V, part * P.span), t1 = min(V, t0 + P.span);
+    const int t0 = min(nrow, part * P.span), t1 = min(nrow, t0 + P.span);
     const int u0 = t0 / 8, nu = (t1 - t0 + 7) / 8;   // this part's units of 8 tokens
     const float c = P.c;
     float mc = -F_INF, s = 0.0f, bv = -F_INF, zd = 0.0f;
@@ -215,7 +222,37 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
                 if (g + 4 * VT < nu)
                     u[k] = fetch_unit<E>(row, (u0 + g + 4 * VT) * 8, t1, P.vec);
                 const int x0 = (u0 + g) * 8;
-                if ((unsigned)(dt - x0) < 8u || P.greedy) {
+                if (slrow) {
+                    // the unit's list entries: strictly ascending inside [0, V); the
+                    // drafted token's logit; the first entry of each 256-token segment
+                    float x[8];
+#pragma unroll
+                    for (int p = 0; p < 4; ++p)
+                        upk(X[p], x[2 * p], x[2 * p + 1]);
+                    int32_t *lb = P.lb + ((size_t)b * K + i) * (P.nseg + 1);
+                    int prev = x0 > 0 ? __ldg(lst + x0 - 1) : -1;
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int si = x0 + e;
+                        if (si >= t1)
+                            break;
+                        const int cur = __ldg(lst + si);
+                        if (cur < 0 || cur >= V || cur <= prev) {
+                            fl |= VR_SLBAD;
+                        } else {
+                            if (cur == dt) {
+                                zd = x[e];
+                                hz = true;
+                            }
+                            for (int t = prev < 0 ? 0 : prev / VSEG + 1; t <= cur / VSEG; ++t)
+                                lb[t] = si;
+                            if (si == nrow - 1)
+                                for (int t = cur / VSEG + 1; t <= P.nseg; ++t)
+                                    lb[t] = nrow;
+                        }
+                        prev = cur;
+                    }
+                } else if ((unsigned)(dt - x0) < 8u || P.greedy) {
                     float x[8];
 #pragma unroll
                     for (int p = 0; p < 4; ++p)
@@ -239,9 +276,11 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
             }
         }
     }
-    fl = warp_or(fl);
-    if (hz)
+    if (hz) {
         sm_zd = zd;
+        fl |= VR_HASD;
+    }
+    fl = warp_or(fl);
     if (P.greedy) {
 #pragma unroll
         for (int o = 16; o; o >>= 1)
@@ -268,10 +307,9 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
     const bool in = lane < NW;
     VrStat st{};
     st.flags = warp_or(in ? sm_f[lane] : 0);
-    if ((unsigned)(dt - t0) < (unsigned)(t1 - t0)) {
-        st.zd = sm_zd;
-        st.flags |= VR_HASD;
-    }
+    // the drafted token's logit, from the thread that held it (VR_HASD); a
+    // shortlisted draft row without it gives p(d) = 0
+    st.zd = (st.flags & VR_HASD) ? sm_zd : (slrow ? -F_INF : 0.0f);
     if (P.greedy) {
         float v = in ? sm_m[lane] : -F_INF;
         int ix = in ? sm_i[lane] : -1;
@@ -295,6 +333,7 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
         if (vr_atom_add(P.rowcnt + ridx, 1u) != (uint32_t)(P.parts - 1))
             return;
         VrStat m{};
+        m.zd = slrow ? -F_INF : 0.0f;
         float Mx = -F_INF;
         for (int h = 0; h < P.parts; ++h) {
             const VrStat q = ld_vrstat(pp + h);
@@ -424,12 +463,46 @@ __device__ __forceinline__ ResK vr_coef(const RowsParams &P, int b, int j)
     return k;
 }
 
+// Draft logits of the 8 tokens [seg * VSEG + 8 lane, +8) from a shortlisted
+// draft row (b, j): the segment's list entries (lb gives their range) are
+// scattered into a per-warp buffer of VSEG floats; tokens off the list read
+// -inf, i.e. p = 0.
+template <class E>
+__device__ __forceinline__ void sl_pairs(const RowsParams &P, int b, int j, int seg, int lane, float *buf, f2 *XD)
+{
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        buf[lane * 8 + e] = -F_INF;
+    __syncwarp();
+    if (seg < P.nseg) {
+        const int32_t *lb = P.lb + ((size_t)b * P.K + j) * (P.nseg + 1);
+        const int32_t *lst = P.sl + b * P.sl_seq + j * P.sl_pos;
+        const void *drow = static_cast<const uint8_t *>(P.draft) + ((size_t)b * P.K + j) * (size_t)P.S * E::ES;
+        const int lo = __ldcg(lb + seg), hi = __ldcg(lb + seg + 1);
+        for (int si = lo + lane; si < hi; si += 32) {
+            const int pos = __ldg(lst + si) - seg * VSEG;
+            if ((unsigned)pos < (unsigned)VSEG)
+                buf[pos] = E::load(drow, (size_t)si);
+        }
+    }
+    __syncwarp();
+    float x[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        x[e] = buf[lane * 8 + e];
+    __syncwarp();
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+        XD[p] = pk(x[2 * p], x[2 * p + 1]);
+}
+
 template <class E>
 __global__ void __launch_bounds__(VRT) vr_residual(const __grid_constant__ RowsParams P)
 {
     constexpr int NW = VRT / 32;
     constexpr int UPS = VSEG / 8;   // units per segment (one per lane)
     __shared__ int sm_j, sm_code;
+    __shared__ float sl_buf[NW][VSEG];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x / P.nch, ch = blockIdx.x % P.nch;
     const int K = P.K, V = P.V;
@@ -443,10 +516,11 @@ __global__ void __launch_bounds__(VRT) vr_residual(const __grid_constant__ RowsP
         return;
     const int j = sm_j;
     const bool qonly = j == K;
+    const bool slist = P.sl && !qonly;   // draft values come from the shortlist
     const ResK k = vr_coef(P, b, j);
     const uint8_t *trow = static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + j) * (size_t)V * E::ES;
     const uint8_t *drow =
-        qonly ? trow : static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + j) * (size_t)V * E::ES;
+        (qonly || slist) ? trow : static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + j) * (size_t)V * E::ES;
     // this chunk's segments [s_lo, s_hi); at step t warp w takes segment
     // s_lo + t * NW + w, lane l its unit l (tokens seg * VSEG + 8 l ..)
     const int spc = (P.nseg + P.nch - 1) / P.nch;
@@ -460,7 +534,7 @@ __global__ void __launch_bounds__(VRT) vr_residual(const __grid_constant__ RowsP
     for (int q = 0; q < 4; ++q)
         if (q < nsteps) {
             ut[q] = fetch_unit<E>(trow, unit_x0(q), V, P.vec);
-            if (!qonly)
+            if (!qonly && !slist)
                 ud[q] = fetch_unit<E>(drow, unit_x0(q), V, P.vec);
         }
     for (int t0 = 0; t0 < nsteps; t0 += 4) {
@@ -470,11 +544,13 @@ __global__ void __launch_bounds__(VRT) vr_residual(const __grid_constant__ RowsP
             if (t < nsteps) {
                 f2 XT[4], XD[4];
                 unit_pairs<E>(ut[q], XT);
-                if (!qonly)
+                if (slist)
+                    sl_pairs<E>(P, b, j, s_lo + t * NW + warp, lane, sl_buf[warp], XD);
+                else if (!qonly)
                     unit_pairs<E>(ud[q], XD);
                 if (t + 4 < nsteps) {
                     ut[q] = fetch_unit<E>(trow, unit_x0(t + 4), V, P.vec);
-                    if (!qonly)
+                    if (!qonly && !slist)
                         ud[q] = fetch_unit<E>(drow, unit_x0(t + 4), V, P.vec);
                 }
                 float r[8], qv[8];
@@ -506,6 +582,7 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
 {
     constexpr int NW = VST / 32;
     __shared__ int sm_j, sm_code, sm_seg, sm_last[NW];
+    __shared__ float sl_buf0[VSEG];
     __shared__ DF sm_r[NW], sm_q[NW], sm_before;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x;
@@ -521,22 +598,32 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
 
     // per-position outputs (every row was computed when they are asked for)
     if (P.aux_q || P.aux_p || P.aux_lse) {
-        for (int i = tid; i < 2 * K + 1; i += VST) {
-            const VrStat s = ld_vrstat(st + i);
-            const bool ok = !(s.flags & (VR_BAD | VR_SKIP)) && s.m > -F_INF && s.s_hi > 0.0f;
+        // log2 of the row's sum 2^(x c); whether the row is usable
+        auto row_l2 = [&](const VrStat &s, bool &ok) {
+            ok = !(s.flags & (VR_BAD | VR_SKIP | VR_SLBAD)) && s.m > -F_INF && s.s_hi > 0.0f;
             int e;
             float f;
             log2_split(DF{s.s_hi, s.s_lo}, e, f);
-            const float l2 = s.m + ((float)e + f);   // log2 sum 2^(x c)
+            return s.m + ((float)e + f);
+        };
+        const float nan = __int_as_float(0x7fc00000);
+        for (int i = tid; i < 2 * K + 1; i += VST) {
+            bool ok;
+            const float l2 = row_l2(ld_vrstat(st + i), ok);
             if (P.aux_lse)
-                P.aux_lse[(size_t)b * (2 * K + 1) + i] = ok ? l2 * 0.6931471805599453f : __int_as_float(0x7fc00000);
-            const int pos = i <= K ? i : i - K - 1;
-            if (pos < K && (i <= K ? P.aux_q : P.aux_p)) {
-                const int dt = __ldg(P.tokens + (size_t)b * K + pos);
-                const bool tok_ok = dt >= 0 && dt < V;
-                const float v = ok && tok_ok ? ex2a(fmaf(s.zd, P.c, -l2)) : __int_as_float(0x7fc00000);
-                (i <= K ? P.aux_q : P.aux_p)[(size_t)b * K + pos] = v;
-            }
+                P.aux_lse[(size_t)b * (2 * K + 1) + i] = ok ? l2 * 0.6931471805599453f : nan;
+        }
+        // q_i(d_i) and p_i(d_i) where both rows of the position and the token are usable
+        for (int i = tid; i < K; i += VST) {
+            const VrStat t = ld_vrstat(st + i), d = ld_vrstat(st + K + 1 + i);
+            bool okt, okd;
+            const float lt = row_l2(t, okt), ld = row_l2(d, okd);
+            const int dt = __ldg(P.tokens + (size_t)b * K + i);
+            const bool ok = okt && okd && dt >= 0 && dt < V;
+            if (P.aux_q)
+                P.aux_q[(size_t)b * K + i] = ok ? ex2a(fmaf(t.zd, P.c, -lt)) : nan;
+            if (P.aux_p)
+                P.aux_p[(size_t)b * K + i] = ok ? ex2a(fmaf(d.zd, P.c, -ld)) : nan;
         }
     }
     if (code) {
@@ -639,17 +726,20 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
             if (seg >= 0) {
                 const ResK k = vr_coef(P, b, j);
                 const bool qonly = j == K || useq;
+                const bool slist = P.sl && !qonly;
                 const uint8_t *trow =
                     static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + j) * (size_t)V * E::ES;
-                const uint8_t *drow = static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + j) * (size_t)V * E::ES;
                 const int x0 = seg * VSEG + lane * 8;
                 const Unit<E> ut = fetch_unit<E>(trow, x0, V, P.vec);
                 Unit<E> ud{};
-                if (!qonly)
-                    ud = fetch_unit<E>(drow, x0, V, P.vec);
+                if (!qonly && !slist)
+                    ud = fetch_unit<E>(static_cast<const uint8_t *>(P.draft) +
+                                           ((size_t)b * K + j) * (size_t)V * E::ES, x0, V, P.vec);
                 f2 XT[4], XD[4];
                 unit_pairs<E>(ut, XT);
-                if (!qonly)
+                if (slist)
+                    sl_pairs<E>(P, b, j, seg, lane, sl_buf0, XD);
+                else if (!qonly)
                     unit_pairs<E>(ud, XD);
                 float r[8], q[8];
                 vr_res8(XT, XD, k, qonly, r, q);

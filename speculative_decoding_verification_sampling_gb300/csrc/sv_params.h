@@ -210,7 +210,7 @@ struct alignas(16) VrStat {
     float zd;
     int pad0, pad1, pad2;
 };
-enum { VR_BAD = 1, VR_SKIP = 2, VR_HASD = 4 };
+enum { VR_BAD = 1, VR_SKIP = 2, VR_HASD = 4, VR_SLBAD = 8 };
 constexpr int VR_SMAX = 16;   // most parts a row is split into
 struct VrSeg {
     float r, q;   // residual and target masses of one 256-token segment, relative to 2^Mt
@@ -234,6 +234,14 @@ struct RowsParams {
     VrSeg *segm;             // [B][nseg]
     int B, K, V, nseg, nch;
     int pos, npos;             // vr_stats: the positions [pos, pos + npos) this launch streams
+    // shortlisted draft (sl != nullptr): the draft row of (b, i) holds sl_len[i]
+    // logits for the tokens sl[b sl_seq + i sl_pos + s] (ascending); draft rows
+    // are [B][K][S]; lb[(b K + i)][t] is the first list entry >= 256 t
+    const int32_t *sl;
+    long long sl_seq, sl_pos;
+    int S;
+    int sl_len[32];
+    int32_t *lb;               // [B][K][nseg + 1]
     int parts, span;           // vr_stats: parts per row, tokens per part (a multiple of 8)
     int greedy, skip, vec;
     float c;
@@ -243,7 +251,7 @@ struct RowsParams {
 struct WsLayout {
     size_t ctl, state, res_rec, pair_cnt, res_cnt, fin, errres, sw_ctl, sw_seq, sw_cnt, sw_res_ready, sw_res_done,
         vr_pair, vr_rej, vr_rowcnt, errcode, terminal, gtok, dec, part, seg, sl_lb, sw_part, sw_stat, sw_res, sw_resm,
-        vr_stat, vr_errc, vr_part, vr_segm, total;
+        vr_stat, vr_errc, vr_part, vr_segm, vr_lb, total;
     size_t reset_end;   // [ctl, reset_end) holds what a call must find zeroed
     int npt_max, nseg;
 };
@@ -291,6 +299,7 @@ inline WsLayout ws_layout(int B, int K, int V, int S)
     w.vr_errc = o;  o = align256(o + Bz * P * 4);
     w.vr_part = o;  o = align256(o + Bz * (2 * P - 1) * (size_t)VR_SMAX * sizeof(VrStat));
     w.vr_segm = o;  o = align256(o + Bz * (size_t)w.nseg * sizeof(VrSeg));
+    w.vr_lb = o;    o = align256(o + (S > 0 ? Bz * (P - 1) * (size_t)(w.nseg + 1) * 4 : 0));
     w.total = o;
     return w;
 }

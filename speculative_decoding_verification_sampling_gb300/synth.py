@@ -221,3 +221,39 @@ def tree_greedy(B: int = 32, V: int = 128256, branching=(4, 2, 2, 1, 1), dtype=t
     par = torch.tensor(parent, dtype=torch.int32, device=device).expand(B, N).contiguous()
     return dict(name=f"tree greedy B={B} N={N} V={V} branching={tuple(branching)}", target=target,
                 tree_tokens=tokens.to(torch.int32), parent=par, B=B, N=N, V=V)
+
+
+def shortlist_per_position(B: int = 64, K: int = 6, V: int = 262144, n_clusters: int = 64, budget=None,
+                           dtype=torch.bfloat16, T: float = 1.0, sigma: float = 0.5, seed: int = 7,
+                           device="cpu") -> dict:
+    """Per-position shortlists: the vocabulary split at random into n_clusters
+    clusters; at draft step t each sequence draws budget[t] clusters (default
+    the DynaSpec position-aware budget with k_max = 8: 8, 8, 1, 1, 1, 1), whose
+    sorted union is its list; target is full-vocabulary Zipf, the draft is
+    target + N(0, sigma^2) on the list, compact [B][K][S] with S = max list
+    length (row (b, t) holds len[t] entries); drafted tokens from the draft
+    softmax on the list."""
+    if budget is None:
+        budget = [8 if t < 2 else max(1, 8 // ((t + 1) * 2)) for t in range(K)]
+    g = _gen(seed, device)
+    target = zipf_logits(B * (K + 1), V, g, device).reshape(B, K + 1, V).to(dtype)
+    size = V // n_clusters
+    clusters = torch.randperm(V, generator=g, device=device)[:n_clusters * size].reshape(n_clusters, size)
+    lens = [budget[t] * size for t in range(K)]
+    S = max(lens)
+    lists = torch.zeros((B, K, S), dtype=torch.int32, device=device)
+    draft = torch.zeros((B, K, S), dtype=torch.float32, device=device)
+    tokens = torch.zeros((B, K), dtype=torch.int32, device=device)
+    for t in range(K):
+        n = lens[t]
+        for b in range(B):
+            pick = torch.randperm(n_clusters, generator=g, device=device)[:budget[t]]
+            lst = torch.sort(clusters[pick].reshape(-1)).values
+            lists[b, t, :n] = lst.to(torch.int32)
+        idx = lists[:, t, :n].long()
+        draft[:, t, :n] = torch.gather(target[:, t].float(), 1, idx) + _normal((B, n), sigma, g, device)
+        pos = gumbel_max_tokens(draft[:, t, :n].to(dtype), T, g).long()
+        tokens[:, t] = torch.gather(idx, 1, pos[:, None])[:, 0].to(torch.int32)
+    return dict(name=f"per-position shortlists B={B} K={K} V={V} lens={lens}", target=target,
+                draft=draft.to(dtype), draft_tokens=tokens, T=T, shortlist=lists, shortlist_len=lens,
+                B=B, K=K, V=V, S=S)
