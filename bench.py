@@ -619,7 +619,63 @@ def _tree_greedy_workload(B: int, K: int, dev):
                 l2=f"inputs larger than L2: device copies of the {nbytes / 1e6:.0f} MB node rows, rotated")
 
 
-EXTRA_WORKLOADS = {"draft_sample": _draft_sample_workload, "kv_commit": _kv_commit_workload,
+def _shortlist_pos_workload(B: int, K: int, dev):
+    """Verification with per-position shortlists: B=64, K=6, V=262144 bf16,
+    Zipf target, 64 clusters of 4096 tokens, the DynaSpec position-aware budget
+    with k_max = 8 (8, 8, 1, 1, 1, 1 clusters per draft step), draft = target +
+    N(0, 0.5^2) on each list (compact rows of up to 32768 logits)."""
+    import torch
+    import oracle
+    import speculative_decoding_verification_sampling_gb300 as sv
+    from speculative_decoding_verification_sampling_gb300 import synth
+    Bs, Ks, Vs = 64, 6, 262144
+    cfg = synth.shortlist_per_position(B=Bs, K=Ks, V=Vs, seed=DATA_SEED)
+    lens = cfg["shortlist_len"]
+    S = cfg["S"]
+    host = [cfg["target"], cfg["draft"], cfg["shortlist"], cfg["draft_tokens"]]
+    nbytes = sum(h.numel() * h.element_size() for h in host)
+    ref = oracle.verify(cfg["target"], cfg["draft"], cfg["draft_tokens"], TEMPERATURE, VERIFY_SEED,
+                        shortlist=cfg["shortlist"], shortlist_len=lens)
+    # bytes the left-to-right rule reads: target rows 0..j, draft rows and lists 0..min(j, K-1)
+    need = 0
+    for j in ref["accept_len"].tolist():
+        j = Ks if j < 0 else j
+        need += (j + 1) * Vs * 2 + sum(lens[t] * 6 for t in range(min(j + 1, Ks)))
+    need += Bs * (Ks * 4 + (Ks + 1) * 4 + 4)
+
+    def make_sets(n):
+        d0 = [h.to(dev) for h in host]
+        return [(d0 if i == 0 else [x.clone() for x in d0]) + [None] for i in range(n)]
+
+    def call(st, stream):
+        t, d, sl, k, _ = st
+        st[4] = sv.spec_verify_shortlist_pos(t, d, sl, k, TEMPERATURE, VERIFY_SEED, shortlist_len=lens,
+                                             stream=stream)
+
+    def result(st):
+        return st[4][0].cpu()
+
+    def oracle_run(i):
+        b = i % Bs
+        oracle.verify(cfg["target"][b:b + 1], cfg["draft"][b:b + 1], cfg["draft_tokens"][b:b + 1], TEMPERATURE,
+                      VERIFY_SEED, shortlist=cfg["shortlist"][b:b + 1], shortlist_len=lens, seq_ids=[b],
+                      threads=1)
+        return Ks
+
+    return dict(metric="verified draft positions/s with per-position shortlists (DynaSpec budget, V=262144 "
+                       "bf16); achieved HBM GB/s", unit="positions/s", units=Bs * Ks, alg_bytes=need,
+                h2d=nbytes, d2h=Bs * (Ks + 2) * 4, make_sets=make_sets, call=call, result=result,
+                host_inputs=host, upload=lambda st: st[:4], oracle_run=oracle_run,
+                kernel="vr_stats x2 + vr_residual + vr_sample (row-parallel, per-position shortlists)",
+                B=Bs, K=Ks,
+                workload=f"per-position shortlists B={Bs} K={Ks} V={Vs} bf16 T=1: Zipf target, 64 clusters "
+                         f"of 4096, budget (8, 8, 1, 1, 1, 1) clusters, list lengths {lens}, draft = "
+                         f"target + N(0, 0.5^2) on the lists",
+                l2=f"inputs larger than L2: device copies of the {nbytes / 1e6:.0f} MB input set, rotated")
+
+
+EXTRA_WORKLOADS = {"shortlist_pos": _shortlist_pos_workload,
+                   "draft_sample": _draft_sample_workload, "kv_commit": _kv_commit_workload,
                    "tree_greedy": _tree_greedy_workload}
 
 

@@ -155,7 +155,7 @@ __device__ __forceinline__ int vr_end(const RowsParams &P, int b, int &j)
 }
 
 // ---------------------------------------------------------------- 1. row statistics
-template <class E, int VT>
+template <class E, int VT, bool SL>
 __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParams P)
 {
     constexpr int NW = VT / 32;
@@ -193,10 +193,10 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
         }
     }
     // a shortlisted draft row holds sl_len[i] logits, for the listed tokens
-    const bool slrow = kind && P.sl;
+    const bool slrow = SL && kind;   // (SL: the call has a shortlisted draft)
     const int nrow = slrow ? P.sl_len[i] : V;
     const uint8_t *row =
-        kind ? static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + i) * (size_t)(P.sl ? P.S : V) * E::ES
+        kind ? static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + i) * (size_t)(SL ? P.S : V) * E::ES
              : static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + i) * (size_t)V * E::ES;
     const int32_t *lst = slrow ? P.sl + b * P.sl_seq + i * P.sl_pos : nullptr;
     const int dt = i < K ? __ldg(P.tokens + (size_t)b * K + i) : -1;
@@ -821,7 +821,10 @@ cudaError_t launch_stats(RowsParams P, int pos, int npos, int sms, cudaStream_t 
     P.npos = npos;
     P.span = ((P.V + S - 1) / S + 7) / 8 * 8;
     P.parts = (P.V + P.span - 1) / P.span;
-    vr_stats<E, VST_T><<<rows * P.parts, VST_T, 0, stream>>>(P);
+    if (P.sl)
+        vr_stats<E, VST_T, true><<<rows * P.parts, VST_T, 0, stream>>>(P);
+    else
+        vr_stats<E, VST_T, false><<<rows * P.parts, VST_T, 0, stream>>>(P);
     return cudaGetLastError();
 }
 
