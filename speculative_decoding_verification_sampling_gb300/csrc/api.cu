@@ -292,6 +292,8 @@ spec_status_t run_rows(bool greedy, const void *target, spec_dtype_t tdt, const 
     P.rowcnt = reinterpret_cast<uint32_t *>(w + L.vr_rowcnt);
     P.vpart = reinterpret_cast<sv::VrStat *>(w + L.vr_part);
     P.segm = reinterpret_cast<sv::VrSeg *>(w + L.vr_segm);
+    P.vctl = reinterpret_cast<uint32_t *>(w + L.vr_ctl);
+    P.spin_limit = spin_limit();
     P.B = B;
     P.K = K;
     P.V = V;
@@ -317,9 +319,10 @@ spec_status_t run_rows(bool greedy, const void *target, spec_dtype_t tdt, const 
     if (debug_enabled())
         std::fprintf(stderr, "specverify: rows kernels %s %s B=%d K=%d V=%d skip=%d vec=%d\n",
                      greedy ? "greedy" : "stochastic", tdt == SPEC_BF16 ? "bf16" : "f32", B, K, V, P.skip, P.vec);
-    if (sv::launch_rows(P, tdt == SPEC_BF16 ? 1 : 0, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    int nl = 0;
+    if (sv::launch_rows(P, tdt == SPEC_BF16 ? 1 : 0, static_cast<cudaStream_t>(stream), &nl) != cudaSuccess)
         return SPEC_ERR_CUDA;
-    g_launches.fetch_add((uint64_t)sv::rows_launches(K, greedy), std::memory_order_relaxed);
+    g_launches.fetch_add((uint64_t)nl, std::memory_order_relaxed);
     return SPEC_OK;
 }
 

@@ -1,18 +1,24 @@
-// k_rows.cu -- row-parallel verification: three kernels in stream order.
+// k_rows.cu -- row-parallel verification: statistics, residual masses, draw.
 //
 // The rule is that of the other kernels (nextadmin.net lesson "Speculative
 // Decoding", § Core algorithm steps 4-6; aiengineeringfromscratch.com lesson
 // 25, § The exact rule and § Greedy case; q = target, p = draft).  Here the
 // work is cut by rows instead of by sequences, so that every SM streams
 // independent rows at full bandwidth:
-//   1. vr_stats: one launch per position, one CTA per logit row of that
-//      position.  It streams the row once (16-byte loads, four in flight per
-//      thread) into its reference and sum (greedy: its argmax) and keeps the
-//      logit at the drafted token.  The CTA completing the second row of a
-//      position decides it; a rejection (or an error) sets the position's bit
-//      in the sequence's mask.  Rows of a sequence with a bit below their
-//      position skip their reads, so only the rows the left-to-right rule
-//      examines are streamed.
+//   1. Row statistics: each logit row is streamed once into its reference
+//      and sum (greedy: its argmax), keeping the logit at the drafted token.
+//      The second row of a position to finish decides it; a rejection (or an
+//      error) sets the position's bit in the sequence's mask.  Rows of a
+//      sequence with a bit below their position skip their reads, so only the
+//      rows the left-to-right rule examines are streamed (up to the rows
+//      started before the decision they wait on is known).
+//      - vr_stream (stochastic calls with draft logits and aligned rows): one
+//        persistent launch; rows are claimed position-major from a counter
+//        and copied in 16 KB stages by cp.async.bulk into a shared-memory
+//        ring, reduced by consumer warps; an epilogue thread decides.
+//      - vr_stats (greedy, shortlisted drafts, unaligned rows): one launch for
+//        positions 0-1 and one for the rest, one CTA per part of a row,
+//        16-byte loads with four in flight per thread.
 //   2. vr_residual: eight CTAs per sequence.  The mask gives the position j
 //      where the sequence ends; each CTA streams its eighth of row pair j into
 //      residual masses r' = q' (1 - 2^delta)_+ and target masses q' per
@@ -26,6 +32,7 @@
 #include "sv_launch.h"
 
 #include <algorithm>
+#include <cstdlib>
 
 namespace sv {
 namespace {
@@ -154,6 +161,75 @@ __device__ __forceinline__ int vr_end(const RowsParams &P, int b, int &j)
     return (m >> j) & 1u ? __ldcg(P.errc + (size_t)b * (P.K + 1) + j) : 0;
 }
 
+// A part's statistics st of row ridx (sequence b, position i; kind 1: the
+// draft row), from one CTA: the last part of the row to finish merges the
+// parts in part order and writes the row's statistics; the second row of a
+// position to finish decides it (greedy and position K: the only row), and a
+// rejection or an error sets the position's bit in rej.
+__device__ __noinline__ void vr_commit(const RowsParams &P, size_t ridx, int b, int i, int kind, int part, int dt,
+                                       VrStat st, bool slrow)
+{
+    const int K = P.K;
+    const bool pairs = !P.greedy && i < K;
+    if (P.parts > 1) {
+        // the last part of the row to finish merges the parts, in part order
+        VrStat *pp = P.vpart + ridx * VR_SMAX;
+        pp[part] = st;
+        if (vr_atom_add(P.rowcnt + ridx, 1u) != (uint32_t)(P.parts - 1))
+            return;
+        VrStat m{};
+        m.zd = slrow ? -F_INF : 0.0f;
+        float Mx = -F_INF;
+        for (int h = 0; h < P.parts; ++h) {
+            const VrStat q = ld_vrstat(pp + h);
+            m.flags |= q.flags;
+            if (q.flags & VR_HASD)
+                m.zd = q.zd;
+            if (P.greedy) {
+                if (h == 0) {
+                    m.m = q.m;
+                    m.s_hi = q.s_hi;
+                } else {
+                    int ix = __float_as_int(m.s_hi);
+                    argmax_merge(m.m, ix, q.m, __float_as_int(q.s_hi));
+                    m.s_hi = __int_as_float(ix);
+                }
+            } else {
+                Mx = fmaxf(Mx, q.m);
+            }
+        }
+        if (!P.greedy) {
+            DF S{0.0f, 0.0f};
+            for (int h = 0; h < P.parts; ++h) {
+                const VrStat q = ld_vrstat(pp + h);
+                if (q.m > -F_INF)
+                    S = df_add(S, df_scale_pow2(DF{q.s_hi, q.s_lo}, q.m - Mx));
+            }
+            m.m = Mx;
+            m.s_hi = S.hi;
+            m.s_lo = S.lo;
+        }
+        st = m;
+    }
+    P.stat[ridx] = st;
+    // the second row of a position to finish decides it (greedy and position K:
+    // the only row); a rejection or an error sets the position's bit
+    VrStat t = st, d{};
+    if (pairs) {
+        if (vr_atom_add(P.pair + (size_t)b * (K + 1) + i, 1u) != 1u)
+            return;
+        const VrStat o = ld_vrstat(P.stat + (size_t)b * (2 * K + 1) + (kind ? i : K + 1 + i));
+        t = kind ? o : st;
+        d = kind ? st : o;
+    }
+    bool acc = false;
+    const int code = vr_decide(P, b, i, dt, t, d, acc);
+    if (code || (!acc && i < K)) {
+        P.errc[(size_t)b * (K + 1) + i] = code;
+        atomicOr(P.rej + b, 1u << i);
+    }
+}
+
 // ---------------------------------------------------------------- 1. row statistics
 template <class E, int VT, bool SL>
 __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParams P)
@@ -173,7 +249,6 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
     const int rg = (int)blockIdx.x / P.parts, part = (int)blockIdx.x % P.parts;
     const int i = P.pos + rg / rpp;
     const int rl = rg % rpp;
-    const bool pairs = !P.greedy && i < K;
     const int b = P.greedy ? rl : rl >> 1;
     const int kind = P.greedy ? 0 : rl & 1;
     if (kind && i == K)
@@ -324,64 +399,292 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
         st.s_hi = S.hi;
         st.s_lo = S.lo;
     }
-    if (lane != 0)
-        return;
-    if (P.parts > 1) {
-        // the last part of the row to finish merges the parts, in part order
-        VrStat *pp = P.vpart + ridx * VR_SMAX;
-        pp[part] = st;
-        if (vr_atom_add(P.rowcnt + ridx, 1u) != (uint32_t)(P.parts - 1))
+    if (lane == 0)
+        vr_commit(P, ridx, b, i, kind, part, dt, st, slrow);
+}
+
+// ---------------------------------------------------------------- 1b. row statistics from a bulk-copy stream
+// The statistics and decisions of vr_stats for stochastic calls with aligned
+// rows and draft logits, from one persistent launch (VS_CPS CTAs per SM).
+// Rows are handed out position-major over every position from one counter,
+// each cut into P.parts parts; a row whose sequence has ended before its
+// position is skipped when its part is claimed, so the decisions of earlier
+// positions are mostly known by then.  In each CTA:
+//   - a producer thread claims parts and copies them in VS_STAGE-byte stages
+//     (cp.async.bulk, completion on the stage's mbarrier) into a ring of
+//     VS_NS stages, running ahead across parts;
+//   - VS_NCW consumer warps reduce each stage from shared memory (the
+//     per-token arithmetic of vr_stats), merge their partials at the end of
+//     a part and hand the part's statistics over to
+//   - an epilogue thread, which merges the parts of the row and decides the
+//     position (vr_commit), so the consumers never wait on global memory.
+// Every wait is bounded; one that runs out sets the timeout word, reported by
+// vr_sample as ST_TIMEOUT.
+constexpr int kMaxDevicesRows = 64;
+constexpr int VS_NS = 4;          // stages in the ring
+constexpr int VS_STAGE = 16384;   // bytes per stage
+constexpr int VS_CPS = 3;         // CTAs per SM
+constexpr int VS_NCW = 8;         // consumer warps
+constexpr int VS_EPN = 4;         // epilogue slots
+constexpr int VS_MB = 8;          // part-merge buffers (more than VS_NS)
+constexpr int VS_T = (VS_NCW + 2) * 32;
+
+struct VsMeta {
+    int item, tok0, ntok, last, dt;
+};
+struct VsEp {
+    VrStat st;
+    int item, dt, pad0, pad1;
+};
+
+// Bounded wait for the phase of parity `par`; sets the timeout word when the
+// polls run out.
+__device__ __forceinline__ bool vs_wait(unsigned long long *bar, uint32_t par, uint32_t limit, uint32_t *tflag)
+{
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_test(bar, par))
+            return true;
+        if (it >= limit) {
+            atomicExch(tflag, 1u);
+            return false;
+        }
+        if (it > 16)
+            __nanosleep(64);
+    }
+}
+
+// Row r of the stream's order: positions 0..K-1 hold the target and draft rows
+// of every sequence side by side, position K the B target rows.
+__device__ __forceinline__ void vs_row(const RowsParams &P, int r, int &i, int &b, int &kind)
+{
+    const int nk = 2 * P.B * P.K;
+    if (r < nk) {
+        i = r / (2 * P.B);
+        const int rl = r - i * 2 * P.B;
+        b = rl >> 1;
+        kind = rl & 1;
+    } else {
+        i = P.K;
+        b = r - nk;
+        kind = 0;
+    }
+}
+
+template <class E>
+__global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsParams P)
+{
+    extern __shared__ __align__(128) uint8_t vs_buf[];
+    __shared__ unsigned long long full[VS_NS], empty[VS_NS], epf[VS_EPN], epe[VS_EPN], mg[VS_MB];
+    __shared__ VsMeta meta[VS_NS];
+    __shared__ VsEp ep[VS_EPN];
+    __shared__ float rm[VS_MB][VS_NCW], rhi[VS_MB][VS_NCW], rlo[VS_MB][VS_NCW], rzd[VS_MB];
+    __shared__ int rfl[VS_MB][VS_NCW];
+    constexpr int STOK = VS_STAGE / E::ES;   // tokens per stage
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int K = P.K, V = P.V;
+    const uint32_t lim = P.spin_limit;
+    uint32_t *tflag = P.vctl + 1;
+    if (tid == 0) {
+        for (int s = 0; s < VS_NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], VS_NCW);
+        }
+        for (int s = 0; s < VS_EPN; ++s) {
+            mbar_init(&epf[s], 1);
+            mbar_init(&epe[s], 1);
+        }
+        for (int s = 0; s < VS_MB; ++s)
+            mbar_init(&mg[s], VS_NCW);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int nitems = P.B * (2 * K + 1) * P.parts;
+
+    if (warp == VS_NCW) {
+        // ---- producer
+        if (lane != 0)
             return;
-        VrStat m{};
-        m.zd = slrow ? -F_INF : 0.0f;
-        float Mx = -F_INF;
-        for (int h = 0; h < P.parts; ++h) {
-            const VrStat q = ld_vrstat(pp + h);
-            m.flags |= q.flags;
-            if (q.flags & VR_HASD)
-                m.zd = q.zd;
-            if (P.greedy) {
-                if (h == 0) {
-                    m.m = q.m;
-                    m.s_hi = q.s_hi;
-                } else {
-                    int ix = __float_as_int(m.s_hi);
-                    argmax_merge(m.m, ix, q.m, __float_as_int(q.s_hi));
-                    m.s_hi = __int_as_float(ix);
+        int st = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        int item = (int)atomicAdd(P.vctl, 1u);
+        while (ok && item < nitems) {
+            const int next = (int)atomicAdd(P.vctl, 1u);   // claimed ahead, used after this part
+            const int r = item / P.parts, part = item - r * P.parts;
+            int i, b, kind;
+            vs_row(P, r, i, b, kind);
+            const size_t ridx = (size_t)b * (2 * K + 1) + (kind ? K + 1 + i : i);
+            const uint32_t m = (P.skip && i > 0) ? __ldcg(P.rej + b) : 0u;
+            const int dt = i < K ? __ldg(P.tokens + (size_t)b * K + i) : -1;
+            if (m & ((1u << i) - 1u)) {
+                // a rejection (or error) decided at an earlier position makes this row unneeded
+                if (part == 0)
+                    P.stat[ridx] = VrStat{-F_INF, 0.0f, 0.0f, VR_SKIP, 0.0f, 0, 0, 0};
+                item = next;
+                continue;
+            }
+            const uint8_t *row =
+                kind ? static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + i) * (size_t)V * E::ES
+                     : static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + i) * (size_t)V * E::ES;
+            const int t0 = part * P.span, t1 = min(V, t0 + P.span);
+            for (int tok = t0; tok < t1; tok += STOK) {
+                const int n = min(STOK, t1 - tok);
+                if (!vs_wait(&empty[st], ph ^ 1u, lim, tflag)) {
+                    ok = false;
+                    break;
                 }
-            } else {
-                Mx = fmaxf(Mx, q.m);
+                meta[st] = VsMeta{item, tok, n, tok + STOK >= t1 ? 1 : 0, dt};
+                mbar_arrive_tx(&full[st], (uint32_t)(n * E::ES));
+                bulk_g2s(vs_buf + st * VS_STAGE, row + (size_t)tok * E::ES, (uint32_t)(n * E::ES), &full[st]);
+                if (++st == VS_NS) {
+                    st = 0;
+                    ph ^= 1u;
+                }
             }
+            item = next;
         }
-        if (!P.greedy) {
-            DF S{0.0f, 0.0f};
-            for (int h = 0; h < P.parts; ++h) {
-                const VrStat q = ld_vrstat(pp + h);
-                if (q.m > -F_INF)
-                    S = df_add(S, df_scale_pow2(DF{q.s_hi, q.s_lo}, q.m - Mx));
-            }
-            m.m = Mx;
-            m.s_hi = S.hi;
-            m.s_lo = S.lo;
+        // end of the stream
+        if (ok && vs_wait(&empty[st], ph ^ 1u, lim, tflag)) {
+            meta[st].item = -1;
+            mbar_arrive(&full[st]);
         }
-        st = m;
+        return;
     }
-    P.stat[ridx] = st;
-    // the second row of a position to finish decides it (greedy and position K:
-    // the only row); a rejection or an error sets the position's bit
-    VrStat t = st, d{};
-    if (pairs) {
-        if (vr_atom_add(P.pair + (size_t)b * (K + 1) + i, 1u) != 1u)
+    if (warp == VS_NCW + 1) {
+        // ---- epilogue
+        if (lane != 0)
             return;
-        const VrStat o = ld_vrstat(P.stat + (size_t)b * (2 * K + 1) + (kind ? i : K + 1 + i));
-        t = kind ? o : st;
-        d = kind ? st : o;
+        int es = 0;
+        uint32_t eph = 0;
+        while (vs_wait(&epf[es], eph, lim, tflag)) {
+            const VsEp e = ep[es];
+            mbar_arrive(&epe[es]);
+            if (++es == VS_EPN) {
+                es = 0;
+                eph ^= 1u;
+            }
+            if (e.item < 0)
+                break;
+            const int r = e.item / P.parts, part = e.item - r * P.parts;
+            int i, b, kind;
+            vs_row(P, r, i, b, kind);
+            const size_t ridx = (size_t)b * (2 * K + 1) + (kind ? K + 1 + i : i);
+            vr_commit(P, ridx, b, i, kind, part, e.dt, e.st, false);
+        }
+        return;
     }
-    bool acc = false;
-    const int code = vr_decide(P, b, i, dt, t, d, acc);
-    if (code || (!acc && i < K)) {
-        P.errc[(size_t)b * (K + 1) + i] = code;
-        atomicOr(P.rej + b, 1u << i);
+    // ---- consumers (threads 0 .. 32 VS_NCW - 1)
+    constexpr int CT = VS_NCW * 32;
+    const float c = P.c;
+    int st = 0, es = 0, nit = 0;
+    uint32_t ph = 0, eph = 0;
+    float mc = -F_INF, s = 0.0f, zd = 0.0f;
+    int fl = 0;
+    bool ok = true;
+    for (;;) {
+        if (lane == 0)
+            ok = vs_wait(&full[st], ph, lim, tflag);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok)
+            break;
+        (void)mbar_test(&full[st], ph);   // every lane observes the completed phase
+        const VsMeta mt = meta[st];
+        if (mt.item < 0)
+            break;
+        const uint8_t *sb = vs_buf + st * VS_STAGE;
+        const uint4 *p = reinterpret_cast<const uint4 *>(sb);
+        if constexpr (E::ES == 2) {
+            const int nv = mt.ntok >> 3;   // whole units: ntok is a multiple of 8
+#pragma unroll 4
+            for (int g = tid; g < nv; g += CT) {
+                Unit<E> u;
+                u.a = p[g];
+                f2 X[4];
+                unit_pairs<E>(u, X);
+                acc_group(X, c, mc, s, fl, VR_BAD);
+            }
+        } else {
+            const int nv = mt.ntok >> 2;   // 16-byte vectors of 4 tokens; a unit is vectors g and g + CT
+#pragma unroll 2
+            for (int g = tid; g < nv; g += 2 * CT) {
+                Unit<E> u;
+                u.a = p[g];
+                u.b = g + CT < nv ? p[g + CT] : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+                f2 X[4];
+                unit_pairs<E>(u, X);
+                acc_group(X, c, mc, s, fl, VR_BAD);
+            }
+        }
+        if (tid == 0 && (unsigned)(mt.dt - mt.tok0) < (unsigned)mt.ntok) {
+            const int o = mt.dt - mt.tok0;
+            zd = E::ES == 2 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(sb)[o] << 16)
+                            : reinterpret_cast<const float *>(sb)[o];
+            fl |= VR_HASD;
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[st]);
+        if (++st == VS_NS) {
+            st = 0;
+            ph ^= 1u;
+        }
+        if (mt.last) {
+            // the part's statistics: each warp posts its partial (buffer nit mod
+            // VS_MB, whose mbarrier completes once all consumer warps posted);
+            // warp 0 merges them and hands the result to the epilogue.  No warp
+            // runs more than VS_NS stages, so VS_NS parts, ahead of warp 0: the
+            // buffers never overlap.
+            const int h = nit & (VS_MB - 1);
+            const int wf = warp_or(fl);
+            float M;
+            DF S;
+            merge_ms<32>(mc, DF{s, 0.0f}, c, M, S);
+            if (lane == 0) {
+                rm[h][warp] = M;
+                rhi[h][warp] = S.hi;
+                rlo[h][warp] = S.lo;
+                rfl[h][warp] = wf;
+                if (fl & VR_HASD)
+                    rzd[h] = zd;   // thread 0 alone ever holds the drafted token
+                mbar_arrive(&mg[h]);
+            }
+            if (warp == 0) {
+                bool got = true;
+                if (lane == 0)
+                    got = vs_wait(&mg[h], (uint32_t)(nit / VS_MB) & 1u, lim, tflag);
+                got = __shfl_sync(0xffffffffu, got, 0);
+                if (got) {
+                    (void)mbar_test(&mg[h], (uint32_t)(nit / VS_MB) & 1u);
+                    const bool in = lane < VS_NCW;
+                    VrStat r{};
+                    r.flags = warp_or(in ? rfl[h][lane] : 0);
+                    r.zd = (r.flags & VR_HASD) ? rzd[h] : 0.0f;
+                    merge_ms<VS_NCW>(in ? rm[h][lane] : -F_INF,
+                                     in ? DF{rhi[h][lane], rlo[h][lane]} : DF{0.0f, 0.0f}, c, M, S);
+                    r.m = M;
+                    r.s_hi = S.hi;
+                    r.s_lo = S.lo;
+                    if (lane == 0 && vs_wait(&epe[es], eph ^ 1u, lim, tflag)) {
+                        ep[es] = VsEp{r, mt.item, mt.dt, 0, 0};
+                        mbar_arrive(&epf[es]);
+                    }
+                }
+                if (++es == VS_EPN) {
+                    es = 0;
+                    eph ^= 1u;
+                }
+                __syncwarp();
+            }
+            mc = -F_INF;
+            s = 0.0f;
+            zd = 0.0f;
+            fl = 0;
+            ++nit;
+        }
+    }
+    if (tid == 0 && vs_wait(&epe[es], eph ^ 1u, lim, tflag)) {
+        ep[es].item = -1;
+        mbar_arrive(&epf[es]);
     }
 }
 
@@ -590,6 +893,8 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
     if (tid == 0) {
         int j = 0;
         sm_code = vr_end(P, b, j);
+        if (__ldcg(P.vctl + 1))
+            sm_code = ST_TIMEOUT;   // the statistics stream gave up a wait
         sm_j = j;
     }
     __syncthreads();
@@ -799,8 +1104,15 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
         P.pair[(size_t)b * (K + 1) + i] = 0u;
     for (int i = tid; i < 2 * K + 1; i += VST)
         P.rowcnt[(size_t)b * (2 * K + 1) + i] = 0u;
-    if (tid == 0)
+    if (tid == 0) {
         P.rej[b] = 0u;
+        // the last CTA zeroes the call's counters (every CTA read the timeout word first)
+        if (vr_atom_add(P.vctl + 2, 1u) == gridDim.x - 1) {
+            P.vctl[0] = 0u;
+            P.vctl[1] = 0u;
+            P.vctl[2] = 0u;
+        }
+    }
 }
 
 // A vr_stats launch over `rows` rows: each row is cut into parts so that the
@@ -828,8 +1140,46 @@ cudaError_t launch_stats(RowsParams P, int pos, int npos, int sms, cudaStream_t 
     return cudaGetLastError();
 }
 
+// Whether vr_stream serves the call: stochastic, draft logits, aligned rows.
+bool use_stream(const RowsParams &P)
+{
+    if (const char *ev = std::getenv("SPECVERIFY_ROWS_STREAM"))
+        if (std::atoi(ev) == 0)
+            return false;
+    return !P.greedy && !P.sl && P.vec;
+}
+
+// The persistent statistics launch: VS_CPS CTAs per SM; parts per row so that
+// there are about two parts per CTA, each at least two stages long (the
+// epilogue's round trips per part make finer parts slower).
 template <class E>
-cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream)
+cudaError_t launch_stream(RowsParams P, int sms, cudaStream_t stream)
+{
+    static bool attr_set[kMaxDevicesRows] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    const int smem = VS_NS * VS_STAGE;
+    if (dev < kMaxDevicesRows && !attr_set[dev]) {
+        e = cudaFuncSetAttribute(vr_stream<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess)
+            return e;
+        attr_set[dev] = true;
+    }
+    const int ncta = sms * VS_CPS;
+    const long long rows = (long long)P.B * (2 * P.K + 1);
+    constexpr int STOK = VS_STAGE / E::ES;
+    int S = (int)std::min<long long>(VR_SMAX, (2LL * ncta + rows - 1) / rows);
+    S = std::max(1, std::min(S, P.V / (2 * STOK)));
+    P.span = ((P.V + S - 1) / S + 7) / 8 * 8;
+    P.parts = (P.V + P.span - 1) / P.span;
+    vr_stream<E><<<ncta, VS_T, smem, stream>>>(P);
+    return cudaGetLastError();
+}
+
+template <class E>
+cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream, int &launches)
 {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -837,18 +1187,30 @@ cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream)
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
         return e;
-    // positions 0 and 1 first, then the rest: the second launch sees every
-    // decision of the first (most of what skipping saves), at the cost of one
-    // launch boundary
-    const int first = std::min(2, P.K + 1);
-    e = launch_stats<E>(P, 0, first, sms, stream);
-    if (e == cudaSuccess && first <= P.K)
-        e = launch_stats<E>(P, first, P.K + 1 - first, sms, stream);
+    launches = 0;
+    if (use_stream(P)) {
+        e = launch_stream<E>(P, sms, stream);
+        launches += 1;
+    } else {
+        // positions 0 and 1 first, then the rest: the second launch sees every
+        // decision of the first (most of what skipping saves), at the cost of
+        // one launch boundary
+        const int first = std::min(2, P.K + 1);
+        e = launch_stats<E>(P, 0, first, sms, stream);
+        launches += 1;
+        if (e == cudaSuccess && first <= P.K) {
+            e = launch_stats<E>(P, first, P.K + 1 - first, sms, stream);
+            launches += 1;
+        }
+    }
     if (e != cudaSuccess)
         return e;
-    if (!P.greedy)
+    if (!P.greedy) {
         vr_residual<E><<<P.B * P.nch, VRT, 0, stream>>>(P);
+        launches += 1;
+    }
     vr_sample<E><<<P.B, VST, 0, stream>>>(P);
+    launches += 1;
     return cudaGetLastError();
 }
 
@@ -856,16 +1218,18 @@ cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream)
 
 int rows_chunks() { return VR_NCH; }
 int rows_segment_tokens() { return VSEG; }
-int rows_launches(int K, bool greedy) { return (K + 1 > 2 ? 2 : 1) + (greedy ? 1 : 2); }
-
-cudaError_t launch_rows(const RowsParams &P, int tdt, cudaStream_t stream)
+cudaError_t launch_rows(const RowsParams &P, int tdt, cudaStream_t stream, int *launches)
 {
+    int n = 0;
     if (P.aux_status) {
         cudaError_t e = cudaMemsetAsync(P.aux_status, 0, sizeof(int32_t), stream);
         if (e != cudaSuccess)
             return e;
     }
-    return tdt == 0 ? launch_rows_t<F32>(P, stream) : launch_rows_t<BF16>(P, stream);
+    const cudaError_t e = tdt == 0 ? launch_rows_t<F32>(P, stream, n) : launch_rows_t<BF16>(P, stream, n);
+    if (launches)
+        *launches = n;
+    return e;
 }
 
 }  // namespace sv

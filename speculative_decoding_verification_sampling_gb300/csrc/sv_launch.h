@@ -41,8 +41,8 @@ SweepEntry entry_sweep(int tdt);
 // per sequence chunk, then sampling per sequence (greedy: no residual kernel).
 int rows_chunks();
 int rows_segment_tokens();
-int rows_launches(int K, bool greedy);   // kernels one call launches
-cudaError_t launch_rows(const RowsParams &P, int tdt, cudaStream_t stream);
+// *launches: the kernels the call launched
+cudaError_t launch_rows(const RowsParams &P, int tdt, cudaStream_t stream, int *launches);
 
 // KV-cache commit after verification (k_kv.cu): copy, then the length update.
 cudaError_t launch_kv_commit(void *cache, const void *staged, int NL, int B, int K, int L, long long W,

@@ -246,11 +246,15 @@ struct RowsParams {
     int greedy, skip, vec;
     float c;
     uint32_t key0, key1;
+    // [0] parts claimed by vr_stream, [1] timeout (a bounded wait ran out),
+    // [2] vr_sample CTAs done; the last one zeroes the three
+    uint32_t *vctl;
+    uint32_t spin_limit;
 };
 
 struct WsLayout {
     size_t ctl, state, res_rec, pair_cnt, res_cnt, fin, errres, sw_ctl, sw_seq, sw_cnt, sw_res_ready, sw_res_done,
-        vr_pair, vr_rej, vr_rowcnt, errcode, terminal, gtok, dec, part, seg, sl_lb, sw_part, sw_stat, sw_res, sw_resm,
+        vr_pair, vr_rej, vr_rowcnt, vr_ctl, errcode, terminal, gtok, dec, part, seg, sl_lb, sw_part, sw_stat, sw_res, sw_resm,
         vr_stat, vr_errc, vr_part, vr_segm, vr_lb, total;
     size_t reset_end;   // [ctl, reset_end) holds what a call must find zeroed
     int npt_max, nseg;
@@ -283,6 +287,7 @@ inline WsLayout ws_layout(int B, int K, int V, int S)
     w.vr_pair = o;  o = align256(o + Bz * P * 4);
     w.vr_rej = o;   o = align256(o + Bz * 4);
     w.vr_rowcnt = o; o = align256(o + Bz * (2 * P - 1) * 4);
+    w.vr_ctl = o;   o = align256(o + 4 * 4);
     w.reset_end = o;
     w.errcode = o;  o = align256(o + Bz * P * 4);
     w.terminal = o; o = align256(o + Bz * 4);

@@ -27,19 +27,23 @@ def _device():
     sv.load()
 
 
-@pytest.fixture(scope="module", autouse=True, params=["auto", "cluster", "sweep", "rows", "general"])
+@pytest.fixture(scope="module", autouse=True, params=["auto", "cluster", "sweep", "rows", "rows-stats", "general"])
 def kernel(request):
     """Every case runs under the default dispatch and under each kernel forced
     in turn: the cluster kernel, the sweep kernel, the row-parallel kernels
-    and the chunk-scheduled kernel (each falls back to the next for shapes it
-    does not serve)."""
-    old = os.environ.get("SPECVERIFY_KERNEL")
-    os.environ["SPECVERIFY_KERNEL"] = request.param
+    (with the bulk-copy statistics stream, and with the per-position
+    statistics launches in its place: "rows-stats") and the chunk-scheduled
+    kernel (each falls back to the next for shapes it does not serve)."""
+    saved = {k: os.environ.get(k) for k in ("SPECVERIFY_KERNEL", "SPECVERIFY_ROWS_STREAM")}
+    os.environ["SPECVERIFY_KERNEL"] = "rows" if request.param == "rows-stats" else request.param
+    if request.param == "rows-stats":
+        os.environ["SPECVERIFY_ROWS_STREAM"] = "0"
     yield request.param
-    if old is None:
-        os.environ.pop("SPECVERIFY_KERNEL", None)
-    else:
-        os.environ["SPECVERIFY_KERNEL"] = old
+    for k, v in saved.items():
+        if v is None:
+            os.environ.pop(k, None)
+        else:
+            os.environ[k] = v
 
 
 def _to(cfg):
