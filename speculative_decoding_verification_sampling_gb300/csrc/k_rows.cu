@@ -106,6 +106,13 @@ __device__ __forceinline__ uint32_t vr_atom_add(uint32_t *p, uint32_t v)
     return old;
 }
 
+// Programmatic dependent launch: a kernel launched with it may start while
+// the one before it in the stream is finishing; pdl_wait() blocks until that
+// kernel has completed and its writes are visible (a no-op otherwise), and
+// pdl_trigger() lets the next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Decide position i of sequence b from the statistics of its target row t and
 // draft row d (the drafted token dt).  Returns 0 and sets accept, or a status
 // code.  Checks in the oracle's order: token, target row, draft row.
@@ -234,6 +241,8 @@ __device__ __noinline__ void vr_commit(const RowsParams &P, size_t ridx, int b, 
 template <class E, int VT, bool SL>
 __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParams P)
 {
+    pdl_wait();
+    pdl_trigger();
     constexpr int NW = VT / 32;
     __shared__ float sm_m[NW], sm_hi[NW], sm_lo[NW];
     __shared__ int sm_i[NW], sm_f[NW];
@@ -470,9 +479,73 @@ __device__ __forceinline__ void vs_row(const RowsParams &P, int r, int &i, int &
     }
 }
 
+// A consumer thread's share of a stage of ntok tokens (its units of 8 tokens:
+// g = tid, tid + CT, ...; float32 units are vectors g and g + CT of a group of
+// 2 CT vectors): the terms 2^(x c - mc) are summed against the running
+// reference mc and added to s in one step when the total is below 2^64 (no
+// new maximum, NaN or +inf among them); otherwise the units go through
+// acc_group one by one, which moves the reference and flags NaN / +inf.
+template <class E, int CT>
+__device__ __forceinline__ void vs_stage(const uint4 *p, int ntok, int tid, float c, float &mc, float &s, int &fl)
+{
+    const f2 cc = pk(c, c), nm = pk(-mc, -mc);
+    f2 a0 = pk(0.0f, 0.0f), a1 = pk(0.0f, 0.0f);
+    const uint4 ninf = make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+    if constexpr (E::ES == 2) {
+        const int nv = ntok >> 3;   // whole units: ntok is a multiple of 8
+#pragma unroll 4
+        for (int g = tid; g < nv; g += CT) {
+            const uint4 w = p[g];
+            a0 = add2(a0, ex2x2(fma2(E::pair(w, 0), cc, nm)));
+            a1 = add2(a1, ex2x2(fma2(E::pair(w, 1), cc, nm)));
+            a0 = add2(a0, ex2x2(fma2(E::pair(w, 2), cc, nm)));
+            a1 = add2(a1, ex2x2(fma2(E::pair(w, 3), cc, nm)));
+        }
+    } else {
+        const int nv = ntok >> 2;
+#pragma unroll 2
+        for (int g = tid; g < nv; g += 2 * CT) {
+            const uint4 w = p[g], w2 = g + CT < nv ? p[g + CT] : ninf;
+            a0 = add2(a0, ex2x2(fma2(E::pair(w, 0), cc, nm)));
+            a1 = add2(a1, ex2x2(fma2(E::pair(w, 1), cc, nm)));
+            a0 = add2(a0, ex2x2(fma2(E::pair(w2, 0), cc, nm)));
+            a1 = add2(a1, ex2x2(fma2(E::pair(w2, 1), cc, nm)));
+        }
+    }
+    float l0, h0, l1, h1;
+    upk(a0, l0, h0);
+    upk(a1, l1, h1);
+    const float t = (l0 + h0) + (l1 + h1);
+    if (t < 18446744073709551616.0f) {
+        s += t;
+        return;
+    }
+    if constexpr (E::ES == 2) {
+        const int nv = ntok >> 3;
+        for (int g = tid; g < nv; g += CT) {
+            Unit<E> u;
+            u.a = p[g];
+            f2 X[4];
+            unit_pairs<E>(u, X);
+            acc_group(X, c, mc, s, fl, VR_BAD);
+        }
+    } else {
+        const int nv = ntok >> 2;
+        for (int g = tid; g < nv; g += 2 * CT) {
+            Unit<E> u;
+            u.a = p[g];
+            u.b = g + CT < nv ? p[g + CT] : ninf;
+            f2 X[4];
+            unit_pairs<E>(u, X);
+            acc_group(X, c, mc, s, fl, VR_BAD);
+        }
+    }
+}
+
 template <class E>
 __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsParams P)
 {
+    pdl_trigger();
     extern __shared__ __align__(128) uint8_t vs_buf[];
     __shared__ unsigned long long full[VS_NS], empty[VS_NS], epf[VS_EPN], epe[VS_EPN], mg[VS_MB];
     __shared__ VsMeta meta[VS_NS];
@@ -593,28 +666,7 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
             break;
         const uint8_t *sb = vs_buf + st * VS_STAGE;
         const uint4 *p = reinterpret_cast<const uint4 *>(sb);
-        if constexpr (E::ES == 2) {
-            const int nv = mt.ntok >> 3;   // whole units: ntok is a multiple of 8
-#pragma unroll 4
-            for (int g = tid; g < nv; g += CT) {
-                Unit<E> u;
-                u.a = p[g];
-                f2 X[4];
-                unit_pairs<E>(u, X);
-                acc_group(X, c, mc, s, fl, VR_BAD);
-            }
-        } else {
-            const int nv = mt.ntok >> 2;   // 16-byte vectors of 4 tokens; a unit is vectors g and g + CT
-#pragma unroll 2
-            for (int g = tid; g < nv; g += 2 * CT) {
-                Unit<E> u;
-                u.a = p[g];
-                u.b = g + CT < nv ? p[g + CT] : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
-                f2 X[4];
-                unit_pairs<E>(u, X);
-                acc_group(X, c, mc, s, fl, VR_BAD);
-            }
-        }
+        vs_stage<E, CT>(p, mt.ntok, tid, c, mc, s, fl);
         if (tid == 0 && (unsigned)(mt.dt - mt.tok0) < (unsigned)mt.ntok) {
             const int o = mt.dt - mt.tok0;
             zd = E::ES == 2 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(sb)[o] << 16)
@@ -802,6 +854,8 @@ __device__ __forceinline__ void sl_pairs(const RowsParams &P, int b, int j, int 
 template <class E>
 __global__ void __launch_bounds__(VRT) vr_residual(const __grid_constant__ RowsParams P)
 {
+    pdl_wait();
+    pdl_trigger();
     constexpr int NW = VRT / 32;
     constexpr int UPS = VSEG / 8;   // units per segment (one per lane)
     __shared__ int sm_j, sm_code;
@@ -883,6 +937,7 @@ __device__ __forceinline__ void vr_emit(const RowsParams &P, int b, int j, int x
 template <class E>
 __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsParams P)
 {
+    pdl_wait();
     constexpr int NW = VST / 32;
     __shared__ int sm_j, sm_code, sm_seg, sm_last[NW];
     __shared__ float sl_buf0[VSEG];
@@ -1115,6 +1170,24 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
     }
 }
 
+// Launch kern(P) so that it may begin while the previous kernel in the
+// stream finishes (it waits for that kernel's results with pdl_wait).
+template <class Kern>
+cudaError_t launch_after(Kern kern, int grid, int block, int smem, cudaStream_t stream, const RowsParams &P)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
 // A vr_stats launch over `rows` rows: each row is cut into parts so that the
 // launch brings about as many threads as the GPU holds (the bytes in flight
 // grow with them), with parts of at least 4096 tokens.
@@ -1133,11 +1206,12 @@ cudaError_t launch_stats(RowsParams P, int pos, int npos, int sms, cudaStream_t 
     P.npos = npos;
     P.span = ((P.V + S - 1) / S + 7) / 8 * 8;
     P.parts = (P.V + P.span - 1) / P.span;
+    // the first launch of a call waits for whatever came before it in full
     if (P.sl)
-        vr_stats<E, VST_T, true><<<rows * P.parts, VST_T, 0, stream>>>(P);
-    else
-        vr_stats<E, VST_T, false><<<rows * P.parts, VST_T, 0, stream>>>(P);
-    return cudaGetLastError();
+        return pos == 0 ? (vr_stats<E, VST_T, true><<<rows * P.parts, VST_T, 0, stream>>>(P), cudaGetLastError())
+                        : launch_after(vr_stats<E, VST_T, true>, rows * P.parts, VST_T, 0, stream, P);
+    return pos == 0 ? (vr_stats<E, VST_T, false><<<rows * P.parts, VST_T, 0, stream>>>(P), cudaGetLastError())
+                    : launch_after(vr_stats<E, VST_T, false>, rows * P.parts, VST_T, 0, stream, P);
 }
 
 // Whether vr_stream serves the call: stochastic, draft logits, aligned rows.
@@ -1172,6 +1246,8 @@ cudaError_t launch_stream(RowsParams P, int sms, cudaStream_t stream)
     constexpr int STOK = VS_STAGE / E::ES;
     int S = (int)std::min<long long>(VR_SMAX, (2LL * ncta + rows - 1) / rows);
     S = std::max(1, std::min(S, P.V / (2 * STOK)));
+    if (const char *ev = std::getenv("SPECVERIFY_ROWS_PARTS"))
+        S = std::max(1, std::min(VR_SMAX, std::atoi(ev)));
     P.span = ((P.V + S - 1) / S + 7) / 8 * 8;
     P.parts = (P.V + P.span - 1) / P.span;
     vr_stream<E><<<ncta, VS_T, smem, stream>>>(P);
@@ -1206,12 +1282,14 @@ cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream, int &launches)
     if (e != cudaSuccess)
         return e;
     if (!P.greedy) {
-        vr_residual<E><<<P.B * P.nch, VRT, 0, stream>>>(P);
+        e = launch_after(vr_residual<E>, P.B * P.nch, VRT, 0, stream, P);
         launches += 1;
+        if (e != cudaSuccess)
+            return e;
     }
-    vr_sample<E><<<P.B, VST, 0, stream>>>(P);
+    e = launch_after(vr_sample<E>, P.B, VST, 0, stream, P);
     launches += 1;
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace

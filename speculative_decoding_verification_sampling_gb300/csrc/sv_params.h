@@ -247,7 +247,7 @@ struct RowsParams {
     float c;
     uint32_t key0, key1;
     // [0] parts claimed by vr_stream, [1] timeout (a bounded wait ran out),
-    // [2] vr_sample CTAs done; the last one zeroes the three
+    // [2] vr_sample CTAs done (the last one zeroes the three)
     uint32_t *vctl;
     uint32_t spin_limit;
 };
