@@ -649,8 +649,8 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
     // ---- consumers (threads 0 .. 32 VS_NCW - 1)
     constexpr int CT = VS_NCW * 32;
     const float c = P.c;
-    int st = 0, es = 0, nit = 0;
-    uint32_t ph = 0, eph = 0;
+    int st = 0, nit = 0;
+    uint32_t ph = 0;
     float mc = -F_INF, s = 0.0f, zd = 0.0f;
     int fl = 0;
     bool ok = true;
@@ -683,9 +683,10 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
         if (mt.last) {
             // the part's statistics: each warp posts its partial (buffer nit mod
             // VS_MB, whose mbarrier completes once all consumer warps posted);
-            // warp 0 merges them and hands the result to the epilogue.  No warp
-            // runs more than VS_NS stages, so VS_NS parts, ahead of warp 0: the
-            // buffers never overlap.
+            // warp nit mod VS_NCW merges them and hands the result to the
+            // epilogue (slot nit mod VS_EPN), so the merges are spread over the
+            // warps.  No warp runs more than VS_NS stages, so VS_NS parts,
+            // ahead of another: the buffers never overlap.
             const int h = nit & (VS_MB - 1);
             const int wf = warp_or(fl);
             float M;
@@ -700,7 +701,7 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
                     rzd[h] = zd;   // thread 0 alone ever holds the drafted token
                 mbar_arrive(&mg[h]);
             }
-            if (warp == 0) {
+            if (warp == nit % VS_NCW) {
                 bool got = true;
                 if (lane == 0)
                     got = vs_wait(&mg[h], (uint32_t)(nit / VS_MB) & 1u, lim, tflag);
@@ -716,14 +717,11 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
                     r.m = M;
                     r.s_hi = S.hi;
                     r.s_lo = S.lo;
-                    if (lane == 0 && vs_wait(&epe[es], eph ^ 1u, lim, tflag)) {
+                    const int es = nit % VS_EPN;
+                    if (lane == 0 && vs_wait(&epe[es], ((uint32_t)(nit / VS_EPN) & 1u) ^ 1u, lim, tflag)) {
                         ep[es] = VsEp{r, mt.item, mt.dt, 0, 0};
                         mbar_arrive(&epf[es]);
                     }
-                }
-                if (++es == VS_EPN) {
-                    es = 0;
-                    eph ^= 1u;
                 }
                 __syncwarp();
             }
@@ -734,31 +732,30 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
             ++nit;
         }
     }
-    if (tid == 0 && vs_wait(&epe[es], eph ^ 1u, lim, tflag)) {
-        ep[es].item = -1;
-        mbar_arrive(&epf[es]);
+    if (tid == 0 && vs_wait(&epe[nit % VS_EPN], ((uint32_t)(nit / VS_EPN) & 1u) ^ 1u, lim, tflag)) {
+        ep[nit % VS_EPN].item = -1;
+        mbar_arrive(&epf[nit % VS_EPN]);
     }
 }
 
 // ---------------------------------------------------------------- 2. residual masses
-// q'(x) = 2^(xt c - Mt) and r'(x) = q'(x) (1 - 2^delta)_+ for 8 tokens, delta =
-// (xd - xt) c - dL (both scaled by the target's normaliser, which cancels in
-// the inverse CDF).  1 - 2^delta on [-1, 0) is -2 * 2^(delta/2) * sinh(delta
-// ln2 / 2) with sinh as its odd Taylor series to y^9, so nothing cancels as
-// q -> p; below -1 it is 1 - 2^delta.  With qonly (the bonus row) r' = q'.
-__device__ __forceinline__ void vr_res8(const f2 *XT, const f2 *XD, const ResK &k, bool qonly, float *r, float *q)
+// q'(x) = 2^(xt c - Mt) and r'(x) = q'(x) (1 - 2^delta)_+ for 8 tokens as four
+// float pairs, delta = (xd - xt) c - dL (both scaled by the target's
+// normaliser, which cancels in the inverse CDF).  1 - 2^delta on [-1, 0) is
+// 2^(delta/2) * (-2 sinh(delta ln2 / 2)) with sinh as its odd Taylor series to
+// y^9 (the factor -2 folded into its coefficients, an exact scaling), so
+// nothing cancels as q -> p; below -1 it is 1 - 2^delta.  With qonly (the
+// bonus row) r' = q'.
+__device__ __forceinline__ void vr_res8(const f2 *XT, const f2 *XD, const ResK &k, bool qonly, f2 *R, f2 *Q)
 {
     const f2 cc = pk(k.c, k.c), nMt = pk(-k.Mt, -k.Mt);
-    f2 Q[4];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
+    for (int p = 0; p < 4; ++p)
         Q[p] = ex2x2(fma2(XT[p], cc, nMt));
-        upk(Q[p], q[2 * p], q[2 * p + 1]);
-    }
     if (qonly) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            r[e] = q[e];
+        for (int p = 0; p < 4; ++p)
+            R[p] = Q[p];
         return;
     }
     const f2 ndh = pk(-k.dLhi, -k.dLhi), ndl = pk(-k.dLlo, -k.dLlo);
@@ -775,25 +772,68 @@ __device__ __forceinline__ void vr_res8(const f2 *XT, const f2 *XD, const ResK &
         upk(ex2x2(pk(far0 ? d0 : 0.5f * d0, far1 ? d1 : 0.5f * d1)), e0, e1);
         const f2 y = mul2(pk(d0, d1), hl);
         const f2 y2 = mul2(y, y);
-        f2 sp = pk(1.0f / 362880.0f, 1.0f / 362880.0f);
-        sp = fma2(sp, y2, pk(1.0f / 5040.0f, 1.0f / 5040.0f));
-        sp = fma2(sp, y2, pk(1.0f / 120.0f, 1.0f / 120.0f));
-        sp = fma2(sp, y2, pk(1.0f / 6.0f, 1.0f / 6.0f));
-        sp = fma2(sp, y2, pk(1.0f, 1.0f));
+        f2 sp = pk(-2.0f / 362880.0f, -2.0f / 362880.0f);
+        sp = fma2(sp, y2, pk(-2.0f / 5040.0f, -2.0f / 5040.0f));
+        sp = fma2(sp, y2, pk(-2.0f / 120.0f, -2.0f / 120.0f));
+        sp = fma2(sp, y2, pk(-2.0f / 6.0f, -2.0f / 6.0f));
+        sp = fma2(sp, y2, pk(-2.0f, -2.0f));
         float s0, s1;
-        upk(mul2(y, sp), s0, s1);                                     // sinh(delta ln2 / 2)
-        const float o0 = far0 ? 1.0f - e0 : -2.0f * e0 * s0;
-        const float o1 = far1 ? 1.0f - e1 : -2.0f * e1 * s1;
-        upk(mul2(Q[p], pk(o0, o1)), r[2 * p], r[2 * p + 1]);
+        upk(mul2(y, sp), s0, s1);                                     // -2 sinh(delta ln2 / 2)
+        // far: 1 - e; near: e * (-2 sinh)
+        const float o0 = fmaf(far0 ? -1.0f : s0, e0, far0 ? 1.0f : 0.0f);
+        const float o1 = fmaf(far1 ? -1.0f : s1, e1, far1 ? 1.0f : 0.0f);
+        R[p] = mul2(Q[p], pk(o0, o1));
     }
 }
-// Lane sums of one unit, in a fixed order (the locate pass repeats it).
-__device__ __forceinline__ float sum8f(const float *v)
+// The sum of a unit's 8 values held as four pairs, in a fixed order (the
+// locate pass repeats it).
+__device__ __forceinline__ float sum4p(const f2 *V)
 {
-    return ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+    float lo, hi;
+    upk(add2(add2(V[0], V[1]), add2(V[2], V[3])), lo, hi);
+    return lo + hi;
+}
+// Sum each of 8 values over the 32 lanes (a transposed butterfly: 9 shuffles
+// in place of 40); lane 4 v ends with the total of value v.
+__device__ __forceinline__ float xpose8(const float *v, int lane)
+{
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float a[4], c[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        a[i] = (b4 ? v[4 + i] : v[i]) + __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[4 + i], 16);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        c[i] = (b3 ? a[2 + i] : a[i]) + __shfl_xor_sync(0xffffffffu, b3 ? a[i] : a[2 + i], 8);
+    float d = (b2 ? c[1] : c[0]) + __shfl_xor_sync(0xffffffffu, b2 ? c[0] : c[1], 4);
+    d += __shfl_xor_sync(0xffffffffu, d, 2);
+    d += __shfl_xor_sync(0xffffffffu, d, 1);
+    return d;
 }
 
-// The coefficients of the distribution sequence b samples at its end j.
+// The coefficients of the distribution sequence b samples at its end j, from
+// the statistics t of its target row j and d of its draft row j (j < K).
+__device__ __forceinline__ ResK res_coef(const RowsParams &P, const VrStat &t, const VrStat &d, int j)
+{
+    ResK k;
+    k.Mt = t.m;
+    k.c = P.c;
+    k.dLhi = k.dLlo = 0.0f;
+    if (j < P.K) {
+        // dL = (Md - Mt) + log2 Sd - log2 St as a float pair
+        int et, ed;
+        float ft, fd;
+        log2_split(DF{t.s_hi, t.s_lo}, et, ft);
+        log2_split(DF{d.s_hi, d.s_lo}, ed, fd);
+        DF dl = two_sum(d.m, -t.m);
+        dl = df_add(dl, DF{(float)(ed - et), 0.0f});
+        dl = df_add(dl, DF{fd - ft, 0.0f});
+        k.dLhi = dl.hi;
+        k.dLlo = dl.lo;
+    }
+    return k;
+}
+// The same, loading the statistics (the draft row's only where it is used).
 __device__ __forceinline__ ResK vr_coef(const RowsParams &P, int b, int j)
 {
     const VrStat *st = P.stat + (size_t)b * (2 * P.K + 1);
@@ -803,7 +843,6 @@ __device__ __forceinline__ ResK vr_coef(const RowsParams &P, int b, int j)
     k.c = P.c;
     k.dLhi = k.dLlo = 0.0f;
     if (j < P.K) {
-        // dL = (Md - Mt) + log2 Sd - log2 St as a float pair
         const VrStat d = ld_vrstat(st + P.K + 1 + j);
         int et, ed;
         float ft, fd;
@@ -852,7 +891,7 @@ __device__ __forceinline__ void sl_pairs(const RowsParams &P, int b, int j, int 
 }
 
 template <class E>
-__global__ void __launch_bounds__(VRT) vr_residual(const __grid_constant__ RowsParams P)
+__global__ void __launch_bounds__(VRT, E::ES == 2 ? 3 : 1) vr_residual(const __grid_constant__ RowsParams P)
 {
     pdl_wait();
     pdl_trigger();
@@ -895,9 +934,12 @@ __global__ void __launch_bounds__(VRT) vr_residual(const __grid_constant__ RowsP
                 ud[q] = fetch_unit<E>(drow, unit_x0(q), V, P.vec);
         }
     for (int t0 = 0; t0 < nsteps; t0 += 4) {
+        // the (r', q') sums of four steps' units, reduced over the lanes at once
+        float v[8];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int t = t0 + q;
+            v[2 * q] = v[2 * q + 1] = 0.0f;
             if (t < nsteps) {
                 f2 XT[4], XD[4];
                 unit_pairs<E>(ut[q], XT);
@@ -910,51 +952,49 @@ __global__ void __launch_bounds__(VRT) vr_residual(const __grid_constant__ RowsP
                     if (!qonly && !slist)
                         ud[q] = fetch_unit<E>(drow, unit_x0(t + 4), V, P.vec);
                 }
-                float r[8], qv[8];
-                vr_res8(XT, XD, k, qonly, r, qv);
-                const float rs = warp_sumf(sum8f(r)), qs = warp_sumf(sum8f(qv));
-                const int seg = s_lo + t * NW + warp;
-                if (lane == 0 && seg < s_hi)
-                    out[seg] = VrSeg{rs, qs};
+                f2 R[4], Q[4];
+                vr_res8(XT, XD, k, qonly, R, Q);
+                v[2 * q] = sum4p(R);
+                v[2 * q + 1] = sum4p(Q);
             }
         }
+        const float tot = xpose8(v, lane);
+        const int vi = lane >> 2;
+        const int seg = s_lo + (t0 + (vi >> 1)) * NW + warp;
+        if ((lane & 3) == 0 && t0 + (vi >> 1) < nsteps && seg < s_hi)
+            reinterpret_cast<float *>(out + seg)[vi & 1] = tot;
     }
 }
 
 // ---------------------------------------------------------------- 3. sampling and outputs
-// Accepted drafts 0..j-1, then x at j, -1 after.
-__device__ __forceinline__ void vr_emit(const RowsParams &P, int b, int j, int x)
-{
-    int32_t *o = P.out_tokens + (size_t)b * (P.K + 1);
-    for (int i = 0; i < j; ++i)
-        o[i] = __ldg(P.tokens + (size_t)b * P.K + i);
-    o[j] = x;
-    for (int i = j + 1; i <= P.K; ++i)
-        o[i] = -1;
-    P.out_len[b] = j;
-}
 
 template <class E>
 __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsParams P)
 {
     pdl_wait();
     constexpr int NW = VST / 32;
-    __shared__ int sm_j, sm_code, sm_seg, sm_last[NW];
+    __shared__ int sm_seg, sm_last[NW], sm_x, sm_e[32];
+    __shared__ uint32_t sm_m, sm_tf;
     __shared__ float sl_buf0[VSEG];
     __shared__ DF sm_r[NW], sm_q[NW], sm_before;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int b = blockIdx.x;
     const int K = P.K, V = P.V;
+    // where the sequence ended, in one round trip: the mask, every position's
+    // status and the timeout word together (vr_end's reading of them)
+    if (tid <= K)
+        sm_e[tid] = __ldcg(P.errc + (size_t)b * (K + 1) + tid);
     if (tid == 0) {
-        int j = 0;
-        sm_code = vr_end(P, b, j);
-        if (__ldcg(P.vctl + 1))
-            sm_code = ST_TIMEOUT;   // the statistics stream gave up a wait
-        sm_j = j;
+        sm_m = __ldcg(P.rej + b);
+        sm_tf = __ldcg(P.vctl + 1);
     }
     __syncthreads();
-    const int j = sm_j, code = sm_code;
+    const uint32_t msk = sm_m;
+    const int j = msk ? __ffs(msk) - 1 : K;
+    const int code = sm_tf ? (int)ST_TIMEOUT : ((msk >> j) & 1u ? sm_e[j] : 0);   // timeout: the stream gave up a wait
     const VrStat *st = P.stat + (size_t)b * (2 * K + 1);
+    // the accepted drafts, emitted in parallel at the end
+    const int tokv = tid < j ? __ldg(P.tokens + (size_t)b * K + tid) : -1;
 
     // per-position outputs (every row was computed when they are asked for)
     if (P.aux_q || P.aux_p || P.aux_lse) {
@@ -986,11 +1026,12 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
                 P.aux_p[(size_t)b * K + i] = ok ? ex2a(fmaf(d.zd, P.c, -ld)) : nan;
         }
     }
+    if (tid == 0)
+        sm_x = -1;
     if (code) {
+        if (tid <= K)
+            P.out_tokens[(size_t)b * (K + 1) + tid] = -1;
         if (tid == 0) {
-            int32_t *o = P.out_tokens + (size_t)b * (K + 1);
-            for (int i = 0; i <= K; ++i)
-                o[i] = -1;
             P.out_len[b] = -code;
             if (P.aux_R)
                 P.aux_R[b] = __int_as_float(0x7fc00000);
@@ -999,21 +1040,44 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
         }
     } else if (P.greedy) {
         if (tid == 0) {
-            vr_emit(P, b, j, __float_as_int(ld_vrstat(st + j).s_hi));
+            sm_x = __float_as_int(ld_vrstat(st + j).s_hi);
             if (P.aux_R)
                 P.aux_R[b] = __int_as_float(0x7fc00000);
         }
     } else {
+        // the statistics of row pair j, loaded now for the coefficients used at the end
+        VrStat tS{}, dS{};
+        if (warp == 0) {
+            tS = ld_vrstat(st + j);
+            if (j < K)
+                dS = ld_vrstat(st + K + 1 + j);
+        }
         // totals of the residual and target masses of row pair j
         const int nseg = P.nseg;
         const VrSeg *sg = P.segm + (size_t)b * nseg;
         const int per = (nseg + VST - 1) / VST;
         const int s0 = min(nseg, tid * per), s1 = min(nseg, s0 + per);
+        // a thread's segments stay in registers when there are at most PC of them
+        constexpr int PC = 8;
+        const bool cached = per <= PC;
+        float2 cg[PC];
         DF ownr{0.0f, 0.0f}, ownq{0.0f, 0.0f};
-        for (int s = s0; s < s1; ++s) {
-            const float2 g = __ldcg(reinterpret_cast<const float2 *>(sg + s));
-            ownr = df_add(ownr, DF{g.x, 0.0f});
-            ownq = df_add(ownq, DF{g.y, 0.0f});
+        if (cached) {
+#pragma unroll
+            for (int k = 0; k < PC; ++k)
+                cg[k] = s0 + k < s1 ? __ldcg(reinterpret_cast<const float2 *>(sg + s0 + k)) : make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int k = 0; k < PC; ++k)
+                if (s0 + k < s1) {
+                    ownr = df_add(ownr, DF{cg[k].x, 0.0f});
+                    ownq = df_add(ownq, DF{cg[k].y, 0.0f});
+                }
+        } else {
+            for (int s = s0; s < s1; ++s) {
+                const float2 g = __ldcg(reinterpret_cast<const float2 *>(sg + s));
+                ownr = df_add(ownr, DF{g.x, 0.0f});
+                ownq = df_add(ownq, DF{g.y, 0.0f});
+            }
         }
         const DF ir = warp_incl_scan_df(ownr, lane), iq = warp_incl_scan_df(ownq, lane);
         if (lane == 31) {
@@ -1047,16 +1111,31 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
         const DF thr = df_add(DF{th, fmaf(v, F.hi, -th)}, DF{v * F.lo, 0.0f});
         if (df_gt(incl, thr) && !df_gt(excl, thr)) {
             DF G = excl;
-            for (int s = s0; s < s1; ++s) {
-                const float2 g = __ldcg(reinterpret_cast<const float2 *>(sg + s));
-                const float m = useq ? g.y : g.x;
-                const DF nG = df_add(G, DF{m, 0.0f});
-                if (df_gt(nG, thr) && m > 0.0f) {
-                    sm_seg = s;
-                    sm_before = G;
-                    break;
+            if (cached) {
+                bool found = false;
+#pragma unroll
+                for (int k = 0; k < PC; ++k) {
+                    const float m = useq ? cg[k].y : cg[k].x;
+                    const DF nG = df_add(G, DF{m, 0.0f});
+                    if (!found && s0 + k < s1 && df_gt(nG, thr) && m > 0.0f) {
+                        sm_seg = s0 + k;
+                        sm_before = G;
+                        found = true;
+                    }
+                    G = nG;
                 }
-                G = nG;
+            } else {
+                for (int s = s0; s < s1; ++s) {
+                    const float2 g = __ldcg(reinterpret_cast<const float2 *>(sg + s));
+                    const float m = useq ? g.y : g.x;
+                    const DF nG = df_add(G, DF{m, 0.0f});
+                    if (df_gt(nG, thr) && m > 0.0f) {
+                        sm_seg = s;
+                        sm_before = G;
+                        break;
+                    }
+                    G = nG;
+                }
             }
         }
         __syncthreads();
@@ -1084,7 +1163,7 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
             }
             int x = -1;
             if (seg >= 0) {
-                const ResK k = vr_coef(P, b, j);
+                const ResK k = res_coef(P, tS, dS, j);
                 const bool qonly = j == K || useq;
                 const bool slist = P.sl && !qonly;
                 const uint8_t *trow =
@@ -1101,9 +1180,13 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
                     sl_pairs<E>(P, b, j, seg, lane, sl_buf0, XD);
                 else if (!qonly)
                     unit_pairs<E>(ud, XD);
-                float r[8], q[8];
-                vr_res8(XT, XD, k, qonly, r, q);
-                const float ls = sum8f(r);
+                f2 R[4], Q[4];
+                vr_res8(XT, XD, k, qonly, R, Q);
+                float r[8];
+#pragma unroll
+                for (int p = 0; p < 4; ++p)
+                    upk(R[p], r[2 * p], r[2 * p + 1]);
+                const float ls = sum4p(R);
                 if (!fb) {
                     const DF rel = df_add(thr, DF{-sm_before.hi, -sm_before.lo});
                     const float t = rel.hi + rel.lo;
@@ -1143,18 +1226,24 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
                 }
             }
             if (lane == 0) {
-                vr_emit(P, b, j, x);
+                sm_x = x;
                 if (P.aux_R) {
                     // R of the distribution drawn from (for q_j itself: the residual's, about 0)
-                    const VrStat t = ld_vrstat(st + j);
                     const DF Rr = useq ? tr : F;
-                    P.aux_R[b] = (Rr.hi + Rr.lo) / (t.s_hi + t.s_lo);
+                    P.aux_R[b] = (Rr.hi + Rr.lo) / (tS.s_hi + tS.s_lo);
                 }
             }
         }
     }
-    // the sequence's control words, for the next call
     __syncthreads();
+    if (!code) {
+        // accepted drafts 0..j-1, then x at j, -1 after
+        if (tid <= K)
+            P.out_tokens[(size_t)b * (K + 1) + tid] = tid < j ? tokv : (tid == j ? sm_x : -1);
+        if (tid == 0)
+            P.out_len[b] = j;
+    }
+    // the sequence's control words, for the next call
     for (int i = tid; i <= K; i += VST)
         P.pair[(size_t)b * (K + 1) + i] = 0u;
     for (int i = tid; i < 2 * K + 1; i += VST)
