@@ -293,6 +293,8 @@ spec_status_t run_rows(bool greedy, const void *target, spec_dtype_t tdt, const 
     P.vpart = reinterpret_cast<sv::VrStat *>(w + L.vr_part);
     P.segm = reinterpret_cast<sv::VrSeg *>(w + L.vr_segm);
     P.vctl = reinterpret_cast<uint32_t *>(w + L.vr_ctl);
+    P.dw = reinterpret_cast<unsigned long long *>(w + L.vr_dw);
+    P.jobs = reinterpret_cast<sv::VrJob *>(w + L.vr_jobs);
     P.spin_limit = spin_limit();
     P.B = B;
     P.K = K;

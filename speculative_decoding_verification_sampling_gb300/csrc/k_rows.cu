@@ -168,6 +168,42 @@ __device__ __forceinline__ int vr_end(const RowsParams &P, int b, int &j)
     return (m >> j) & 1u ? __ldcg(P.errc + (size_t)b * (P.K + 1) + j) : 0;
 }
 
+__device__ __forceinline__ unsigned long long vr_atom_or64(unsigned long long *p, unsigned long long v)
+{
+    unsigned long long old;
+    asm volatile("atom.acq_rel.gpu.global.or.b64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v) : "memory");
+    return old;
+}
+__device__ __forceinline__ uint32_t ld_acq(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ int ld_acq_s32(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_rel_s32(int *p, int v)
+{
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Whether a sequence's word (decided positions low, ending positions high)
+// says it has ended: the first ending position j and every position up to it
+// decided.
+__device__ __forceinline__ bool vr_ended(unsigned long long w)
+{
+    const uint32_t E = (uint32_t)(w >> 32), D = (uint32_t)w;
+    if (!E)
+        return false;
+    const int j = __ffs(E) - 1;
+    const uint32_t need = j == 31 ? 0xffffffffu : (2u << j) - 1u;
+    return (D & need) == need;
+}
+__device__ __noinline__ void vr_post_end(const RowsParams &P, int b, unsigned long long w);
+
 // A part's statistics st of row ridx (sequence b, position i; kind 1: the
 // draft row), from one CTA: the last part of the row to finish merges the
 // parts in part order and writes the row's statistics; the second row of a
@@ -231,9 +267,18 @@ __device__ __noinline__ void vr_commit(const RowsParams &P, size_t ridx, int b, 
     }
     bool acc = false;
     const int code = vr_decide(P, b, i, dt, t, d, acc);
-    if (code || (!acc && i < K)) {
+    const bool ends = code || (!acc && i < K);
+    if (ends) {
         P.errc[(size_t)b * (K + 1) + i] = code;
         atomicOr(P.rej + b, 1u << i);
+    }
+    if (P.fused) {
+        // position i decided (and ending the sequence, at K always): the update
+        // completing the sequence's end posts its residual job
+        const unsigned long long bits = (1ull << i) | ((ends || i == K) ? (1ull << (32 + i)) : 0ull);
+        const unsigned long long old = vr_atom_or64(P.dw + b, bits);
+        if (!vr_ended(old) && vr_ended(old | bits))
+            vr_post_end(P, b, old | bits);
     }
 }
 
@@ -412,6 +457,109 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
         vr_commit(P, ridx, b, i, kind, part, dt, st, slrow);
 }
 
+// ---------------------------------------------------------------- residual arithmetic
+// q'(x) = 2^(xt c - Mt) and r'(x) = q'(x) (1 - 2^delta)_+ for 8 tokens as four
+// float pairs, delta = (xd - xt) c - dL (both scaled by the target's
+// normaliser, which cancels in the inverse CDF).  1 - 2^delta on [-1, 0) is
+// 2^(delta/2) * (-2 sinh(delta ln2 / 2)) with sinh as its odd Taylor series to
+// y^9 (the factor -2 folded into its coefficients, an exact scaling), so
+// nothing cancels as q -> p; below -1 it is 1 - 2^delta.  With qonly (the
+// bonus row) r' = q'.
+__device__ __forceinline__ void vr_res8(const f2 *XT, const f2 *XD, const ResK &k, bool qonly, f2 *R, f2 *Q)
+{
+    const f2 cc = pk(k.c, k.c), nMt = pk(-k.Mt, -k.Mt);
+#pragma unroll
+    for (int p = 0; p < 4; ++p)
+        Q[p] = ex2x2(fma2(XT[p], cc, nMt));
+    if (qonly) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+            R[p] = Q[p];
+        return;
+    }
+    const f2 ndh = pk(-k.dLhi, -k.dLhi), ndl = pk(-k.dLlo, -k.dLlo);
+    const f2 hl = pk(0.34657359027997264f, 0.34657359027997264f);   // ln2 / 2
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const f2 dd = fma2(XT[p], pk(-1.0f, -1.0f), XD[p]);           // xd - xt
+        float d0, d1;
+        upk(add2(fma2(dd, cc, ndh), ndl), d0, d1);                    // delta
+        d0 = fminf(d0, 0.0f);                                         // also maps NaN (both -inf) to 0
+        d1 = fminf(d1, 0.0f);
+        const bool far0 = d0 < -1.0f, far1 = d1 < -1.0f;
+        float e0, e1;
+        upk(ex2x2(pk(far0 ? d0 : 0.5f * d0, far1 ? d1 : 0.5f * d1)), e0, e1);
+        const f2 y = mul2(pk(d0, d1), hl);
+        const f2 y2 = mul2(y, y);
+        f2 sp = pk(-2.0f / 362880.0f, -2.0f / 362880.0f);
+        sp = fma2(sp, y2, pk(-2.0f / 5040.0f, -2.0f / 5040.0f));
+        sp = fma2(sp, y2, pk(-2.0f / 120.0f, -2.0f / 120.0f));
+        sp = fma2(sp, y2, pk(-2.0f / 6.0f, -2.0f / 6.0f));
+        sp = fma2(sp, y2, pk(-2.0f, -2.0f));
+        float s0, s1;
+        upk(mul2(y, sp), s0, s1);                                     // -2 sinh(delta ln2 / 2)
+        // far: 1 - e; near: e * (-2 sinh)
+        const float o0 = fmaf(far0 ? -1.0f : s0, e0, far0 ? 1.0f : 0.0f);
+        const float o1 = fmaf(far1 ? -1.0f : s1, e1, far1 ? 1.0f : 0.0f);
+        R[p] = mul2(Q[p], pk(o0, o1));
+    }
+}
+// The sum of a unit's 8 values held as four pairs, in a fixed order (the
+// locate pass repeats it).
+__device__ __forceinline__ float sum4p(const f2 *V)
+{
+    float lo, hi;
+    upk(add2(add2(V[0], V[1]), add2(V[2], V[3])), lo, hi);
+    return lo + hi;
+}
+// Sum each of 8 values over the 32 lanes (a transposed butterfly: 9 shuffles
+// in place of 40); lane 4 v ends with the total of value v.
+__device__ __forceinline__ float xpose8(const float *v, int lane)
+{
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float a[4], c[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        a[i] = (b4 ? v[4 + i] : v[i]) + __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[4 + i], 16);
+#pragma unroll
+    for (int i = 0; i < 2; ++i)
+        c[i] = (b3 ? a[2 + i] : a[i]) + __shfl_xor_sync(0xffffffffu, b3 ? a[i] : a[2 + i], 8);
+    float d = (b2 ? c[1] : c[0]) + __shfl_xor_sync(0xffffffffu, b2 ? c[0] : c[1], 4);
+    d += __shfl_xor_sync(0xffffffffu, d, 2);
+    d += __shfl_xor_sync(0xffffffffu, d, 1);
+    return d;
+}
+
+// Sum each of NV (2 or 4) values over the 32 lanes, transposed: lane
+// l * 32 / NV ends with the total of value l.
+template <int NV>
+__device__ __forceinline__ float xpose_sum(const float *v, int lane)
+{
+    static_assert(NV == 2 || NV == 4, "two or four values");
+    float a;
+    if constexpr (NV == 4) {
+        const bool h4 = lane & 16;
+        float a0 = h4 ? v[2] : v[0], a1 = h4 ? v[3] : v[1];
+        const float s0 = h4 ? v[0] : v[2], s1 = h4 ? v[1] : v[3];
+        a0 += __shfl_xor_sync(0xffffffffu, s0, 16);
+        a1 += __shfl_xor_sync(0xffffffffu, s1, 16);
+        const bool h3 = lane & 8;
+        a = h3 ? a1 : a0;
+        a += __shfl_xor_sync(0xffffffffu, h3 ? a0 : a1, 8);
+#pragma unroll
+        for (int o = 4; o; o >>= 1)
+            a += __shfl_xor_sync(0xffffffffu, a, o);
+    } else {
+        const bool h4 = lane & 16;
+        a = h4 ? v[1] : v[0];
+        a += __shfl_xor_sync(0xffffffffu, h4 ? v[0] : v[1], 16);
+#pragma unroll
+        for (int o = 8; o; o >>= 1)
+            a += __shfl_xor_sync(0xffffffffu, a, o);
+    }
+    return a;
+}
+
 // ---------------------------------------------------------------- 1b. row statistics from a bulk-copy stream
 // The statistics and decisions of vr_stats for stochastic calls with aligned
 // rows and draft logits, from one persistent launch (VS_CPS CTAs per SM).
@@ -436,10 +584,16 @@ constexpr int VS_CPS = 3;         // CTAs per SM
 constexpr int VS_NCW = 8;         // consumer warps
 constexpr int VS_EPN = 4;         // epilogue slots
 constexpr int VS_MB = 8;          // part-merge buffers (more than VS_NS)
+constexpr int VR2_HALF = VS_STAGE / 2;   // bytes of each row in a residual stage
 constexpr int VS_T = (VS_NCW + 2) * 32;
 
+// A stage: type 0, tokens [tok0, tok0 + ntok) of the row of part `item`;
+// type 1, a residual stage of sequence b's row pair j (target half, then draft
+// half unless qonly) with its coefficients.
 struct VsMeta {
     int item, tok0, ntok, last, dt;
+    int type, b, j, qonly;
+    float Mt, dLhi, dLlo;
 };
 struct VsEp {
     VrStat st;
@@ -556,7 +710,7 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K = P.K, V = P.V;
     const uint32_t lim = P.spin_limit;
-    uint32_t *tflag = P.vctl + 1;
+    uint32_t *tflag = P.vctl + VC_TIMEOUT * VC_LINE;
     if (tid == 0) {
         for (int s = 0; s < VS_NS; ++s) {
             mbar_init(&full[s], 1);
@@ -580,9 +734,101 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
         int st = 0;
         uint32_t ph = 0;
         bool ok = true;
-        int item = (int)atomicAdd(P.vctl, 1u);
-        while (ok && item < nitems) {
-            const int next = (int)atomicAdd(P.vctl, 1u);   // claimed ahead, used after this part
+        constexpr int RT = VR2_HALF / E::ES;   // tokens of each row in a residual stage
+        // the next statistics part: claimed one ahead, except with the residual
+        // pass, where a producer claims a part only when it starts it (a part
+        // held while residual chunks go first would delay the decisions that
+        // post the residual jobs)
+        int item = P.fused ? -1 : (int)atomicAdd(P.vctl + VC_CLAIM * VC_LINE, 1u);
+        bool drained = false;
+        uint32_t idle = 0;
+        int pend = -1;   // a residual chunk number claimed ahead of its job
+        while (ok) {
+            if (P.fused) {
+                // a posted residual chunk first: its row pair was streamed
+                // recently, so it is mostly read from L2.  Chunks are handed out
+                // by one counter (atomicAdd, no compare-and-swap storms); a
+                // producer holds at most one number claimed ahead of the posted
+                // jobs and takes it up once its job is posted.
+                int ticket = -1;
+                const uint32_t avail = ld_acq(P.vctl + VC_JOBS * VC_LINE) * (uint32_t)P.rnch;
+                if (pend < 0 && (drained || __ldcg(P.vctl + VC_TICKETS * VC_LINE) < avail))
+                    pend = (int)atomicAdd(P.vctl + VC_TICKETS * VC_LINE, 1u);
+                if (pend >= 0 && (uint32_t)pend < avail) {
+                    ticket = pend;
+                    pend = -1;
+                }
+                if (ticket >= 0) {
+                    idle = 0;
+                    const int e = ticket / P.rnch, ch = ticket - e * P.rnch;
+                    // the job was reserved before its chunks could be claimed: its
+                    // poster is writing it
+                    int b1 = 0;
+                    for (uint32_t it = 0; it <= lim; ++it) {
+                        b1 = ld_acq_s32(&P.jobs[e].b1);
+                        if (b1)
+                            break;
+                        __nanosleep(32);
+                    }
+                    if (!b1) {
+                        atomicExch(tflag, 1u);
+                        ok = false;
+                        break;
+                    }
+                    const VrJob jb = P.jobs[e];
+                    const int b = b1 - 1, j = jb.j;
+                    const bool qonly = j == K;
+                    const uint8_t *trow =
+                        static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + j) * (size_t)V * E::ES;
+                    const uint8_t *drow =
+                        qonly ? trow
+                              : static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + j) * (size_t)V * E::ES;
+                    for (int sg = 0; sg < P.rcs; ++sg) {
+                        const int tok0 = (ch * P.rcs + sg) * RT;
+                        if (tok0 >= V)
+                            break;
+                        const int n = min(RT, V - tok0);
+                        if (!vs_wait(&empty[st], ph ^ 1u, lim, tflag)) {
+                            ok = false;
+                            break;
+                        }
+                        meta[st] = VsMeta{-2, tok0, n, 0, -1, 1, b, j, qonly ? 1 : 0, jb.Mt, jb.dLhi, jb.dLlo};
+                        const uint32_t nb = (uint32_t)(n * E::ES);
+                        mbar_arrive_tx(&full[st], qonly ? nb : 2u * nb);
+                        bulk_g2s(vs_buf + st * VS_STAGE, trow + (size_t)tok0 * E::ES, nb, &full[st]);
+                        if (!qonly)
+                            bulk_g2s(vs_buf + st * VS_STAGE + VR2_HALF, drow + (size_t)tok0 * E::ES, nb, &full[st]);
+                        if (++st == VS_NS) {
+                            st = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    continue;
+                }
+            }
+            if (P.fused && !drained) {
+                item = (int)atomicAdd(P.vctl + VC_CLAIM * VC_LINE, 1u);
+                drained = item >= nitems;
+            }
+            if (item >= nitems || drained) {
+                // no part left: with the residual pass, wait until every sequence
+                // has ended and every posted chunk is claimed
+                if (!P.fused)
+                    break;
+                // every sequence ended: the jobs are final, and a number held past
+                // them has no chunk
+                if (ld_acq(P.vctl + VC_ENDED * VC_LINE) >= (uint32_t)P.B &&
+                    (pend < 0 || (uint32_t)pend >= ld_acq(P.vctl + VC_JOBS * VC_LINE) * (uint32_t)P.rnch))
+                    break;
+                if (++idle > lim) {
+                    atomicExch(tflag, 1u);
+                    ok = false;
+                    break;
+                }
+                __nanosleep(500);
+                continue;
+            }
+            const int next = P.fused ? nitems : (int)atomicAdd(P.vctl + VC_CLAIM * VC_LINE, 1u);   // claimed ahead
             const int r = item / P.parts, part = item - r * P.parts;
             int i, b, kind;
             vs_row(P, r, i, b, kind);
@@ -606,7 +852,7 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
                     ok = false;
                     break;
                 }
-                meta[st] = VsMeta{item, tok, n, tok + STOK >= t1 ? 1 : 0, dt};
+                meta[st] = VsMeta{item, tok, n, tok + STOK >= t1 ? 1 : 0, dt, 0, 0, 0, 0, 0.0f, 0.0f, 0.0f};
                 mbar_arrive_tx(&full[st], (uint32_t)(n * E::ES));
                 bulk_g2s(vs_buf + st * VS_STAGE, row + (size_t)tok * E::ES, (uint32_t)(n * E::ES), &full[st]);
                 if (++st == VS_NS) {
@@ -618,7 +864,7 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
         }
         // end of the stream
         if (ok && vs_wait(&empty[st], ph ^ 1u, lim, tflag)) {
-            meta[st].item = -1;
+            meta[st] = VsMeta{-1, 0, 0, 0, -1, 0, 0, 0, 0, 0.0f, 0.0f, 0.0f};
             mbar_arrive(&full[st]);
         }
         return;
@@ -662,9 +908,54 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
             break;
         (void)mbar_test(&full[st], ph);   // every lane observes the completed phase
         const VsMeta mt = meta[st];
-        if (mt.item < 0)
+        if (mt.type == 0 && mt.item < 0)
             break;
         const uint8_t *sb = vs_buf + st * VS_STAGE;
+        if (mt.type == 1) {
+            // a residual stage: the masses of its 256-token segments
+            constexpr int SPW = VR2_HALF / E::ES / VSEG / VS_NCW;   // segments per warp
+            static_assert(SPW * VSEG * VS_NCW * E::ES == VR2_HALF, "a stage is whole segments");
+            const ResK k{mt.Mt, mt.dLhi, mt.dLlo, c};
+            float v[2 * SPW];
+#pragma unroll
+            for (int q = 0; q < SPW; ++q) {
+                const int x = (warp + q * VS_NCW) * VSEG + lane * 8;   // token within the stage
+                v[2 * q] = v[2 * q + 1] = 0.0f;
+                if (x < mt.ntok) {
+                    const uint4 *pt = reinterpret_cast<const uint4 *>(sb + (size_t)x * E::ES);
+                    const uint4 *pd = reinterpret_cast<const uint4 *>(sb + VR2_HALF + (size_t)x * E::ES);
+                    Unit<E> ut, ud;
+                    ut.a = pt[0];
+                    ud.a = mt.qonly ? ut.a : pd[0];
+                    if constexpr (E::ES == 4) {
+                        const uint4 ninf = make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+                        const bool whole = x + 8 <= mt.ntok;   // else its last four tokens are past the row
+                        ut.b = whole ? pt[1] : ninf;
+                        ud.b = mt.qonly ? ut.b : (whole ? pd[1] : ninf);
+                    }
+                    f2 XT[4], XD[4], R[4], Q[4];
+                    unit_pairs<E>(ut, XT);
+                    unit_pairs<E>(ud, XD);
+                    vr_res8(XT, XD, k, mt.qonly != 0, R, Q);
+                    v[2 * q] = sum4p(R);
+                    v[2 * q + 1] = sum4p(Q);
+                }
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[st]);
+            if (++st == VS_NS) {
+                st = 0;
+                ph ^= 1u;
+            }
+            // lane (2q + w) * 32 / (2 SPW) holds value w of segment q (w = 0: r', 1: q')
+            const float tot = xpose_sum<2 * SPW>(v, lane);
+            const int vi = lane / (32 / (2 * SPW));
+            const int sl = warp + (vi >> 1) * VS_NCW;
+            if (lane % (32 / (2 * SPW)) == 0 && sl * VSEG < mt.ntok)
+                reinterpret_cast<float *>(P.segm + (size_t)mt.b * P.nseg + mt.tok0 / VSEG + sl)[vi & 1] = tot;
+            continue;
+        }
         const uint4 *p = reinterpret_cast<const uint4 *>(sb);
         vs_stage<E, CT>(p, mt.ntok, tid, c, mc, s, fl);
         if (tid == 0 && (unsigned)(mt.dt - mt.tok0) < (unsigned)mt.ntok) {
@@ -739,78 +1030,6 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
 }
 
 // ---------------------------------------------------------------- 2. residual masses
-// q'(x) = 2^(xt c - Mt) and r'(x) = q'(x) (1 - 2^delta)_+ for 8 tokens as four
-// float pairs, delta = (xd - xt) c - dL (both scaled by the target's
-// normaliser, which cancels in the inverse CDF).  1 - 2^delta on [-1, 0) is
-// 2^(delta/2) * (-2 sinh(delta ln2 / 2)) with sinh as its odd Taylor series to
-// y^9 (the factor -2 folded into its coefficients, an exact scaling), so
-// nothing cancels as q -> p; below -1 it is 1 - 2^delta.  With qonly (the
-// bonus row) r' = q'.
-__device__ __forceinline__ void vr_res8(const f2 *XT, const f2 *XD, const ResK &k, bool qonly, f2 *R, f2 *Q)
-{
-    const f2 cc = pk(k.c, k.c), nMt = pk(-k.Mt, -k.Mt);
-#pragma unroll
-    for (int p = 0; p < 4; ++p)
-        Q[p] = ex2x2(fma2(XT[p], cc, nMt));
-    if (qonly) {
-#pragma unroll
-        for (int p = 0; p < 4; ++p)
-            R[p] = Q[p];
-        return;
-    }
-    const f2 ndh = pk(-k.dLhi, -k.dLhi), ndl = pk(-k.dLlo, -k.dLlo);
-    const f2 hl = pk(0.34657359027997264f, 0.34657359027997264f);   // ln2 / 2
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const f2 dd = fma2(XT[p], pk(-1.0f, -1.0f), XD[p]);           // xd - xt
-        float d0, d1;
-        upk(add2(fma2(dd, cc, ndh), ndl), d0, d1);                    // delta
-        d0 = fminf(d0, 0.0f);                                         // also maps NaN (both -inf) to 0
-        d1 = fminf(d1, 0.0f);
-        const bool far0 = d0 < -1.0f, far1 = d1 < -1.0f;
-        float e0, e1;
-        upk(ex2x2(pk(far0 ? d0 : 0.5f * d0, far1 ? d1 : 0.5f * d1)), e0, e1);
-        const f2 y = mul2(pk(d0, d1), hl);
-        const f2 y2 = mul2(y, y);
-        f2 sp = pk(-2.0f / 362880.0f, -2.0f / 362880.0f);
-        sp = fma2(sp, y2, pk(-2.0f / 5040.0f, -2.0f / 5040.0f));
-        sp = fma2(sp, y2, pk(-2.0f / 120.0f, -2.0f / 120.0f));
-        sp = fma2(sp, y2, pk(-2.0f / 6.0f, -2.0f / 6.0f));
-        sp = fma2(sp, y2, pk(-2.0f, -2.0f));
-        float s0, s1;
-        upk(mul2(y, sp), s0, s1);                                     // -2 sinh(delta ln2 / 2)
-        // far: 1 - e; near: e * (-2 sinh)
-        const float o0 = fmaf(far0 ? -1.0f : s0, e0, far0 ? 1.0f : 0.0f);
-        const float o1 = fmaf(far1 ? -1.0f : s1, e1, far1 ? 1.0f : 0.0f);
-        R[p] = mul2(Q[p], pk(o0, o1));
-    }
-}
-// The sum of a unit's 8 values held as four pairs, in a fixed order (the
-// locate pass repeats it).
-__device__ __forceinline__ float sum4p(const f2 *V)
-{
-    float lo, hi;
-    upk(add2(add2(V[0], V[1]), add2(V[2], V[3])), lo, hi);
-    return lo + hi;
-}
-// Sum each of 8 values over the 32 lanes (a transposed butterfly: 9 shuffles
-// in place of 40); lane 4 v ends with the total of value v.
-__device__ __forceinline__ float xpose8(const float *v, int lane)
-{
-    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
-    float a[4], c[2];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-        a[i] = (b4 ? v[4 + i] : v[i]) + __shfl_xor_sync(0xffffffffu, b4 ? v[i] : v[4 + i], 16);
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-        c[i] = (b3 ? a[2 + i] : a[i]) + __shfl_xor_sync(0xffffffffu, b3 ? a[i] : a[2 + i], 8);
-    float d = (b2 ? c[1] : c[0]) + __shfl_xor_sync(0xffffffffu, b2 ? c[0] : c[1], 4);
-    d += __shfl_xor_sync(0xffffffffu, d, 2);
-    d += __shfl_xor_sync(0xffffffffu, d, 1);
-    return d;
-}
-
 // The coefficients of the distribution sequence b samples at its end j, from
 // the statistics t of its target row j and d of its draft row j (j < K).
 __device__ __forceinline__ ResK res_coef(const RowsParams &P, const VrStat &t, const VrStat &d, int j)
@@ -855,6 +1074,27 @@ __device__ __forceinline__ ResK vr_coef(const RowsParams &P, int b, int j)
         k.dLlo = dl.lo;
     }
     return k;
+}
+
+// Sequence b has ended (word w): post its residual job -- the position j it
+// ended at and the coefficients of row pair j -- unless it ended in error
+// (vr_sample writes those outputs); then count it as ended.
+__device__ __noinline__ void vr_post_end(const RowsParams &P, int b, unsigned long long w)
+{
+    const int K = P.K;
+    const int j = __ffs((uint32_t)(w >> 32)) - 1;
+    const int code = (__ldcg(P.rej + b) >> j) & 1u ? __ldcg(P.errc + (size_t)b * (K + 1) + j) : 0;
+    if (!code) {
+        const ResK k = vr_coef(P, b, j);
+        const uint32_t e = vr_atom_add(P.vctl + VC_JOBS * VC_LINE, 1u);
+        VrJob *jb = P.jobs + e;
+        jb->j = j;
+        jb->Mt = k.Mt;
+        jb->dLhi = k.dLhi;
+        jb->dLlo = k.dLlo;
+        st_rel_s32(&jb->b1, b + 1);
+    }
+    vr_atom_add(P.vctl + VC_ENDED * VC_LINE, 1u);
 }
 
 // Draft logits of the 8 tokens [seg * VSEG + 8 lane, +8) from a shortlisted
@@ -986,7 +1226,7 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
         sm_e[tid] = __ldcg(P.errc + (size_t)b * (K + 1) + tid);
     if (tid == 0) {
         sm_m = __ldcg(P.rej + b);
-        sm_tf = __ldcg(P.vctl + 1);
+        sm_tf = __ldcg(P.vctl + VC_TIMEOUT * VC_LINE);
     }
     __syncthreads();
     const uint32_t msk = sm_m;
@@ -1250,11 +1490,13 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
         P.rowcnt[(size_t)b * (2 * K + 1) + i] = 0u;
     if (tid == 0) {
         P.rej[b] = 0u;
+        P.dw[b] = 0ull;
+        P.jobs[b].b1 = 0;   // job slots are taken in posting order: slot b is some sequence's
         // the last CTA zeroes the call's counters (every CTA read the timeout word first)
-        if (vr_atom_add(P.vctl + 2, 1u) == gridDim.x - 1) {
-            P.vctl[0] = 0u;
-            P.vctl[1] = 0u;
-            P.vctl[2] = 0u;
+        if (vr_atom_add(P.vctl + VC_SDONE * VC_LINE, 1u) == gridDim.x - 1) {
+#pragma unroll
+            for (int w = 0; w < VC_N; ++w)
+                P.vctl[w * VC_LINE] = 0u;
         }
     }
 }
@@ -1312,6 +1554,19 @@ bool use_stream(const RowsParams &P)
     return !P.greedy && !P.sl && P.vec;
 }
 
+constexpr long long kFusedMinRows = 1024;
+
+// Whether vr_stream runs the residual pass: SPECVERIFY_ROWS_FUSED=1 always,
+// =0 never (vr_residual does), unset by the call's size (-1); for
+// measurement and tests.
+int fused_mode()
+{
+    const char *ev = std::getenv("SPECVERIFY_ROWS_FUSED");
+    if (!ev || !*ev)
+        return -1;
+    return std::atoi(ev) != 0 ? 1 : 0;
+}
+
 // The persistent statistics launch: VS_CPS CTAs per SM; parts per row so that
 // there are about two parts per CTA, each at least two stages long (the
 // epilogue's round trips per part make finer parts slower).
@@ -1354,6 +1609,16 @@ cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream, int &launches)
         return e;
     launches = 0;
     if (use_stream(P)) {
+        // the residual pass in the same launch, in chunks of four stages, for
+        // calls of at least kFusedMinRows rows (measured: B = 256, K = 4 at
+        // 122 us against 138 us with vr_residual; B = 64, K = 4 at 64.5 us
+        // against 61.5 us)
+        const int fm = fused_mode();
+        P.fused = fm == 1 || (fm < 0 && (long long)P.B * (2 * P.K + 1) >= kFusedMinRows) ? 1 : 0;
+        constexpr int RT = VR2_HALF / E::ES;
+        const int nst = (P.V + RT - 1) / RT;
+        P.rcs = 4;
+        P.rnch = (nst + P.rcs - 1) / P.rcs;
         e = launch_stream<E>(P, sms, stream);
         launches += 1;
     } else {
@@ -1370,7 +1635,7 @@ cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream, int &launches)
     }
     if (e != cudaSuccess)
         return e;
-    if (!P.greedy) {
+    if (!P.greedy && !P.fused) {
         e = launch_after(vr_residual<E>, P.B * P.nch, VRT, 0, stream, P);
         launches += 1;
         if (e != cudaSuccess)

@@ -211,9 +211,22 @@ struct alignas(16) VrStat {
     int pad0, pad1, pad2;
 };
 enum { VR_BAD = 1, VR_SKIP = 2, VR_HASD = 4, VR_SLBAD = 8 };
+// The row-parallel call's counters (words VC_* * VC_LINE of vctl): parts
+// claimed by vr_stream, timeout (a bounded wait ran out), vr_sample CTAs done
+// (the last one zeroes the counters), residual jobs posted, residual chunks
+// claimed, sequences ended.
+enum { VC_CLAIM = 0, VC_TIMEOUT = 1, VC_SDONE = 2, VC_JOBS = 3, VC_TICKETS = 4, VC_ENDED = 5, VC_N = 6 };
+constexpr int VC_LINE = 32;
 constexpr int VR_SMAX = 16;   // most parts a row is split into
 struct VrSeg {
     float r, q;   // residual and target masses of one 256-token segment, relative to 2^Mt
+};
+// A residual job of vr_stream: sequence b (stored as b + 1, 0 until written)
+// ended at position j; the coefficients of its row pair j.
+struct alignas(16) VrJob {
+    int b1, j;
+    float Mt, dLhi, dLlo;
+    int pad0, pad1, pad2;
 };
 
 struct RowsParams {
@@ -246,15 +259,20 @@ struct RowsParams {
     int greedy, skip, vec;
     float c;
     uint32_t key0, key1;
-    // [0] parts claimed by vr_stream, [1] timeout (a bounded wait ran out),
-    // [2] vr_sample CTAs done (the last one zeroes the three)
+    // the call's counters, each on its own 128-byte line (index VC_* * 32)
     uint32_t *vctl;
     uint32_t spin_limit;
+    // vr_stream's residual pass (fused != 0): per sequence the decided
+    // positions (low 32 bits) and the positions that end it (high 32 bits);
+    // the posted jobs; chunks per sequence and stages per chunk
+    unsigned long long *dw;
+    VrJob *jobs;
+    int fused, rnch, rcs;
 };
 
 struct WsLayout {
     size_t ctl, state, res_rec, pair_cnt, res_cnt, fin, errres, sw_ctl, sw_seq, sw_cnt, sw_res_ready, sw_res_done,
-        vr_pair, vr_rej, vr_rowcnt, vr_ctl, errcode, terminal, gtok, dec, part, seg, sl_lb, sw_part, sw_stat, sw_res, sw_resm,
+        vr_pair, vr_rej, vr_rowcnt, vr_ctl, vr_dw, vr_jobs, errcode, terminal, gtok, dec, part, seg, sl_lb, sw_part, sw_stat, sw_res, sw_resm,
         vr_stat, vr_errc, vr_part, vr_segm, vr_lb, total;
     size_t reset_end;   // [ctl, reset_end) holds what a call must find zeroed
     int npt_max, nseg;
@@ -287,7 +305,9 @@ inline WsLayout ws_layout(int B, int K, int V, int S)
     w.vr_pair = o;  o = align256(o + Bz * P * 4);
     w.vr_rej = o;   o = align256(o + Bz * 4);
     w.vr_rowcnt = o; o = align256(o + Bz * (2 * P - 1) * 4);
-    w.vr_ctl = o;   o = align256(o + 4 * 4);
+    w.vr_ctl = o;   o = align256(o + VC_N * VC_LINE * 4);
+    w.vr_dw = o;    o = align256(o + Bz * 8);
+    w.vr_jobs = o;  o = align256(o + Bz * sizeof(VrJob));
     w.reset_end = o;
     w.errcode = o;  o = align256(o + Bz * P * 4);
     w.terminal = o; o = align256(o + Bz * 4);

@@ -27,17 +27,24 @@ def _device():
     sv.load()
 
 
-@pytest.fixture(scope="module", autouse=True, params=["auto", "cluster", "sweep", "rows", "rows-stats", "general"])
+@pytest.fixture(scope="module", autouse=True,
+                params=["auto", "cluster", "sweep", "rows", "rows-stats", "rows-unfused", "general"])
 def kernel(request):
     """Every case runs under the default dispatch and under each kernel forced
     in turn: the cluster kernel, the sweep kernel, the row-parallel kernels
     (with the bulk-copy statistics stream, and with the per-position
     statistics launches in its place: "rows-stats") and the chunk-scheduled
-    kernel (each falls back to the next for shapes it does not serve)."""
-    saved = {k: os.environ.get(k) for k in ("SPECVERIFY_KERNEL", "SPECVERIFY_ROWS_STREAM")}
-    os.environ["SPECVERIFY_KERNEL"] = "rows" if request.param == "rows-stats" else request.param
+    kernel (each falls back to the next for shapes it does not serve);
+    "rows" runs the residual pass inside the statistics stream at every size,
+    "rows-unfused" keeps it in its own launch."""
+    saved = {k: os.environ.get(k) for k in ("SPECVERIFY_KERNEL", "SPECVERIFY_ROWS_STREAM", "SPECVERIFY_ROWS_FUSED")}
+    os.environ["SPECVERIFY_KERNEL"] = "rows" if request.param.startswith("rows") else request.param
     if request.param == "rows-stats":
         os.environ["SPECVERIFY_ROWS_STREAM"] = "0"
+    if request.param == "rows":
+        os.environ["SPECVERIFY_ROWS_FUSED"] = "1"
+    if request.param == "rows-unfused":
+        os.environ["SPECVERIFY_ROWS_FUSED"] = "0"
     yield request.param
     for k, v in saved.items():
         if v is None:
