@@ -62,7 +62,7 @@ CSRC = os.path.join(_ROOT, "speculative_decoding_verification_sampling_gb300", "
 TRAFFIC_RECORD = os.path.join(_ROOT, "profiles", "rows_kernels_stoch_b256_k4.md")
 # What one call launches at this workload (the library's dispatch): the
 # row-parallel kernels, two statistics launches, the residual masses, the sampling.
-PATH_KERNELS = "vr_stream + vr_residual + vr_sample (row-parallel verification, stochastic, bf16)"
+PATH_KERNELS = "vr_stream (statistics + residual masses) + vr_sample (row-parallel verification, stochastic, bf16)"
 REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
 
