@@ -462,7 +462,8 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
 // float pairs, delta = (xd - xt) c - dL (both scaled by the target's
 // normaliser, which cancels in the inverse CDF).  1 - 2^delta on [-1, 0) is
 // 2^(delta/2) * (-2 sinh(delta ln2 / 2)) with sinh as its odd Taylor series to
-// y^9 (the factor -2 folded into its coefficients, an exact scaling), so
+// y^7 (|y| <= ln2 / 2, so the first term left out is below 6e-9 relative;
+// the factor -2 is folded into the coefficients, an exact scaling), so
 // nothing cancels as q -> p; below -1 it is 1 - 2^delta.  With qonly (the
 // bonus row) r' = q'.
 __device__ __forceinline__ void vr_res8(const f2 *XT, const f2 *XD, const ResK &k, bool qonly, f2 *R, f2 *Q)
@@ -491,8 +492,7 @@ __device__ __forceinline__ void vr_res8(const f2 *XT, const f2 *XD, const ResK &
         upk(ex2x2(pk(far0 ? d0 : 0.5f * d0, far1 ? d1 : 0.5f * d1)), e0, e1);
         const f2 y = mul2(pk(d0, d1), hl);
         const f2 y2 = mul2(y, y);
-        f2 sp = pk(-2.0f / 362880.0f, -2.0f / 362880.0f);
-        sp = fma2(sp, y2, pk(-2.0f / 5040.0f, -2.0f / 5040.0f));
+        f2 sp = pk(-2.0f / 5040.0f, -2.0f / 5040.0f);
         sp = fma2(sp, y2, pk(-2.0f / 120.0f, -2.0f / 120.0f));
         sp = fma2(sp, y2, pk(-2.0f / 6.0f, -2.0f / 6.0f));
         sp = fma2(sp, y2, pk(-2.0f, -2.0f));
@@ -743,68 +743,70 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
         bool drained = false;
         uint32_t idle = 0;
         int pend = -1;   // a residual chunk number claimed ahead of its job
+        // Take up a posted residual chunk, if there is one; true when it was
+        // taken (streamed, or a wait gave up and ok is false).  Residual chunks
+        // go before the next statistics part: the row pair was streamed
+        // recently, so part of it is still in L2.
+        // Chunks are handed out by one counter (atomicAdd, no compare-and-swap
+        // storms); a producer holds at most one number claimed ahead of the
+        // posted jobs and takes it up once its job is posted.
+        auto take_residual = [&]() -> bool {
+            const uint32_t avail = ld_acq(P.vctl + VC_JOBS * VC_LINE) * (uint32_t)P.rnch;
+            if (pend < 0 && (drained || __ldcg(P.vctl + VC_TICKETS * VC_LINE) < avail))
+                pend = (int)atomicAdd(P.vctl + VC_TICKETS * VC_LINE, 1u);
+            if (pend < 0 || (uint32_t)pend >= avail)
+                return false;
+            const int ticket = pend;
+            pend = -1;
+            const int e = ticket / P.rnch, ch = ticket - e * P.rnch;
+            // the job was reserved before its chunks could be claimed: its
+            // poster is writing it
+            int b1 = 0;
+            for (uint32_t it = 0; it <= lim; ++it) {
+                b1 = ld_acq_s32(&P.jobs[e].b1);
+                if (b1)
+                    break;
+                __nanosleep(32);
+            }
+            if (!b1) {
+                atomicExch(tflag, 1u);
+                ok = false;
+                return true;
+            }
+            const VrJob jb = P.jobs[e];
+            const int b = b1 - 1, j = jb.j;
+            const bool qonly = j == K;
+            const uint8_t *trow =
+                static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + j) * (size_t)V * E::ES;
+            const uint8_t *drow =
+                qonly ? trow
+                      : static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + j) * (size_t)V * E::ES;
+            for (int sg = 0; sg < P.rcs; ++sg) {
+                const int tok0 = (ch * P.rcs + sg) * RT;
+                if (tok0 >= V)
+                    break;
+                const int n = min(RT, V - tok0);
+                if (!vs_wait(&empty[st], ph ^ 1u, lim, tflag)) {
+                    ok = false;
+                    break;
+                }
+                meta[st] = VsMeta{-2, tok0, n, 0, -1, 1, b, j, qonly ? 1 : 0, jb.Mt, jb.dLhi, jb.dLlo};
+                const uint32_t nb = (uint32_t)(n * E::ES);
+                mbar_arrive_tx(&full[st], qonly ? nb : 2u * nb);
+                bulk_g2s(vs_buf + st * VS_STAGE, trow + (size_t)tok0 * E::ES, nb, &full[st]);
+                if (!qonly)
+                    bulk_g2s(vs_buf + st * VS_STAGE + VR2_HALF, drow + (size_t)tok0 * E::ES, nb, &full[st]);
+                if (++st == VS_NS) {
+                    st = 0;
+                    ph ^= 1u;
+                }
+            }
+            return true;
+        };
         while (ok) {
-            if (P.fused) {
-                // a posted residual chunk first: its row pair was streamed
-                // recently, so it is mostly read from L2.  Chunks are handed out
-                // by one counter (atomicAdd, no compare-and-swap storms); a
-                // producer holds at most one number claimed ahead of the posted
-                // jobs and takes it up once its job is posted.
-                int ticket = -1;
-                const uint32_t avail = ld_acq(P.vctl + VC_JOBS * VC_LINE) * (uint32_t)P.rnch;
-                if (pend < 0 && (drained || __ldcg(P.vctl + VC_TICKETS * VC_LINE) < avail))
-                    pend = (int)atomicAdd(P.vctl + VC_TICKETS * VC_LINE, 1u);
-                if (pend >= 0 && (uint32_t)pend < avail) {
-                    ticket = pend;
-                    pend = -1;
-                }
-                if (ticket >= 0) {
-                    idle = 0;
-                    const int e = ticket / P.rnch, ch = ticket - e * P.rnch;
-                    // the job was reserved before its chunks could be claimed: its
-                    // poster is writing it
-                    int b1 = 0;
-                    for (uint32_t it = 0; it <= lim; ++it) {
-                        b1 = ld_acq_s32(&P.jobs[e].b1);
-                        if (b1)
-                            break;
-                        __nanosleep(32);
-                    }
-                    if (!b1) {
-                        atomicExch(tflag, 1u);
-                        ok = false;
-                        break;
-                    }
-                    const VrJob jb = P.jobs[e];
-                    const int b = b1 - 1, j = jb.j;
-                    const bool qonly = j == K;
-                    const uint8_t *trow =
-                        static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + j) * (size_t)V * E::ES;
-                    const uint8_t *drow =
-                        qonly ? trow
-                              : static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + j) * (size_t)V * E::ES;
-                    for (int sg = 0; sg < P.rcs; ++sg) {
-                        const int tok0 = (ch * P.rcs + sg) * RT;
-                        if (tok0 >= V)
-                            break;
-                        const int n = min(RT, V - tok0);
-                        if (!vs_wait(&empty[st], ph ^ 1u, lim, tflag)) {
-                            ok = false;
-                            break;
-                        }
-                        meta[st] = VsMeta{-2, tok0, n, 0, -1, 1, b, j, qonly ? 1 : 0, jb.Mt, jb.dLhi, jb.dLlo};
-                        const uint32_t nb = (uint32_t)(n * E::ES);
-                        mbar_arrive_tx(&full[st], qonly ? nb : 2u * nb);
-                        bulk_g2s(vs_buf + st * VS_STAGE, trow + (size_t)tok0 * E::ES, nb, &full[st]);
-                        if (!qonly)
-                            bulk_g2s(vs_buf + st * VS_STAGE + VR2_HALF, drow + (size_t)tok0 * E::ES, nb, &full[st]);
-                        if (++st == VS_NS) {
-                            st = 0;
-                            ph ^= 1u;
-                        }
-                    }
-                    continue;
-                }
+            if (P.fused && take_residual()) {
+                idle = 0;
+                continue;
             }
             if (P.fused && !drained) {
                 item = (int)atomicAdd(P.vctl + VC_CLAIM * VC_LINE, 1u);
