@@ -600,10 +600,16 @@ struct VsEp {
     int item, dt, pad0, pad1;
 };
 
-// Bounded wait for the phase of parity `par`; sets the timeout word when the
-// polls run out.
+// Bounded wait for the phase of parity `par` of one of the CTA's own
+// barriers (its ring of copies and its hand-offs); sets the timeout word when
+// it runs out.  The bound is the call's spin limit, but never below
+// VS_RING_MIN polls, so a small limit cannot leave copies in flight when the
+// CTA winds down: the waits on other CTAs (the end of every sequence, a
+// posted job) are the ones a small limit exercises.
+constexpr uint32_t VS_RING_MIN = 1u << 20;
 __device__ __forceinline__ bool vs_wait(unsigned long long *bar, uint32_t par, uint32_t limit, uint32_t *tflag)
 {
+    limit = max(limit, VS_RING_MIN);
     for (uint32_t it = 0;; ++it) {
         if (mbar_test(bar, par))
             return true;
@@ -742,7 +748,8 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
         int item = P.fused ? -1 : (int)atomicAdd(P.vctl + VC_CLAIM * VC_LINE, 1u);
         bool drained = false;
         uint32_t idle = 0;
-        int pend = -1;   // a residual chunk number claimed ahead of its job
+        int pend = -1;      // a residual chunk number claimed ahead of its job
+        bool stop = false;  // a wait on other CTAs gave up (ok: the ring is intact)
         // Take up a posted residual chunk, if there is one; true when it was
         // taken (streamed, or a wait gave up and ok is false).  Residual chunks
         // go before the next statistics part: the row pair was streamed
@@ -769,8 +776,9 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
                 __nanosleep(32);
             }
             if (!b1) {
+                // gave up on another CTA: stop claiming, wind down normally
                 atomicExch(tflag, 1u);
-                ok = false;
+                stop = true;
                 return true;
             }
             const VrJob jb = P.jobs[e];
@@ -805,6 +813,8 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
         };
         while (ok) {
             if (P.fused && take_residual()) {
+                if (stop)
+                    break;
                 idle = 0;
                 continue;
             }
@@ -823,8 +833,9 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
                     (pend < 0 || (uint32_t)pend >= ld_acq(P.vctl + VC_JOBS * VC_LINE) * (uint32_t)P.rnch))
                     break;
                 if (++idle > lim) {
+                    // gave up on the other CTAs: stop claiming, wind down normally
                     atomicExch(tflag, 1u);
-                    ok = false;
+                    stop = true;
                     break;
                 }
                 __nanosleep(500);
