@@ -106,6 +106,8 @@ __device__ __forceinline__ void draft_error(const DraftParams &P, int r)
 template <class E, int DT>
 __global__ void __launch_bounds__(DT) draft_sample_kernel(const __grid_constant__ DraftParams P)
 {
+    // a kernel launched after this one (the tree walk) may start launching
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int DWARPS = DT / 32;
     constexpr int TPV = 16 / E::ES;    // tokens per 16-byte vector
     constexpr int QT = 32 * TPV;       // tokens per quarter of a segment (one load per lane)

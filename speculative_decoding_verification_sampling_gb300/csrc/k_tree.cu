@@ -12,7 +12,7 @@
 //
 // Verification is two launches: the argmax of every node row (the draft
 // sampler's greedy kernel, one CTA per row, into the workspace), then one CTA
-// per sequence that walks the nodes in order:
+// per sequence that applies, to every node at once, the walk in node order:
 //   a child of an accepted node is accepted iff its token equals the parent
 //   row's argmax; the longest accepted path ends at the deepest accepted node
 //   (lowest index among equally deep ones); the emitted tokens are the path's
@@ -31,6 +31,7 @@ namespace {
 
 constexpr int TW = 128;         // threads of a walk CTA
 constexpr int TREE_NMAX = 2048; // nodes per tree
+constexpr int TREE_KEY = 4096;  // (depth, -index) keys: depth * TREE_KEY + TREE_KEY - 1 - index
 
 struct TreeParams {
     const int32_t *tokens;   // [B][N]
@@ -43,18 +44,33 @@ struct TreeParams {
     int B, N, V;
 };
 
+// One CTA per tree, every node at once.  A node is accepted iff every link on
+// its path to the root holds (a link: the node's token lies in [0, V) and
+// equals the argmax of its parent's row); a node's depth is the number of
+// links on that path.  Both come from pointer jumping over the parent array
+// (ceil(log2 N) rounds, double-buffered in shared memory).  The walk in node
+// order that the rule describes stops at the first node in error, so the
+// status is that of the lowest-numbered one:
+//   - a child of an accepted node whose token lies outside [0, V) (3);
+//   - an accepted node whose row is in error (2).
+// The deepest accepted node (the lowest index among equally deep ones) comes
+// from one atomicMax over (depth, -index), and its path is written back.
 __global__ void __launch_bounds__(TW) tree_walk(const __grid_constant__ TreeParams P)
 {
     __shared__ int32_t s_par[TREE_NMAX], s_tok[TREE_NMAX], s_g[TREE_NMAX];
-    __shared__ uint8_t s_acc[TREE_NMAX];
-    __shared__ int16_t s_depth[TREE_NMAX];
-    __shared__ int s_bad;
-    const int b = blockIdx.x, N = P.N;
+    __shared__ int16_t s_anc[2][TREE_NMAX], s_dep[2][TREE_NMAX];
+    __shared__ uint8_t s_ok[2][TREE_NMAX];
+    __shared__ int s_bad, s_err, s_best;
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the argmax launch's results
+    const int b = blockIdx.x, N = P.N, tid = threadIdx.x;
     const size_t o = (size_t)b * N;
-    if (threadIdx.x == 0)
+    if (tid == 0) {
         s_bad = 0;
+        s_err = 0x7fffffff;
+        s_best = TREE_KEY - 1;   // node 0 at depth 0
+    }
     __syncthreads();
-    for (int n = threadIdx.x; n < N; n += TW) {
+    for (int n = tid; n < N; n += TW) {
         const int p = __ldg(P.parent + o + n);
         s_par[n] = p;
         s_tok[n] = __ldg(P.tokens + o + n);
@@ -65,50 +81,64 @@ __global__ void __launch_bounds__(TW) tree_walk(const __grid_constant__ TreePara
         P.out_nodes[o + n] = -1;
     }
     __syncthreads();
-    if (threadIdx.x != 0)
-        return;
-    int code = s_bad ? 1 : 0;
-    if (!code) {
-        s_acc[0] = 1;
-        s_depth[0] = 0;
-        for (int n = 0; n < N; ++n) {
-            if (n > 0) {
-                const int p = s_par[n];
-                s_depth[n] = (int16_t)(s_depth[p] + 1);
-                s_acc[n] = 0;
-                if (!s_acc[p])
-                    continue;
-                const int t = s_tok[n];
-                if (t < 0 || t >= P.V) {
-                    code = ST_TOKEN;
-                    break;
-                }
-                if (t != s_g[p])
-                    continue;
-                s_acc[n] = 1;
-            }
-            if (s_g[n] < 0) {
-                code = ST_NONFINITE;
-                break;
-            }
+    if (s_bad) {
+        if (tid == 0) {
+            P.out_len[b] = -1;
+            if (P.status)
+                atomicCAS(P.status, 0, 1);
         }
+        return;
     }
-    if (code) {
+    // round 0: each node's own link, one level up
+    for (int n = tid; n < N; n += TW) {
+        const int t = s_tok[n];
+        s_anc[0][n] = (int16_t)(n == 0 ? 0 : s_par[n]);
+        s_dep[0][n] = (int16_t)(n == 0 ? 0 : 1);
+        s_ok[0][n] = n == 0 || (t >= 0 && t < P.V && t == s_g[s_par[n]]);
+    }
+    __syncthreads();
+    int cur = 0;
+    for (int step = 1; step < N; step <<= 1) {
+        for (int n = tid; n < N; n += TW) {
+            const int a = s_anc[cur][n];
+            s_ok[cur ^ 1][n] = s_ok[cur][n] & s_ok[cur][a];
+            s_dep[cur ^ 1][n] = (int16_t)(s_dep[cur][n] + s_dep[cur][a]);
+            s_anc[cur ^ 1][n] = s_anc[cur][a];
+        }
+        __syncthreads();
+        cur ^= 1;
+    }
+    // the first node in error, and the deepest accepted node
+    int err = 0x7fffffff, best = TREE_KEY - 1;
+    for (int n = tid; n < N; n += TW) {
+        const bool acc = s_ok[cur][n];
+        const int t = s_tok[n];
+        if (n > 0 && s_ok[cur][s_par[n]] && !(t >= 0 && t < P.V))
+            err = min(err, n * 4 + ST_TOKEN);
+        else if (acc && s_g[n] < 0)
+            err = min(err, n * 4 + ST_NONFINITE);
+        if (acc)
+            best = max(best, s_dep[cur][n] * TREE_KEY + (TREE_KEY - 1 - n));
+    }
+    if (err != 0x7fffffff)
+        atomicMin(&s_err, err);
+    atomicMax(&s_best, best);
+    __syncthreads();
+    if (tid != 0)
+        return;
+    if (s_err != 0x7fffffff) {
+        const int code = s_err & 3;
         P.out_len[b] = -code;
         if (P.status)
             atomicCAS(P.status, 0, code);
         return;
     }
-    int best = 0;
-    for (int n = 1; n < N; ++n)
-        if (s_acc[n] && s_depth[n] > s_depth[best])
-            best = n;
-    const int d = s_depth[best];
-    for (int n = best, k = d - 1; n > 0; n = s_par[n], --k) {
+    const int bn = TREE_KEY - 1 - (s_best % TREE_KEY), d = s_best / TREE_KEY;
+    for (int n = bn, k = d - 1; n > 0; n = s_par[n], --k) {
         P.out_tokens[o + k] = s_tok[n];
         P.out_nodes[o + k] = n;
     }
-    P.out_tokens[o + d] = s_g[best];
+    P.out_tokens[o + d] = s_g[bn];
     P.out_len[b] = d;
 }
 
@@ -153,8 +183,18 @@ cudaError_t launch_tree_walk(const int32_t *tokens, const int32_t *parent, const
                              cudaStream_t stream)
 {
     TreeParams P{tokens, parent, g, out_tokens, out_nodes, out_len, status, B, N, V};
-    tree_walk<<<B, TW, 0, stream>>>(P);
-    return cudaGetLastError();
+    // launched so that it may start while the argmax launch finishes (it waits
+    // for that launch's results first)
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)B);
+    cfg.blockDim = dim3(TW);
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, tree_walk, P);
 }
 
 cudaError_t launch_tree_mask(const int32_t *parent, int B, int N, uint8_t *mask, int32_t *status, cudaStream_t stream)

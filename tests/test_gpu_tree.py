@@ -109,3 +109,21 @@ def test_mask_reports_malformed_parents():
     st = torch.full((1,), -4, dtype=torch.int32, device=DEV)
     sv.spec_tree_mask(par, device_status=st)
     assert int(st.item()) == 1
+
+
+def test_token_error_under_accepted_parent():
+    # node 1 (the argmax of row 0) is accepted; its child, node 3, carries a
+    # token outside [0, V): SPEC_ERR_TOKEN_RANGE.  A bad token under a rejected
+    # node (node 4, under node 2) is never examined.
+    g = torch.Generator().manual_seed(7)
+    B, V = 3, 100
+    parent = torch.tensor([-1, 0, 0, 1, 2], dtype=torch.int32).expand(B, 5).clone()
+    z = torch.randn((B, 5, V), generator=g)
+    z[:, 0, 4] = 20.0
+    tokens = torch.tensor([0, 4, 7, 50, 60], dtype=torch.int32).expand(B, 5).clone()
+    tokens[0, 3] = V + 5
+    tokens[1, 4] = -7
+    tokens[2, 3] = -1
+    ref = _check(z, tokens, parent)
+    assert ref["accept_len"].tolist() == [-3, ref["accept_len"][1], -3]
+    assert ref["accept_len"][1] >= 0
