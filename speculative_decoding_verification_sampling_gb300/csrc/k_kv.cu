@@ -14,7 +14,8 @@
 // Two kernels in stream order: the copy (one CTA per (layer, sequence,
 // chunk): the a committed entries of a layer are contiguous in both buffers,
 // so each is one contiguous copy of a * W bytes, 16-byte vectors with four in
-// flight per thread), then the length update (one thread per sequence).
+// flight per thread), then the length update (one thread per sequence),
+// launched behind the copy with programmatic dependent launch.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -45,6 +46,10 @@ __device__ __forceinline__ bool kv_ok(const KvParams &P, int a, int n)
 
 __global__ void __launch_bounds__(KT) kv_copy(const __grid_constant__ KvParams P)
 {
+    // the length update may start launching; it waits for this launch's end
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (blockIdx.x == 0 && threadIdx.x == 0 && P.status)
+        *P.status = 0;   // only the length update, after this launch, reports
     const int ch = blockIdx.x % P.nch;
     const long long lb = blockIdx.x / P.nch;   // layer * B + b
     const int b = (int)(lb % P.B);
@@ -81,6 +86,7 @@ __global__ void __launch_bounds__(KT) kv_copy(const __grid_constant__ KvParams P
 
 __global__ void kv_len(const __grid_constant__ KvParams P)
 {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // every copy has read the old lengths
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= P.B)
         return;
@@ -117,14 +123,30 @@ cudaError_t launch_kv_commit(void *cache, const void *staged, int NL, int B, int
         P.nch = 1;
     P.chunk = ((most + P.nch - 1) / P.nch + 15) / 16 * 16;
     *launches = 0;
+    if (staged) {
+        // the copy zeroes the status word; the length update is launched
+        // behind it with programmatic dependent launch
+        kv_copy<<<(unsigned)((long long)NL * B * P.nch), KT, 0, stream>>>(P);
+        ++*launches;
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)((B + 255) / 256));
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        ++*launches;
+        return cudaLaunchKernelEx(&cfg, kv_len, P);
+    }
     if (status) {
         cudaError_t e = cudaMemsetAsync(status, 0, sizeof(int32_t), stream);
         if (e != cudaSuccess)
             return e;
-    }
-    if (staged) {
-        kv_copy<<<(unsigned)((long long)NL * B * P.nch), KT, 0, stream>>>(P);
-        ++*launches;
     }
     kv_len<<<(B + 255) / 256, 256, 0, stream>>>(P);
     ++*launches;
