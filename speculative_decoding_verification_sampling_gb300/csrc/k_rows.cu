@@ -1115,7 +1115,9 @@ __device__ __noinline__ void vr_post_end(const RowsParams &P, int b, unsigned lo
 // scattered into a per-warp buffer of VSEG floats; tokens off the list read
 // -inf, i.e. p = 0.
 template <class E>
-__device__ __forceinline__ void sl_pairs(const RowsParams &P, int b, int j, int seg, int lane, float *buf, f2 *XD)
+// lo, hi: the segment's list range when known (lo >= 0), else loaded here.
+__device__ __forceinline__ void sl_pairs(const RowsParams &P, int b, int j, int seg, int lane, float *buf, f2 *XD,
+                                         int lo = -1, int hi = -1)
 {
 #pragma unroll
     for (int e = 0; e < 8; ++e)
@@ -1125,7 +1127,10 @@ __device__ __forceinline__ void sl_pairs(const RowsParams &P, int b, int j, int 
         const int32_t *lb = P.lb + ((size_t)b * P.K + j) * (P.nseg + 1);
         const int32_t *lst = P.sl + b * P.sl_seq + j * P.sl_pos;
         const void *drow = static_cast<const uint8_t *>(P.draft) + ((size_t)b * P.K + j) * (size_t)P.S * E::ES;
-        const int lo = __ldcg(lb + seg), hi = __ldcg(lb + seg + 1);
+        if (lo < 0) {
+            lo = __ldcg(lb + seg);
+            hi = __ldcg(lb + seg + 1);
+        }
         for (int si = lo + lane; si < hi; si += 32) {
             const int pos = __ldg(lst + si) - seg * VSEG;
             if ((unsigned)pos < (unsigned)VSEG)
@@ -1177,6 +1182,18 @@ __global__ void __launch_bounds__(VRT, E::ES == 2 ? 3 : 1) vr_residual(const __g
     const int nsteps = (s_hi - s_lo + NW - 1) / NW;
     VrSeg *out = P.segm + (size_t)b * P.nseg;
     auto unit_x0 = [&](int t) { return ((s_lo + t * NW + warp) * UPS + lane) * 8; };
+    // a shortlisted draft: the list ranges of this warp's segments, one load
+    // per lane up front, when the warp has at most 32 steps
+    const bool pre = slist && nsteps <= 32;
+    int blo = -1, bhi = -1;
+    if (pre && lane < nsteps) {
+        const int sg = s_lo + lane * NW + warp;
+        if (sg < P.nseg) {
+            const int32_t *lbp = P.lb + ((size_t)b * K + j) * (P.nseg + 1);
+            blo = __ldcg(lbp + sg);
+            bhi = __ldcg(lbp + sg + 1);
+        }
+    }
     // four steps in flight; each buffer is refilled right after its use
     Unit<E> ut[4], ud[4];
 #pragma unroll
@@ -1196,10 +1213,13 @@ __global__ void __launch_bounds__(VRT, E::ES == 2 ? 3 : 1) vr_residual(const __g
             if (t < nsteps) {
                 f2 XT[4], XD[4];
                 unit_pairs<E>(ut[q], XT);
-                if (slist)
-                    sl_pairs<E>(P, b, j, s_lo + t * NW + warp, lane, sl_buf[warp], XD);
-                else if (!qonly)
+                if (slist) {
+                    // the segment's list range: loaded up front (lane t holds step t's)
+                    const int lo = __shfl_sync(0xffffffffu, blo, t & 31), hi = __shfl_sync(0xffffffffu, bhi, t & 31);
+                    sl_pairs<E>(P, b, j, s_lo + t * NW + warp, lane, sl_buf[warp], XD, pre ? lo : -1, hi);
+                } else if (!qonly) {
                     unit_pairs<E>(ud[q], XD);
+                }
                 if (t + 4 < nsteps) {
                     ut[q] = fetch_unit<E>(trow, unit_x0(t + 4), V, P.vec);
                     if (!qonly && !slist)
