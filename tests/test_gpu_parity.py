@@ -344,3 +344,27 @@ def test_gpu_output_distribution_chi_square():
     q1 = np.exp(zt[0] - zt[0].max())
     q1 /= q1.sum()
     assert chisquare(np.bincount(first, minlength=V), q1 * B).pvalue > 1e-3
+
+
+# ------------------------------------------------------------------ every output slot written
+POISON = 0x7F7F7F7F
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_outputs_fully_written_over_poison(T):
+    """Outputs pre-filled with 0x7F7F7F7F: every slot is written (unused token
+    slots as -1), and the results are the oracle's."""
+    B, K, V = 32, 4, 4096
+    cfg = synth.stochastic_gaussian(B, K, V, torch.bfloat16, T if T > 0 else 1.0, 2.0, 0.5, seed=21)
+    cfg = dict(cfg, T=T)
+    d = _to(cfg)
+    ot = torch.full((B, K + 1), POISON, dtype=torch.int32, device=DEV)
+    ol = torch.full((B,), POISON, dtype=torch.int32, device=DEV)
+    if T == 0:
+        sv.spec_verify_greedy(d["target"], d["draft_tokens"], out_tokens=ot, out_accept_len=ol)
+    else:
+        sv.spec_verify(d["target"], d["draft"], d["draft_tokens"], T, 9, out_tokens=ot, out_accept_len=ol)
+    torch.cuda.synchronize()
+    t, l = ot.cpu().numpy(), ol.cpu().numpy()
+    assert not (t == POISON).any() and not (l == POISON).any()
+    assert_parity(t, l, _oracle(cfg, 9), f"poisoned outputs T={T}")
