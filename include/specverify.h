@@ -286,10 +286,11 @@ spec_status_t spec_philox_words(uint64_t seed, uint32_t tag, int B, int P, uint3
 
 /* Number of kernels this library has launched in this process, over every
  * entry point and device: a successful spec_verify* call launches one kernel,
- * or three or four when the row-parallel kernels serve it (large stochastic
- * batches); spec_draft_sample and spec_philox_words launch one each,
- * spec_kv_commit two (one in place).  For
- * accounting; thread-safe.                                                   */
+ * or two to four when the row-parallel kernels serve it (large stochastic
+ * batches: two from 1024 rows with aligned rows, where the residual pass runs
+ * inside the statistics stream); spec_draft_sample and spec_philox_words
+ * launch one each, spec_kv_commit two (one in place).  For accounting;
+ * thread-safe.                                                               */
 uint64_t spec_launch_count(void);
 
 /* A static description of a status code. */
