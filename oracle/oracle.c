@@ -91,7 +91,9 @@ void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
-/* 24-bit uniform in (0, 1), exact in float32 and float64. */
+/* Uniform in (0, 1) from the top 24 bits n = w >> 8 of a word: (n + 0.5) 2^-24,
+ * i.e. (2n + 1) 2^-25, exact in float64.  It needs 25 significant bits, so a
+ * float32 holds it exactly only for n < 2^23.                                 */
 double oracle_uniform24(uint32_t w)
 {
     return ((double)(w >> 8) + 0.5) * (1.0 / 16777216.0);

@@ -23,7 +23,7 @@ from .build import LIB as _LIB_PATH
 __all__ = [
     "SpecVerifyError", "Aux", "spec_verify", "spec_verify_greedy", "spec_verify_shortlist",
     "spec_workspace_bytes", "spec_philox_words", "spec_draft_sample", "spec_kv_commit", "spec_verify_tree_greedy", "spec_tree_mask",
-    "spec_verify_shortlist_pos", "dynaspec_budget", "spec_status_string", "spec_launch_count", "spec_verify_static", "library_path", "load",
+    "spec_verify_shortlist_pos", "spec_status_string", "spec_launch_count", "spec_verify_static", "library_path", "load",
 ]
 
 SPEC_F32, SPEC_BF16 = 0, 1
@@ -414,14 +414,6 @@ def spec_tree_mask(parent: torch.Tensor, *, out=None, device_status=None, stream
     if rc:
         raise SpecVerifyError(rc, "spec_tree_mask")
     return out
-
-
-def dynaspec_budget(kmax: int, K: int) -> list[int]:
-    """Clusters the drafter uses at draft step t = 0..K-1 under DynaSpec's
-    position-aware budget (DynaSpec summary, § Method 3): kmax for t in {0, 1},
-    floor(kmax / ((t + 1) * 2)) for t >= 2, taken as printed, and at least one
-    cluster (an empty shortlist would leave the drafter nothing to propose)."""
-    return [kmax if t < 2 else max(1, kmax // ((t + 1) * 2)) for t in range(K)]
 
 
 def spec_verify_shortlist_pos(target: torch.Tensor, draft_sl: torch.Tensor, shortlist_idx: torch.Tensor,

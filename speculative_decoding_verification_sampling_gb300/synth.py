@@ -223,6 +223,15 @@ def tree_greedy(B: int = 32, V: int = 128256, branching=(4, 2, 2, 1, 1), dtype=t
                 tree_tokens=tokens.to(torch.int32), parent=par, B=B, N=N, V=V)
 
 
+def dynaspec_budget(kmax: int, K: int) -> list[int]:
+    """Clusters drawn at draft step t = 0..K-1 under DynaSpec's position-aware
+    budget (DynaSpec summary, § Method 3): kmax for t in {0, 1} and
+    floor(kmax / ((t + 1) * 2)) for t >= 2, as printed, with at least one
+    cluster, since an empty shortlist would leave the drafter nothing to
+    propose.  Input generation only: the library never evaluates it."""
+    return [kmax if t < 2 else max(1, kmax // ((t + 1) * 2)) for t in range(K)]
+
+
 def shortlist_per_position(B: int = 64, K: int = 6, V: int = 262144, n_clusters: int = 64, budget=None,
                            dtype=torch.bfloat16, T: float = 1.0, sigma: float = 0.5, seed: int = 7,
                            device="cpu") -> dict:
@@ -234,7 +243,7 @@ def shortlist_per_position(B: int = 64, K: int = 6, V: int = 262144, n_clusters:
     length (row (b, t) holds len[t] entries); drafted tokens from the draft
     softmax on the list."""
     if budget is None:
-        budget = [8 if t < 2 else max(1, 8 // ((t + 1) * 2)) for t in range(K)]
+        budget = dynaspec_budget(8, K)
     g = _gen(seed, device)
     target = zipf_logits(B * (K + 1), V, g, device).reshape(B, K + 1, V).to(dtype)
     size = V // n_clusters

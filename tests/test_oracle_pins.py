@@ -104,9 +104,18 @@ def test_philox_matches_triton_interpreter():
 
 
 def test_uniform24_range():
+    """(n + 1/2) 2^-24 with n = w >> 8: the odd multiples of 2^-25 in (0, 1),
+    exact in float64.  A float32 holds it only for n < 2^23 (it needs 25
+    significant bits above that)."""
     assert oracle.uniform24(0) == 2.0 ** -25
     assert oracle.uniform24(0xFFFFFFFF) == 1.0 - 2.0 ** -25
     assert np.float32(oracle.uniform24(0x12345678)) == oracle.uniform24(0x12345678)
+    for w in (0x80000000, 0x80000100, 0xC0FFEE00, 0xFFFFFF00):
+        u = oracle.uniform24(w)
+        n = w >> 8
+        assert n >= 2 ** 23
+        assert u * 2.0 ** 25 == 2 * n + 1                # exact in float64
+        assert float(np.float32(u)) != u                 # one bit too many for float32
 
 
 # ------------------------------------------------------------------ worked example
