@@ -177,8 +177,10 @@ spec_status_t spec_verify_shortlist_pos(const void *target_logits, spec_dtype_t 
  *   spec_verify serves it.
  *   Overlapping calls race: all calls on a device share the scratch, so they
  *   must be ordered on the GPU (one stream, or events between streams).
- *   The first call on each device looks up the scratch address with a CUDA
- *   runtime call; make that first call outside any stream capture.          */
+ *   Every call looks up the scratch's device address with a CUDA runtime
+ *   call (a host-side lookup, not a stream operation), so the address stays
+ *   right after a cudaDeviceReset.  The first call on a device also loads the
+ *   library's kernels there; make that first call outside any stream capture. */
 spec_status_t spec_verify_static(const void *target_logits, spec_dtype_t tdt, const void *draft_logits,
                                  const int32_t *draft_tokens, int B, int K, int V, float T, uint64_t seed,
                                  int32_t *out_tokens, int32_t *out_accept_len, const spec_aux_t *aux,

@@ -131,10 +131,6 @@ bool debug_enabled()
 // Co-resident clusters for (kernel, cluster size, shared memory), per device.
 std::map<std::tuple<int, int, int, uint32_t>, int> g_max_clusters;
 
-// Address of the static scratch of spec_verify_static, looked up once per
-// device (with that device current) on its first call there.
-uint32_t *g_static_scratch[kMaxDevices] = {};
-
 uint32_t spin_limit()
 {
     const char *s = std::getenv("SPECVERIFY_SPIN_LIMIT");
@@ -285,6 +281,7 @@ spec_status_t run_rows(bool greedy, const void *target, spec_dtype_t tdt, const 
         P.aux_lse = aux->row_lse;
         P.aux_status = aux->device_status;
     }
+    P.ctl = reinterpret_cast<uint32_t *>(w + L.ctl);
     P.stat = reinterpret_cast<sv::VrStat *>(w + L.vr_stat);
     P.pair = reinterpret_cast<uint32_t *>(w + L.vr_pair);
     P.rej = reinterpret_cast<uint32_t *>(w + L.vr_rej);
@@ -472,7 +469,8 @@ spec_status_t run(int mode, const void *target, spec_dtype_t tdt, const void *dr
     if (mode == sv::MODE_GREEDY || (mode == sv::MODE_STOCH && !probs)) {
         const bool full = aux && (aux->q_draft || aux->p_draft || aux->row_lse);
         const KernelChoice kc = kernel_choice();
-        if (kc == KC_ROWS) {
+        // greedy: every target row's argmax in one launch (any batch, any row alignment)
+        if (kc == KC_ROWS || (kc == KC_AUTO && mode == sv::MODE_GREEDY)) {
             const spec_status_t rs = run_rows(mode == sv::MODE_GREEDY, target, tdt, draft, tokens, B, K, V, T, seed,
                                               out_tokens, out_len, workspace, L, aux, stream);
             if (rs != SPEC_ERR_UNSUPPORTED)
@@ -701,20 +699,12 @@ spec_status_t spec_verify_static(const void *target_logits, spec_dtype_t tdt, co
                                     tdt == SPEC_BF16 ? 1 : 0, false, &entry, &occ);
     if (st != SPEC_OK)
         return st;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return SPEC_ERR_CUDA;
+    // the scratch's device address on the current device, looked up on every
+    // call: a host-side lookup, no stream operation, and never stale (a
+    // cudaDeviceReset reloads the module at another address)
     uint32_t *ctl = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        if (!g_static_scratch[dev]) {
-            uint32_t *p = nullptr;
-            if (sv::static_scratch_address(&p) != cudaSuccess || !p)
-                return SPEC_ERR_CUDA;
-            g_static_scratch[dev] = p;
-        }
-        ctl = g_static_scratch[dev];
-    }
+    if (sv::static_scratch_address(&ctl) != cudaSuccess || !ctl)
+        return SPEC_ERR_CUDA;
     return run_cluster(greedy, target_logits, tdt, draft_logits, draft_tokens, B, K, V, T, seed, out_tokens,
                        out_accept_len, ctl, aux, stream, true);
 }

@@ -282,9 +282,7 @@ __global__ void __launch_bounds__(DT) draft_sample_kernel(const __grid_constant_
     }
     const DF incl = df_add(wpre, wincl), excl = df_add(wpre, wexcl);
     const uint4 wd = philox10((uint32_t)i, (uint32_t)b, 1u, 0u, P.key0, P.key1);
-    const float v = ((float)(wd.x >> 8) + 0.5f) * (1.0f / 16777216.0f);
-    const float th = v * total.hi;
-    const DF thr = df_add(DF{th, fmaf(v, total.hi, -th)}, DF{v * total.lo, 0.0f});
+    const DF thr = u24_scale(wd.x, total);   // v R
     if (df_gt(incl, thr) && !df_gt(excl, thr)) {
         // this thread's run holds the crossing: walk it with the same sums
         DF G = excl;

@@ -151,8 +151,7 @@ __device__ __forceinline__ int vr_decide(const RowsParams &P, int b, int i, int 
     // log2(q(d) / p(d)) = (zt - zd) c - (Mt - Md) - (log2 St - log2 Sd)
     const float X = (zt - zd) * P.c - ((t.m - d.m) + ((float)(et - ed) + (ft - fd)));
     const uint4 w = philox10((uint32_t)i, (uint32_t)b, 0u, 0u, P.key0, P.key1);
-    const float u = ((float)(w.x >> 8) + 0.5f) * (1.0f / 16777216.0f);
-    accept = X >= 0.0f || u < ex2a(X);
+    accept = X >= 0.0f || u24_below(w.x, ex2a(X));
     return 0;
 }
 
@@ -1379,9 +1378,7 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
             wexc = DF{0.0f, 0.0f};
         const DF incl = df_add(useq ? pq : pr, winc), excl = df_add(useq ? pq : pr, wexc);
         const uint4 wd = philox10((uint32_t)j, (uint32_t)b, 0u, 0u, P.key0, P.key1);
-        const float v = ((float)(wd.y >> 8) + 0.5f) * (1.0f / 16777216.0f);
-        const float th = v * F.hi;
-        const DF thr = df_add(DF{th, fmaf(v, F.hi, -th)}, DF{v * F.lo, 0.0f});
+        const DF thr = u24_scale(wd.y, F);   // v R
         if (df_gt(incl, thr) && !df_gt(excl, thr)) {
             DF G = excl;
             if (cached) {
@@ -1685,6 +1682,8 @@ int rows_chunks() { return VR_NCH; }
 int rows_segment_tokens() { return VSEG; }
 cudaError_t launch_rows(const RowsParams &P, int tdt, cudaStream_t stream, int *launches)
 {
+    if (P.greedy)
+        return launch_greedy_rows(P, tdt, stream, launches);
     int n = 0;
     if (P.aux_status) {
         cudaError_t e = cudaMemsetAsync(P.aux_status, 0, sizeof(int32_t), stream);

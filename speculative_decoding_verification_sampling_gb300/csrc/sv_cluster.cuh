@@ -132,14 +132,29 @@ __device__ __forceinline__ bool mbar_test_hint(unsigned long long *bar, uint32_t
         : "memory");
     return ok != 0;
 }
+// The same test without suspending: one poll.
+__device__ __forceinline__ bool cl_poll(unsigned long long *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(saddr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Number of hinted waits that make up a spin limit of `limit` polls.
 __device__ __forceinline__ uint32_t hinted_limit(uint32_t limit) { return (limit >> 8) + 16u; }
-// Bounded wait on a ring mbarrier: hinted try_wait sleeps the thread in
-// hardware until the phase completes (or the hint runs out).  Returns false
-// when the waits allowed by `limit` ran out.
+// Bounded wait on one of the CTA's own mbarriers (its ring of copies, its
+// hand-offs between warps): hinted try_wait sleeps the thread in hardware
+// until the phase completes (or the hint runs out).  Returns false when the
+// waits allowed by `limit` ran out.  The bound never goes below OWN_WAIT_MIN
+// polls, so a small spin limit runs out only the waits on other CTAs, and a
+// CTA never winds down with its own copies still landing.
 __device__ __forceinline__ bool ring_wait(unsigned long long *bar, uint32_t parity, uint32_t limit)
 {
-    const uint32_t lim = hinted_limit(limit);
+    const uint32_t lim = hinted_limit(limit > OWN_WAIT_MIN ? limit : OWN_WAIT_MIN);
     for (uint32_t it = 0;; ++it) {
         if (mbar_test_hint(bar, parity))
             return true;
@@ -161,19 +176,33 @@ __device__ __forceinline__ bool ring_wait_warp(unsigned long long *bar, uint32_t
 }
 
 // Warp-uniform bounded wait for an exchange round (records written by peers).
-// Gives up after `limit` polls, or early once another CTA has aborted.
+// Gives up after `limit` polls, or early once another CTA has aborted.  A
+// limit below CL_PLAIN_POLLS is that many plain polls (a spin limit of 1 gives
+// up unless the records are already there); above it, hinted waits.
+constexpr uint32_t CL_PLAIN_POLLS = 64;
 __device__ __forceinline__ bool cl_wait(unsigned long long *bar, uint32_t parity, uint32_t limit,
                                         const uint32_t *abortw, int lane)
 {
     bool ok = true;
     if (lane == 0) {
-        const uint32_t lim = hinted_limit(limit);
-        for (uint32_t it = 0;; ++it) {
-            if (cl_test(bar, parity))
-                break;
-            if (it >= lim || ld_vol(abortw)) {
-                ok = false;
-                break;
+        if (limit < CL_PLAIN_POLLS) {
+            for (uint32_t it = 0;; ++it) {
+                if (cl_poll(bar, parity))
+                    break;
+                if (it + 1 >= limit || ld_vol(abortw)) {
+                    ok = false;
+                    break;
+                }
+            }
+        } else {
+            const uint32_t lim = hinted_limit(limit);
+            for (uint32_t it = 0;; ++it) {
+                if (cl_test(bar, parity))
+                    break;
+                if (it >= lim || ld_vol(abortw)) {
+                    ok = false;
+                    break;
+                }
             }
         }
     }
@@ -715,6 +744,7 @@ __global__ void __launch_bounds__(CL_THREADS, 3) cluster_kernel(const __grid_con
 
     uint32_t round = 0, loads = 0;
     bool load_pending = false, abort = false;
+    int ab_b = -1;   // the sequence this CTA gave up on (an exchange wait ran out)
     int b = (int)cl_id();
     int claimed = P.B;   // rank 0's claim for the next sequence (held by thread 0)
 
@@ -894,15 +924,16 @@ __global__ void __launch_bounds__(CL_THREADS, 3) cluster_kernel(const __grid_con
                         // log2(q(d) / p(d)) = (zt - zd) c - (Mt - Md) - (log2 St - log2 Sd),
                         // the large parts cancelled before rounding
                         const float X = (zt_d - zd_d) * c - ((Mt - Md) + ((float)(et - ed) + (ft - fd)));
-                        const float u = ((float)(wph.x >> 8) + 0.5f) * (1.0f / 16777216.0f);
-                        accept = X >= 0.0f || u < ex2a(X);
+                        accept = X >= 0.0f || u24_below(wph.x, ex2a(X));
                     }
                 }
             }
 
             if (code) {
-                if (code == ST_TIMEOUT)
+                if (code == ST_TIMEOUT) {
                     abort = true;
+                    ab_b = b;
+                }
                 if (me == 0 && tid == 0) {
                     cl_error(P, b, code);
                     if (abort && claimed < P.B)
@@ -943,7 +974,6 @@ __global__ void __launch_bounds__(CL_THREADS, 3) cluster_kernel(const __grid_con
                 kc.dLhi = dl.hi;
                 kc.dLlo = dl.lo;
             }
-            const float v = ((float)(wph.y >> 8) + 0.5f) * (1.0f / 16777216.0f);
             const int gpw = (ng + CL_WARPS - 1) / CL_WARPS;
             const int g0 = min(ng, warp * gpw), g1 = min(ng, g0 + gpw);
             DF Rres{0.0f, 0.0f};
@@ -967,7 +997,15 @@ __global__ void __launch_bounds__(CL_THREADS, 3) cluster_kernel(const __grid_con
                     mbar_arrive_tx(&S.xbar[rp], rec_bytes);
                 ++round;
                 if (!got2) {
+                    // gave up on a peer's record: the sequence and rank 0's
+                    // claimed next one end in a timeout, and the grid winds down
                     abort = true;
+                    ab_b = b;
+                    if (tid == 0) {
+                        if (me == 0 && claimed < P.B)
+                            cl_error(P, claimed, ST_TIMEOUT);
+                        atomicExch(&P.ctl[CTL_CL_ABORT], 1u);
+                    }
                     break;
                 }
                 // cluster total and the CTA whose running sum crosses t = v R
@@ -982,8 +1020,7 @@ __global__ void __launch_bounds__(CL_THREADS, 3) cluster_kernel(const __grid_con
                     useq = true; // R <= 0: sample q_j itself
                     continue;
                 }
-                const float th = v * F.hi;
-                const DF t = df_add(DF{th, fmaf(v, F.hi, -th)}, DF{v * F.lo, 0.0f});
+                const DF t = u24_scale(wph.y, F);   // v R
                 int rstar = -1, rlast = -1;
                 DF pre{0.0f, 0.0f}, prelast{0.0f, 0.0f}, acc{0.0f, 0.0f};
                 for (uint32_t i = 0; i < C; ++i) {
@@ -1060,6 +1097,11 @@ __global__ void __launch_bounds__(CL_THREADS, 3) cluster_kernel(const __grid_con
     __syncthreads();
     cl_sync();
     if (tid == 0) {
+        // a CTA that gave up marks its sequence after the cluster barrier, so
+        // its error comes after anything rank 0 wrote for it (a peer may have
+        // finished the sequence without the part this CTA did not do)
+        if (ab_b >= 0)
+            cl_error(P, ab_b, ST_TIMEOUT);
         if (abort)
             cl_status(P, ST_TIMEOUT);
         __threadfence();

@@ -49,6 +49,10 @@ constexpr int RS = 3;                        // ring stages per worker
 constexpr int SB = 4096;                     // bytes per stage
 constexpr int SEG = 256;                     // tokens per segment
 constexpr uint32_t DRAIN_LIMIT = 1u << 24;   // polls while waiting for our own bulk copies
+// Floor of the bound on waits for a CTA's own barriers (its copies, its
+// hand-offs between warps): the spin limit lowers only the waits on other
+// CTAs, so a small limit exercises those and never leaves copies in flight.
+constexpr uint32_t OWN_WAIT_MIN = 1u << 20;
 #define F_INF __int_as_float(0x7f800000)
 
 enum Kind { K_NONE = 0, K_STAT_T = 1, K_STAT_D = 2, K_RES = 3 };
@@ -333,6 +337,24 @@ __device__ __forceinline__ uint4 philox10(uint32_t c0, uint32_t c1, uint32_t c2,
 __device__ __forceinline__ double uniform24(uint32_t w)
 {
     return ((double)(w >> 8) + 0.5) * (1.0 / 16777216.0);
+}
+// The same uniform (2n + 1) 2^-25, n = w >> 8, in float32 arithmetic.  It has
+// 25 significant bits, one more than a float holds, so it is never rounded to
+// a float; instead:
+//  - u24_below(w, a): whether it is below a in [0, 1], decided exactly:
+//    2n + 1 < a 2^25 holds for the integer 2n + 1 iff it is below ceil(a 2^25)
+//    (a 2^25 is an exact scaling, and its ceiling an exact conversion);
+//  - u24_scale(w, F): its product with the float pair F, as a float pair, from
+//    the exact parts n 2^-24 and 2^-25 (the rounding of the pair alone).
+__device__ __forceinline__ bool u24_below(uint32_t w, float a)
+{
+    return (w >> 8) * 2u + 1u < __float2uint_ru(a * 33554432.0f);
+}
+__device__ __forceinline__ DF u24_scale(uint32_t w, DF F)
+{
+    const float vh = (float)(w >> 8) * (1.0f / 16777216.0f);
+    const float th = vh * F.hi;
+    return df_add(DF{th, fmaf(vh, F.hi, -th)}, DF{fmaf(vh, F.lo, F.hi * (1.0f / 33554432.0f)), 0.0f});
 }
 
 // ------------------------------------------------------------------ element types
@@ -1561,7 +1583,7 @@ __device__ void worker(const Params &P, WorkerShared &ws, uint8_t *ring, int wid
         }
         idle = 0;
         const int s = (int)(consumed % RS);
-        if (!warp_wait(&ws.full[s], (consumed / RS) & 1u, P.spin_limit, nullptr, lane)) {
+        if (!warp_wait(&ws.full[s], (consumed / RS) & 1u, max(P.spin_limit, OWN_WAIT_MIN), nullptr, lane)) {
             ok = false;
             break;
         }

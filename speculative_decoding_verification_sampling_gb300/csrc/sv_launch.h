@@ -43,6 +43,9 @@ int rows_chunks();
 int rows_segment_tokens();
 // *launches: the kernels the call launched
 cudaError_t launch_rows(const RowsParams &P, int tdt, cudaStream_t stream, int *launches);
+// Greedy verification in one launch (k_greedy_rows.cu): the argmax of every
+// target row in parts; the last row of a sequence walks the rule.
+cudaError_t launch_greedy_rows(const RowsParams &P, int tdt, cudaStream_t stream, int *launches);
 
 // KV-cache commit after verification (k_kv.cu): copy, then the length update.
 cudaError_t launch_kv_commit(void *cache, const void *staged, int NL, int B, int K, int L, long long W,

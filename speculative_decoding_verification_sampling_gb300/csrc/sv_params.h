@@ -151,7 +151,8 @@ constexpr int SW_WARPS = 8;   // consumer warps per CTA
 // bit 1 sample q_j itself (the residual mass was 0).
 struct alignas(16) SwRes {
     int b, j, flags, pad;
-    float Mt, dLhi, dLlo, v;       // residual coefficients and the sampling uniform
+    float Mt, dLhi, dLlo;          // residual coefficients
+    uint32_t vw;                   // the Philox word of the sampling uniform
     float St_hi, St_lo, R_hi, R_lo;   // target sum (to report R), residual mass of an earlier attempt
 };
 constexpr uint32_t SW_READY = 0x80000000u;   // sw_cnt bit: merged statistics written

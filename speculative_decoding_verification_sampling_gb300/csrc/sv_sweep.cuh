@@ -134,7 +134,7 @@ __device__ __forceinline__ SwRes ld_res(const SwRes *p)
     const int4 a = __ldcg(reinterpret_cast<const int4 *>(p));
     const float4 q = __ldcg(reinterpret_cast<const float4 *>(p) + 1);
     const float4 r = __ldcg(reinterpret_cast<const float4 *>(p) + 2);
-    return SwRes{a.x, a.y, a.z, a.w, q.x, q.y, q.z, q.w, r.x, r.y, r.z, r.w};
+    return SwRes{a.x, a.y, a.z, a.w, q.x, q.y, q.z, __float_as_uint(q.w), r.x, r.y, r.z, r.w};
 }
 __device__ __forceinline__ uint32_t ld_acq(const uint32_t *p)
 {
@@ -220,8 +220,7 @@ __device__ __forceinline__ int sw_decide(const SweepParams &P, int b, int f, boo
     // log2(q(d) / p(d)) = (zt - zd) c - (Mt - Md) - (log2 St - log2 Sd)
     const float X = (zt - zd) * P.c - ((s.mt - s.md) + ((float)(et - ed) + (ft - fd)));
     const uint4 w = philox10((uint32_t)f, (uint32_t)b, 0u, 0u, P.key0, P.key1);
-    const float u = ((float)(w.x >> 8) + 0.5f) * (1.0f / 16777216.0f);
-    accept = X >= 0.0f || u < ex2a(X);
+    accept = X >= 0.0f || u24_below(w.x, ex2a(X));
     return 0;
 }
 
@@ -250,7 +249,7 @@ __device__ void sw_post(const SweepParams &P, int b, int j, int flags, DF Rprev)
         r.dLlo = dl.lo;
     }
     const uint4 w = philox10((uint32_t)j, (uint32_t)b, 0u, 0u, P.key0, P.key1);
-    r.v = ((float)(w.y >> 8) + 0.5f) * (1.0f / 16777216.0f);
+    r.vw = w.y;
     r.St_hi = s.st_hi;
     r.St_lo = s.st_lo;
     r.R_hi = Rprev.hi;
@@ -363,8 +362,7 @@ __device__ void sw_locate(const SweepParams &P, int e, uint8_t *loc, DF2 *mass, 
         return;
     }
     const DF R = (!useq || bonus) ? F : DF{r.R_hi, r.R_lo};
-    const float th = r.v * F.hi;
-    const DF t = df_add(DF{th, fmaf(r.v, F.hi, -th)}, DF{r.v * F.lo, 0.0f});
+    const DF t = u24_scale(r.vw, F);
     // the crossing chunk: first lane whose running sum exceeds t, then inside its block
     int chunk = -1;
     DF Gc{0.0f, 0.0f};

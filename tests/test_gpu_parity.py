@@ -154,15 +154,96 @@ def test_throughput_points_full(B, K):
     assert_parity(t, l, _oracle(cfg, 77), f"throughput B={B} K={K}")
 
 
+# inputs and oracle results of the large cases, made once for every kernel
+_CACHE = {}
+
+
+def _cached(key, make):
+    if key not in _CACHE:
+        _CACHE[key] = make()
+    return _CACHE[key]
+
+
 @pytest.mark.parametrize("B,K", [(256, 4), (512, 8)])
-def test_throughput_points_sampled(B, K):
-    """Full-size launch; the oracle checks a sample of the sequences."""
-    cfg = synth.throughput(B=B, K=K, seed=B + K)
+def test_throughput_points_full_size(B, K):
+    """The headline sizes, every sequence checked against the oracle."""
+    cfg = _cached(("tp", B, K), lambda: synth.throughput(B=B, K=K, seed=B + K))
+    ref = _cached(("tp-ref", B, K), lambda: _oracle(cfg, 99))
     t, l = _gpu_run(cfg, 99)
-    idx = np.arange(0, B, 8)
-    ref = _oracle(cfg, 99, idx=idx)
-    assert_parity(t[idx], l[idx], ref, f"throughput B={B} K={K} (sampled)")
+    assert_parity(t, l, ref, f"throughput B={B} K={K}")
     assert ((l >= 0) & (l <= K)).all()
+
+
+def _sparse_rows(B, K, V, seed):
+    """Target and draft rows that are -inf except on a few tokens (down to a
+    single one), with drafted tokens on the draft's support, off it (p(d) = 0:
+    accepted), and where the target is -inf (q(d) = 0)."""
+    g = torch.Generator().manual_seed(seed)
+    tgt = torch.full((B, K + 1, V), -math.inf)
+    drf = torch.full((B, K, V), -math.inf)
+    tok = torch.zeros((B, K), dtype=torch.int32)
+    sizes = [1, 1, 2, 3, 5, 40, 300]
+    for b in range(B):
+        for i in range(K + 1):
+            n = sizes[(b + i) % len(sizes)]
+            sup = torch.randperm(V, generator=g)[:n]
+            tgt[b, i, sup] = 2.0 * torch.randn(n, generator=g)
+            if i == K:
+                continue
+            kind = (b * 7 + i) % 5
+            if kind == 1:      # a single token, most likely off the target's support
+                dsup = torch.randperm(V, generator=g)[:1]
+            elif kind == 2:    # part of the target's support
+                dsup = sup[:max(1, n // 2)]
+            elif kind == 3:    # the target's support and a few tokens more
+                dsup = torch.cat([sup, torch.randperm(V, generator=g)[:3]])
+            elif kind == 4:    # somewhere else
+                dsup = torch.randperm(V, generator=g)[:sizes[(b + 2 * i) % len(sizes)]]
+            else:              # the target's support
+                dsup = sup
+            vals = torch.where(torch.isfinite(tgt[b, i, dsup]), tgt[b, i, dsup], torch.zeros(len(dsup)))
+            drf[b, i, dsup] = vals + 0.5 * torch.randn(len(dsup), generator=g)
+            both = torch.nonzero(torch.isfinite(drf[b, i]) & torch.isfinite(tgt[b, i]))[:, 0]
+            fin = both if len(both) else torch.nonzero(torch.isfinite(drf[b, i]))[:, 0]
+            pick = int(fin[torch.randint(len(fin), (1,), generator=g)])
+            if (b + i) % 6 == 5:   # off the draft's support: p(d) = 0, accepted
+                pick = int(torch.randint(V, (1,), generator=g))
+            tok[b, i] = pick
+    return dict(target=tgt.to(torch.bfloat16), draft=drf.to(torch.bfloat16), draft_tokens=tok, T=1.0)
+
+
+@pytest.mark.parametrize("B,K,V", [(32, 4, 65536), (6, 3, 4096)])
+def test_mostly_minus_inf_rows(B, K, V):
+    cfg = _cached(("sparse", B, K, V), lambda: _sparse_rows(B, K, V, seed=B + V))
+    for seed in (1, 2, 3):
+        ref = _oracle(cfg, seed)
+        assert (ref["accept_len"] >= 0).all()
+        t, l = _gpu_run(cfg, seed)
+        assert_parity(t, l, ref, f"mostly -inf rows B={B} V={V} seed={seed}")
+
+
+def test_shortlist_config_full_vocabulary_form():
+    """The shortlisted-draft workload in the form the DynaSpec summary states
+    (§ Abstract: the drafter works on the shortlist, verification keeps the
+    full vocabulary): B=64, K=6, V=262144, the draft a full-vocabulary row that
+    is -inf off each sequence's 32,768-token shortlist.  spec_verify on that
+    form matches the oracle and the compact spec_verify_shortlist call."""
+    cfg = _cached("sl", synth.shortlist)
+    B, K, V = cfg["B"], cfg["K"], cfg["V"]
+
+    def full_form():
+        full = torch.full((B, K, V), -math.inf, dtype=torch.bfloat16)
+        full.scatter_(2, cfg["shortlist"].long().unsqueeze(1).expand(B, K, -1), cfg["draft"])
+        return dict(target=cfg["target"], draft=full, draft_tokens=cfg["draft_tokens"], T=cfg["T"])
+
+    fcfg = _cached("sl-full", full_form)
+    ref = _cached("sl-full-ref", lambda: _oracle(fcfg, 21))
+    t, l = _gpu_run(fcfg, 21)
+    assert_parity(t, l, ref, "shortlist workload, full-vocabulary draft")
+    ct, cl = _gpu_run(cfg, 21)
+    assert_parity(ct, cl, ref, "shortlist workload, compact draft")
+    np.testing.assert_array_equal(l, cl)
+    np.testing.assert_array_equal(t, ct)
 
 
 @pytest.mark.parametrize("B,K,V,dtype,T", [
@@ -324,6 +405,26 @@ def test_deterministic_and_workspace_left_zeroed():
     for t, l in outs[1:]:
         np.testing.assert_array_equal(t, outs[0][0])
         np.testing.assert_array_equal(l, outs[0][1])
+
+
+def test_greedy_workspace_reused_across_batches():
+    """Greedy calls on one workspace, alternating two batches: each matches the
+    oracle, so every counter a call uses is back at zero for the next."""
+    B, K, V = 48, 5, 20000
+    cfgs = [synth.greedy(B=B, K=K, V=V, seed=s) for s in (41, 42)]
+    refs = [_oracle(c, 0) for c in cfgs]
+    ws = torch.zeros(sv.spec_workspace_bytes(B, K, V), dtype=torch.uint8, device=DEV)
+    dev = [_to(c) for c in cfgs]
+    for call in range(4):
+        d, ref = dev[call % 2], refs[call % 2]
+        st = torch.full((1,), -1, dtype=torch.int32, device=DEV)
+        t, l = sv.spec_verify_greedy(d["target"], d["draft_tokens"], workspace=ws,
+                                     aux=sv.Aux(device_status=st))
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(l.cpu().numpy(), ref["accept_len"])
+        np.testing.assert_array_equal(t.cpu().numpy(), ref["tokens"])
+        assert int(st.cpu()[0]) == 0
+        assert int(ws[:256].count_nonzero()) == 0
 
 
 def test_gpu_output_distribution_chi_square():

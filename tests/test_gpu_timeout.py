@@ -1,16 +1,21 @@
-"""The timeout path of the row-parallel statistics stream, made to run out
-without a GPU fault.
+"""Timeout paths of the kernels, made to run out without a GPU fault.
 
-With the spin limit at 1, the stream's producers give up at once on their
-waits on other CTAs: for every sequence to have ended, and for a posted
-residual job to be written. A producer that gives up sets the timeout word,
-stops claiming work and still closes its ring, so the CTA drains every copy it
-issued before it exits. Waits on the CTA's own barriers keep a floor that
-the spin limit does not lower.
+Every wait on another CTA is bounded by the spin limit (SPECVERIFY_SPIN_LIMIT);
+waits on a CTA's own barriers (its copies, its hand-offs between warps) keep a
+floor that the limit does not lower, so a CTA never winds down with its own
+copies still landing.  At a spin limit of 1 the waits on other CTAs give up at
+once unless what they wait for is already there:
 
-The call must report SPEC_ERR_TIMEOUT (7) for every sequence and in the
-device status. The next call, at the default limit, must give the oracle's
-results: the context is usable and the call's counters were left zeroed.
+- the row-parallel statistics stream: its producers' wait for every sequence
+  to have ended, and for a posted residual job to be written;
+- the cluster kernel: the exchange of per-CTA records inside a cluster;
+- the chunk-scheduled kernel: an idle worker's wait for its residual slot.
+
+A sequence whose outputs were not finished reports SPEC_ERR_TIMEOUT (7) with
+every token -1; the others must still be the oracle's.  The device status is
+7 exactly when a sequence timed out.  The next call, at the default limit, must
+give the oracle's results with status 0: the context is usable and the call's
+control words were left zeroed.
 """
 from __future__ import annotations
 
@@ -28,16 +33,14 @@ from speculative_decoding_verification_sampling_gb300 import synth
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 TIMEOUT = 7
+KEYS = ("SPECVERIFY_KERNEL", "SPECVERIFY_ROWS_FUSED", "SPECVERIFY_SPIN_LIMIT")
 
 
 @pytest.fixture(autouse=True)
 def _env():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    keys = ("SPECVERIFY_KERNEL", "SPECVERIFY_ROWS_FUSED", "SPECVERIFY_SPIN_LIMIT")
-    saved = {k: os.environ.get(k) for k in keys}
-    os.environ["SPECVERIFY_KERNEL"] = "rows"
-    os.environ["SPECVERIFY_ROWS_FUSED"] = "1"
+    saved = {k: os.environ.get(k) for k in KEYS}
     yield
     for k, v in saved.items():
         if v is None:
@@ -53,19 +56,53 @@ def _run(cfg, seed, aux=None):
     return t.cpu().numpy(), l.cpu().numpy()
 
 
-@pytest.mark.parametrize("B,K", [(64, 4), (256, 4)])
-def test_stream_waits_run_out_then_recover(B, K):
-    cfg = synth.throughput(B=B, K=K, seed=B + 7)
+def check_gave_up(t, l, status, ref, what):
+    """Sequences that timed out carry -7 and -1 tokens; the rest are the
+    oracle's; the status is 7 exactly when one timed out."""
+    out = l == -TIMEOUT
+    assert (t[out] == -1).all(), what
+    assert status == (TIMEOUT if out.any() else 0), (what, status, int(out.sum()))
+    keep = ~out
+    if keep.any():
+        sub = {k: v[keep] for k, v in ref.items()}
+        assert_parity(t[keep], l[keep], sub, what)
+    return int(out.sum())
+
+
+def run_out_then_recover(cfg, seed, what, must_time_out=True, all_out=False):
+    ref = oracle.verify(cfg["target"], cfg["draft"], cfg["draft_tokens"], cfg["T"], seed)
     os.environ["SPECVERIFY_SPIN_LIMIT"] = "1"
     aux = sv.Aux(device_status=torch.zeros(1, dtype=torch.int32, device=DEV))
-    t, l = _run(cfg, 5, aux=aux)
-    assert int(aux.device_status.cpu()[0]) == TIMEOUT
-    assert (l == -TIMEOUT).all()
-    assert (t == -1).all()
-
+    t, l = _run(cfg, seed, aux=aux)
+    n = check_gave_up(t, l, int(aux.device_status.cpu()[0]), ref, what + " (spin limit 1)")
+    if must_time_out:
+        assert n > 0, f"{what}: no wait ran out at spin limit 1"
+    if all_out:
+        assert n == len(l), f"{what}: {n} of {len(l)} sequences timed out"
     os.environ.pop("SPECVERIFY_SPIN_LIMIT")
     aux = sv.Aux(device_status=torch.full((1,), -1, dtype=torch.int32, device=DEV))
-    t, l = _run(cfg, 5, aux=aux)
+    t, l = _run(cfg, seed, aux=aux)
     assert int(aux.device_status.cpu()[0]) == 0
-    assert_parity(t, l, oracle.verify(cfg["target"], cfg["draft"], cfg["draft_tokens"], cfg["T"], 5),
-                  f"after a timeout, B={B} K={K}")
+    assert_parity(t, l, ref, f"{what}, after a timeout")
+
+
+@pytest.mark.parametrize("B,K", [(64, 4), (256, 4)])
+def test_stream_waits_run_out_then_recover(B, K):
+    """The stream's producers give up at once: every sequence reports 7."""
+    os.environ["SPECVERIFY_KERNEL"] = "rows"
+    os.environ["SPECVERIFY_ROWS_FUSED"] = "1"
+    run_out_then_recover(synth.throughput(B=B, K=K, seed=B + 7), 5, f"stream B={B} K={K}", all_out=True)
+
+
+@pytest.mark.parametrize("B,K,V", [(24, 4, 128256), (16, 3, 8192)])
+def test_cluster_exchange_waits_run_out_then_recover(B, K, V):
+    os.environ["SPECVERIFY_KERNEL"] = "cluster"
+    cfg = synth.stochastic_gaussian(B, K, V, torch.bfloat16, 1.0, 2.0, 0.5, seed=B + V)
+    run_out_then_recover(cfg, 8, f"cluster B={B} K={K} V={V}")
+
+
+@pytest.mark.parametrize("B,K,V", [(48, 4, 16384), (8, 5, 3000)])
+def test_general_kernel_waits_run_out_then_recover(B, K, V):
+    os.environ["SPECVERIFY_KERNEL"] = "general"
+    cfg = synth.stochastic_gaussian(B, K, V, torch.bfloat16, 1.0, 2.0, 0.5, seed=B + V)
+    run_out_then_recover(cfg, 9, f"chunk-scheduled B={B} K={K} V={V}")
