@@ -458,6 +458,10 @@ def run_gb300(args) -> int:
         line["clocks"] = summarize_clocks(clock_samples)
         line["emitted_tokens_per_s"] = world * float(ref_l.double().add(1).sum()) * args.steps / (elapsed_ms / 1e3)
         line["mean_accept_len"] = mean_len
+        if world == 1 and args.configs:
+            del sets, outs
+            torch.cuda.empty_cache()
+            line["configs"] = config_points(dev, stream)
         if world == 1:
             rate, cores, passes, n, el = oracle_rate(cfg, K, args.cpu_seconds)
             line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -469,6 +473,139 @@ def run_gb300(args) -> int:
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+# --------------------------------------------------------------------------
+# every configuration of the benchmark table, timed call by call
+# --------------------------------------------------------------------------
+def _rule_rows(accept_len, K: int, greedy: bool) -> int:
+    """Rows the left-to-right rule reads: stochastic as `needed_rows`; greedy
+    reads target rows 0..j (all K + 1 when every draft matches)."""
+    if not greedy:
+        return needed_rows(accept_len, K)
+    return sum(min(int(L), K) + 1 for L in accept_len)
+
+
+def config_points(dev, stream, calls: int = 40):
+    """One record per configuration of the benchmark table (small fp32, greedy,
+    Zipf at three draft noises, the shortlisted draft in both layouts, the
+    throughput sweep, draft probabilities).  Inputs are made on the device from
+    seeded generators; each call is timed alone with CUDA events on the
+    launching stream, after a read of 256 MB that evicts the L2 (the smaller
+    configurations fit in it).  Bytes: the logits the left-to-right rule reads
+    (`rule_bytes`) and every logit row (`all_rows_bytes`)."""
+    import torch
+    import speculative_decoding_verification_sampling_gb300 as sv
+    from speculative_decoding_verification_sampling_gb300 import synth
+    peak, src = hbm_peak()
+    flush = torch.zeros((2048, 32768), dtype=torch.int32, device=dev)   # 256 MB
+    fmax = torch.empty(32768, dtype=torch.int32, device=dev)
+    out = []
+    errors = []
+
+    def timed(fn):
+        # the inputs were made on the default stream: the calls come after them
+        stream.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                r = fn()
+            stream.synchronize()
+            es = [torch.cuda.Event(enable_timing=True) for _ in range(calls)]
+            ee = [torch.cuda.Event(enable_timing=True) for _ in range(calls)]
+            for n in range(calls):
+                # a read of 256 MB evicts the L2 and leaves no dirty lines behind
+                torch.amax(flush, dim=0, out=fmax)
+                es[n].record(stream)
+                r = fn()
+                ee[n].record(stream)
+            stream.synchronize()
+        return statistics.fmean(a.elapsed_time(b) for a, b in zip(es, ee)) * 1e3, r
+
+    def record(name, cfg, us, res, elem_bytes, greedy=False, extra_bytes=0, all_rows=None, units=None):
+        B, K, V = cfg["B"], cfg["K"], cfg["V"]
+        acc = res[1].cpu().tolist()
+        bad = [L for L in acc if L < 0]
+        if bad:
+            # a data error on valid inputs is a fault of the library: report it
+            # with the record (the bytes count only the sequences without one)
+            errors.append({"workload": name, "sequences": len(bad), "codes": sorted(set(-L for L in bad))})
+            acc = [L for L in acc if L >= 0] or [0]
+        row_bytes = V * elem_bytes
+        rule = _rule_rows(acc, K, greedy) * row_bytes + extra_bytes
+        allb = all_rows if all_rows is not None else ((K + 1) if greedy else (2 * K + 1)) * B * row_bytes
+        n_units = units if units is not None else B * K
+        examined = sum(min(int(L) + 1, K) for L in acc)
+        rec = {"workload": name, "B": B, "K": K, "V": V, "us_per_call": us,
+               "value": n_units / (us * 1e-6), "unit": "positions/s",
+               "mean_accept_len": statistics.fmean(acc), "accept_rate": sum(acc) / max(1, examined),
+               "rule_bytes": rule, "all_rows_bytes": allb,
+               "roofline": {"bound": "hbm", "achieved": rule / us / 1e3, "peak": peak, "unit": "GB/s",
+                            "frac": rule / us / 1e3 / peak, "peak_source": src,
+                            "all_rows_gbs": allb / us / 1e3}}
+        out.append(rec)
+        return rec
+
+    T1 = TEMPERATURE
+    # 1. B=1 K=4 V=32000 fp32
+    c = synth.small_stochastic(seed=0, device=dev)
+    t, d, k = c["target"], c["draft"], c["draft_tokens"]
+    us, r = timed(lambda: sv.spec_verify(t, d, k, 1.0, VERIFY_SEED, stream=stream))
+    record("small: B=1 K=4 V=32000 fp32 T=1, target N(0, 2^2), draft = target + N(0, 0.5^2)", c, us, r, 4)
+    # 2. greedy B=64 K=5 V=128256 bf16
+    c = synth.greedy(device=dev)
+    t, k = c["target"], c["draft_tokens"]
+    us, r = timed(lambda: sv.spec_verify_greedy(t, k, stream=stream))
+    record("greedy: B=64 K=5 V=128256 bf16 T=0, target N(0, 3^2), drafts = argmax with probability 0.8",
+           c, us, r, 2, greedy=True)
+    # 3. Zipf B=32 K=7 V=152064 bf16 T=0.7 at three draft noises
+    for sigma in (0.25, 0.5, 1.0):
+        c = synth.zipf(sigma=sigma, device=dev)
+        t, d, k = c["target"], c["draft"], c["draft_tokens"]
+        us, r = timed(lambda: sv.spec_verify(t, d, k, c["T"], VERIFY_SEED, stream=stream))
+        rec = record(f"zipf: B=32 K=7 V=152064 bf16 T=0.7, draft = target + N(0, {sigma}^2)", c, us, r, 2)
+        rec["sigma"] = sigma
+    # 4. shortlisted draft, B=64 K=6 V=262144, 32768-token per-sequence lists
+    c = synth.shortlist(device=dev)
+    Bs, Ks, Vs = c["B"], c["K"], c["V"]
+    S = c["shortlist"].shape[1]
+    t, d, sl, k = c["target"], c["draft"], c["shortlist"], c["draft_tokens"]
+    us, r = timed(lambda: sv.spec_verify_shortlist(t, d, sl, k, 1.0, VERIFY_SEED, stream=stream))
+    acc = r[1].cpu().tolist()
+    # rule bytes: target rows 0..j at V, draft rows 0..min(j, K-1) at S, and the sequence's list once
+    need = sum((min(int(L), Ks) + 1) * Vs * 2 + min(int(L) + 1, Ks) * S * 2 for L in acc) + Bs * S * 4
+    rec = record("shortlist (compact): B=64 K=6 V=262144 bf16 T=1, Zipf target, 8 of 64 clusters per sequence "
+                 "(S=32768), draft = target + N(0, 0.5^2) on the list", c, us, r, 2,
+                 all_rows=Bs * (Ks + 1) * Vs * 2 + Bs * Ks * S * 2 + Bs * S * 4)
+    rec["rule_bytes"] = need
+    rec["roofline"].update(achieved=need / us / 1e3, frac=need / us / 1e3 / peak)
+    full = torch.full((Bs, Ks, Vs), float("-inf"), dtype=torch.bfloat16, device=dev)
+    full.scatter_(2, sl.long().unsqueeze(1).expand(Bs, Ks, S), d)
+    us, r = timed(lambda: sv.spec_verify(t, full, k, 1.0, VERIFY_SEED, stream=stream))
+    record("shortlist (full-vocabulary draft, -inf off the list): B=64 K=6 V=262144 bf16 T=1", c, us, r, 2)
+    del full, t, d, sl, k, c
+    # 5. throughput sweep
+    for Kp in (4, 8):
+        for Bp in (1, 8, 64, 256, 512):
+            c = synth.throughput(B=Bp, K=Kp, seed=DATA_SEED, device=dev)
+            t, d, k = c["target"], c["draft"], c["draft_tokens"]
+            us, r = timed(lambda: sv.spec_verify(t, d, k, T1, VERIFY_SEED, stream=stream))
+            record(f"throughput: B={Bp} K={Kp} V=128256 bf16 T=1", c, us, r, 2)
+            del t, d, k, c
+    # draft probabilities at B=256 K=4
+    c = synth.throughput(B=256, K=4, seed=DATA_SEED, device=dev)
+    t, k = c["target"], c["draft_tokens"]
+    probs = torch.softmax(c["draft"].float(), dim=-1)
+    del c["draft"]
+    us, r = timed(lambda: sv.spec_verify(t, probs, k, T1, VERIFY_SEED, draft_is_probs=True, stream=stream))
+    acc = r[1].cpu().tolist()
+    need = sum((min(int(L), 4) + 1) * V * 2 + min(int(L) + 1, 4) * V * 4 for L in acc)
+    rec = record("draft probabilities: B=256 K=4 V=128256, bf16 target logits, fp32 draft probabilities", c, us, r,
+                 2, all_rows=256 * 5 * V * 2 + 256 * 4 * V * 4)
+    rec["rule_bytes"] = need
+    rec["roofline"].update(achieved=need / us / 1e3, frac=need / us / 1e3 / peak)
+    if errors:
+        out.append({"data_errors": errors})
+    return out
 
 
 # --------------------------------------------------------------------------
@@ -794,6 +931,8 @@ def main(argv=None) -> int:
     ap.add_argument("--k", type=int, default=4, help="drafted tokens per sequence")
     ap.add_argument("--rotate", type=int, default=4, help="device copies of the input set")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="length of the oracle sample")
+    ap.add_argument("--no-configs", dest="configs", action="store_false",
+                    help="leave out the per-configuration records (one GPU only)")
     ap.add_argument("--workload", choices=("verify",) + tuple(EXTRA_WORKLOADS), default="verify",
                     help="the verification step (default), or a further workload of the library")
     args = ap.parse_args(argv)

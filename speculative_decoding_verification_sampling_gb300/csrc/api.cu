@@ -476,9 +476,14 @@ spec_status_t run(int mode, const void *target, spec_dtype_t tdt, const void *dr
             if (rs != SPEC_ERR_UNSUPPORTED)
                 return rs;
         }
-        // stochastic calls with enough rows to fill the GPU: the row-parallel kernels
-        // (they also serve the per-position outputs)
-        if (kc == KC_AUTO && mode == sv::MODE_STOCH && (long long)B * (2 * K + 1) >= kRowsMinRows) {
+        // stochastic calls with enough rows to fill the GPU: the row-parallel
+        // kernels (they also serve the per-position outputs); and the smallest
+        // batches or long drafts, where reading every row at once beats the
+        // cluster kernel's one position at a time (B = 1, K = 4 bf16: 39 us
+        // against 53 us; B = 8, K = 8: 51 us against 64 us; B = 8, K = 4 stays
+        // with the cluster kernel, 43 us against 45 us)
+        if (kc == KC_AUTO && mode == sv::MODE_STOCH &&
+            ((long long)B * (2 * K + 1) >= kRowsMinRows || B <= 2 || K >= 6)) {
             const spec_status_t rs = run_rows(false, target, tdt, draft, tokens, B, K, V, T, seed, out_tokens,
                                               out_len, workspace, L, aux, stream);
             if (rs != SPEC_ERR_UNSUPPORTED)

@@ -559,6 +559,53 @@ __device__ __forceinline__ float xpose_sum(const float *v, int lane)
     return a;
 }
 
+// ---------------------------------------------------------------- residual coefficients
+// The coefficients of the distribution sequence b samples at its end j, from
+// the statistics t of its target row j and d of its draft row j (j < K).
+__device__ __forceinline__ ResK res_coef(const RowsParams &P, const VrStat &t, const VrStat &d, int j)
+{
+    ResK k;
+    k.Mt = t.m;
+    k.c = P.c;
+    k.dLhi = k.dLlo = 0.0f;
+    if (j < P.K) {
+        // dL = (Md - Mt) + log2 Sd - log2 St as a float pair
+        int et, ed;
+        float ft, fd;
+        log2_split(DF{t.s_hi, t.s_lo}, et, ft);
+        log2_split(DF{d.s_hi, d.s_lo}, ed, fd);
+        DF dl = two_sum(d.m, -t.m);
+        dl = df_add(dl, DF{(float)(ed - et), 0.0f});
+        dl = df_add(dl, DF{fd - ft, 0.0f});
+        k.dLhi = dl.hi;
+        k.dLlo = dl.lo;
+    }
+    return k;
+}
+// The same, loading the statistics (the draft row's only where it is used).
+__device__ __forceinline__ ResK vr_coef(const RowsParams &P, int b, int j)
+{
+    const VrStat *st = P.stat + (size_t)b * (2 * P.K + 1);
+    const VrStat t = ld_vrstat(st + j);
+    ResK k;
+    k.Mt = t.m;
+    k.c = P.c;
+    k.dLhi = k.dLlo = 0.0f;
+    if (j < P.K) {
+        const VrStat d = ld_vrstat(st + P.K + 1 + j);
+        int et, ed;
+        float ft, fd;
+        log2_split(DF{t.s_hi, t.s_lo}, et, ft);
+        log2_split(DF{d.s_hi, d.s_lo}, ed, fd);
+        DF dl = two_sum(d.m, -t.m);
+        dl = df_add(dl, DF{(float)(ed - et), 0.0f});
+        dl = df_add(dl, DF{fd - ft, 0.0f});
+        k.dLhi = dl.hi;
+        k.dLlo = dl.lo;
+    }
+    return k;
+}
+
 // ---------------------------------------------------------------- 1b. row statistics from a bulk-copy stream
 // The statistics and decisions of vr_stats for stochastic calls with aligned
 // rows and draft logits, from one persistent launch (VS_CPS CTAs per SM).
@@ -585,6 +632,7 @@ constexpr int VS_EPN = 4;         // epilogue slots
 constexpr int VS_MB = 8;          // part-merge buffers (more than VS_NS)
 constexpr int VR2_HALF = VS_STAGE / 2;   // bytes of each row in a residual stage
 constexpr int VS_T = (VS_NCW + 2) * 32;
+constexpr int VS_SMAX = 8;        // most parts per row of the stream
 
 // A stage: type 0, tokens [tok0, tok0 + ntok) of the row of part `item`;
 // type 1, a residual stage of sequence b's row pair j (target half, then draft
@@ -701,8 +749,88 @@ __device__ __forceinline__ void vs_stage(const uint4 *p, int ntok, int tid, floa
     }
 }
 
+// The statistics of a row from its n parts' records (pp[0..n)): the largest
+// reference, the sums rescaled to it (exact powers of two) and added as a
+// float pair, the flags, the drafted token's logit from the part holding it.
+__device__ __forceinline__ VrStat merge_parts(const VrStat *pp, int n)
+{
+    constexpr int MU = 4;   // records loaded at once (a few registers: the kernel keeps 3 CTAs per SM)
+    float M = -F_INF, zd = 0.0f;
+    DF S{0.0f, 0.0f};
+    int fl = 0;
+    for (int h0 = 0; h0 < n; h0 += MU) {
+        float4 a[MU];
+        float z[MU];
+#pragma unroll
+        for (int k = 0; k < MU; ++k)
+            if (h0 + k < n) {
+                a[k] = __ldcg(reinterpret_cast<const float4 *>(pp + h0 + k));
+                z[k] = __ldcg(&pp[h0 + k].zd);
+            }
+#pragma unroll
+        for (int k = 0; k < MU; ++k)
+            if (h0 + k < n) {
+                const int f = __float_as_int(a[k].w);
+                fl |= f;
+                if (f & VR_HASD)
+                    zd = z[k];
+                const float mk = a[k].x;
+                if (mk > -F_INF) {
+                    if (mk > M) {
+                        S = M > -F_INF ? df_scale_pow2(S, M - mk) : DF{0.0f, 0.0f};
+                        M = mk;
+                    }
+                    S = df_add(S, df_scale_pow2(DF{a[k].y, a[k].z}, mk - M));
+                }
+            }
+    }
+    return VrStat{M, S.hi, S.lo, fl, zd, 0, 0, 0};
+}
+
+// The epilogue of vr_stream: part `part` of the target (kind 0) or draft
+// (kind 1) row of position i of sequence b has statistics st.  One counter per
+// position counts the parts of both rows; the last part to finish merges
+// every part (one round of loads), records the two rows and decides the
+// position.  A rejection or an error sets the position's bit in rej, and the
+// per-sequence word of decided and ending positions finds the sequence's end
+// (vr_commit's way).
+__device__ __noinline__ void vs_commit(const RowsParams &P, int b, int i, int kind, int part, int dt, VrStat st)
+{
+    const int K = P.K;
+    const size_t rt = (size_t)b * (2 * K + 1) + i, rd = (size_t)b * (2 * K + 1) + K + 1 + i;
+    const int nrows = i < K ? 2 : 1;
+    VrStat t = st, d{};
+    if (P.parts > 1 || nrows > 1) {
+        P.vpart[(kind ? rd : rt) * VR_SMAX + part] = st;
+        if (vr_atom_add(P.pair + (size_t)b * (K + 1) + i, 1u) != (uint32_t)(nrows * P.parts - 1))
+            return;
+        t = merge_parts(P.vpart + rt * VR_SMAX, P.parts);
+        if (nrows > 1)
+            d = merge_parts(P.vpart + rd * VR_SMAX, P.parts);
+    }
+    P.stat[rt] = t;
+    if (nrows > 1)
+        P.stat[rd] = d;
+    bool acc = false;
+    const int code = vr_decide(P, b, i, dt, t, d, acc);
+    const bool ends = code || (!acc && i < K);
+    if (ends) {
+        P.errc[(size_t)b * (K + 1) + i] = code;
+        atomicOr(P.rej + b, 1u << i);
+    }
+    {
+        // the word of decided (low half) and ending (high half) positions:
+        // blind rows look at it, and with the residual pass in the stream the
+        // update completing the sequence's end posts its residual job
+        const unsigned long long bits = (1ull << i) | ((ends || i == K) ? (1ull << (32 + i)) : 0ull);
+        const unsigned long long old = vr_atom_or64(P.dw + b, bits);
+        if (P.fused && !vr_ended(old) && vr_ended(old | bits))
+            vr_post_end(P, b, old | bits);
+    }
+}
+
 template <class E>
-__global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsParams P)
+__global__ void __launch_bounds__(VS_T, VS_CPS) vr_stream(const __grid_constant__ RowsParams P)
 {
     pdl_trigger();
     extern __shared__ __align__(128) uint8_t vs_buf[];
@@ -740,19 +868,83 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
         uint32_t ph = 0;
         bool ok = true;
         constexpr int RT = VR2_HALF / E::ES;   // tokens of each row in a residual stage
-        // the next statistics part: claimed one ahead, except with the residual
-        // pass, where a producer claims a part only when it starts it (a part
-        // held while residual chunks go first would delay the decisions that
-        // post the residual jobs)
-        int item = P.fused ? -1 : (int)atomicAdd(P.vctl + VC_CLAIM * VC_LINE, 1u);
+        // Work, in the order it is taken:
+        //   1. with the residual pass (P.fused): residual chunks of sequences
+        //      that have ended (the row pair was streamed recently, so part of
+        //      it is still in L2);
+        //   2. parts handed out position-major from one counter.
+        // Without the residual pass the next part is claimed one ahead; with
+        // it, a part is claimed only when it starts (a part held while
+        // residual chunks go first would delay the decisions that post them).
+        const bool dyn = P.fused != 0;
+        const int nstatic = nitems;
+        int item = dyn ? -1 : (int)atomicAdd(P.vctl + VC_CLAIM * VC_LINE, 1u);
         bool drained = false;
         uint32_t idle = 0;
         int pend = -1;      // a residual chunk number claimed ahead of its job
         bool stop = false;  // a wait on other CTAs gave up (ok: the ring is intact)
+        // Stream part `part` of row r of the stream's order.
+        auto stream_part = [&](int r, int part, int it) {
+            int i, b, kind;
+            vs_row(P, r, i, b, kind);
+            const size_t ridx = (size_t)b * (2 * K + 1) + (kind ? K + 1 + i : i);
+            const uint32_t m = (P.skip && i > 0) ? __ldcg(P.rej + b) : 0u;
+            const int dt = i < K ? __ldg(P.tokens + (size_t)b * K + i) : -1;
+            if (m & ((1u << i) - 1u)) {
+                // a rejection (or error) decided at an earlier position makes this row unneeded
+                if (part == 0)
+                    P.stat[ridx] = VrStat{-F_INF, 0.0f, 0.0f, VR_SKIP, 0.0f, 0, 0, 0};
+                return;
+            }
+            const uint8_t *row =
+                kind ? static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + i) * (size_t)V * E::ES
+                     : static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + i) * (size_t)V * E::ES;
+            const int t0 = part * P.span, t1 = min(V, t0 + P.span);
+            // A row started before every earlier position of its sequence was
+            // decided (and accepted) is read blind: before each stage the
+            // producer looks again (the words loaded one stage ahead), and once
+            // a rejection shows up the part is dropped -- its consumers get an
+            // abort stage in place of the rest and post nothing.
+            const uint32_t need = (1u << i) - 1u;
+            bool blind = P.skip && i > 0 && ((uint32_t)__ldcg(P.dw + b) & need) != need;
+            uint32_t rj = 0u, dd = 0u;
+            for (int tok = t0; tok < t1; tok += STOK) {
+                const int n = min(STOK, t1 - tok);
+                if (blind) {
+                    if (tok > t0) {
+                        if (rj & need) {
+                            if (!vs_wait(&empty[st], ph ^ 1u, lim, tflag)) {
+                                ok = false;
+                                break;
+                            }
+                            meta[st] = VsMeta{it, tok, 0, 1, dt, 2, 0, 0, 0, 0.0f, 0.0f, 0.0f};
+                            mbar_arrive(&full[st]);
+                            if (++st == VS_NS) {
+                                st = 0;
+                                ph ^= 1u;
+                            }
+                            break;
+                        }
+                        blind = (dd & need) != need;   // every earlier position decided: needed
+                    }
+                    rj = __ldcg(P.rej + b);
+                    dd = (uint32_t)__ldcg(P.dw + b);
+                }
+                if (!vs_wait(&empty[st], ph ^ 1u, lim, tflag)) {
+                    ok = false;
+                    break;
+                }
+                meta[st] = VsMeta{it, tok, n, tok + STOK >= t1 ? 1 : 0, dt, 0, 0, 0, 0, 0.0f, 0.0f, 0.0f};
+                mbar_arrive_tx(&full[st], (uint32_t)(n * E::ES));
+                bulk_g2s(vs_buf + st * VS_STAGE, row + (size_t)tok * E::ES, (uint32_t)(n * E::ES), &full[st]);
+                if (++st == VS_NS) {
+                    st = 0;
+                    ph ^= 1u;
+                }
+            }
+        };
         // Take up a posted residual chunk, if there is one; true when it was
-        // taken (streamed, or a wait gave up and ok is false).  Residual chunks
-        // go before the next statistics part: the row pair was streamed
-        // recently, so part of it is still in L2.
+        // taken (streamed, or a wait gave up and ok is false).
         // Chunks are handed out by one counter (atomicAdd, no compare-and-swap
         // storms); a producer holds at most one number claimed ahead of the
         // posted jobs and takes it up once its job is posted.
@@ -766,9 +958,10 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
             pend = -1;
             const int e = ticket / P.rnch, ch = ticket - e * P.rnch;
             // the job was reserved before its chunks could be claimed: its
-            // poster is writing it
+            // poster is writing it (a slot past the B a call can post means a
+            // workspace that was not zeroed: give up without touching it)
             int b1 = 0;
-            for (uint32_t it = 0; it <= lim; ++it) {
+            for (uint32_t it = 0; e < P.B && it <= lim; ++it) {
                 b1 = ld_acq_s32(&P.jobs[e].b1);
                 if (b1)
                     break;
@@ -817,17 +1010,17 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
                 idle = 0;
                 continue;
             }
-            if (P.fused && !drained) {
+            if (dyn && !drained) {
                 item = (int)atomicAdd(P.vctl + VC_CLAIM * VC_LINE, 1u);
-                drained = item >= nitems;
+                drained = item >= nstatic;
             }
-            if (item >= nitems || drained) {
+            if (item >= nstatic || drained) {
                 // no part left: with the residual pass, wait until every sequence
                 // has ended and every posted chunk is claimed
-                if (!P.fused)
+                if (!dyn)
                     break;
-                // every sequence ended: the jobs are final, and a number held past
-                // them has no chunk
+                // every sequence ended: the jobs are final, and a number held
+                // past them has no chunk
                 if (ld_acq(P.vctl + VC_ENDED * VC_LINE) >= (uint32_t)P.B &&
                     (pend < 0 || (uint32_t)pend >= ld_acq(P.vctl + VC_JOBS * VC_LINE) * (uint32_t)P.rnch))
                     break;
@@ -840,38 +1033,9 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
                 __nanosleep(500);
                 continue;
             }
-            const int next = P.fused ? nitems : (int)atomicAdd(P.vctl + VC_CLAIM * VC_LINE, 1u);   // claimed ahead
+            const int next = dyn ? nstatic : (int)atomicAdd(P.vctl + VC_CLAIM * VC_LINE, 1u);   // claimed ahead
             const int r = item / P.parts, part = item - r * P.parts;
-            int i, b, kind;
-            vs_row(P, r, i, b, kind);
-            const size_t ridx = (size_t)b * (2 * K + 1) + (kind ? K + 1 + i : i);
-            const uint32_t m = (P.skip && i > 0) ? __ldcg(P.rej + b) : 0u;
-            const int dt = i < K ? __ldg(P.tokens + (size_t)b * K + i) : -1;
-            if (m & ((1u << i) - 1u)) {
-                // a rejection (or error) decided at an earlier position makes this row unneeded
-                if (part == 0)
-                    P.stat[ridx] = VrStat{-F_INF, 0.0f, 0.0f, VR_SKIP, 0.0f, 0, 0, 0};
-                item = next;
-                continue;
-            }
-            const uint8_t *row =
-                kind ? static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + i) * (size_t)V * E::ES
-                     : static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + i) * (size_t)V * E::ES;
-            const int t0 = part * P.span, t1 = min(V, t0 + P.span);
-            for (int tok = t0; tok < t1; tok += STOK) {
-                const int n = min(STOK, t1 - tok);
-                if (!vs_wait(&empty[st], ph ^ 1u, lim, tflag)) {
-                    ok = false;
-                    break;
-                }
-                meta[st] = VsMeta{item, tok, n, tok + STOK >= t1 ? 1 : 0, dt, 0, 0, 0, 0, 0.0f, 0.0f, 0.0f};
-                mbar_arrive_tx(&full[st], (uint32_t)(n * E::ES));
-                bulk_g2s(vs_buf + st * VS_STAGE, row + (size_t)tok * E::ES, (uint32_t)(n * E::ES), &full[st]);
-                if (++st == VS_NS) {
-                    st = 0;
-                    ph ^= 1u;
-                }
-            }
+            stream_part(r, part, item);
             item = next;
         }
         // end of the stream
@@ -899,8 +1063,7 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
             const int r = e.item / P.parts, part = e.item - r * P.parts;
             int i, b, kind;
             vs_row(P, r, i, b, kind);
-            const size_t ridx = (size_t)b * (2 * K + 1) + (kind ? K + 1 + i : i);
-            vr_commit(P, ridx, b, i, kind, part, e.dt, e.st, false);
+            vs_commit(P, b, i, kind, part, e.dt, e.st);
         }
         return;
     }
@@ -922,6 +1085,21 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
         const VsMeta mt = meta[st];
         if (mt.type == 0 && mt.item < 0)
             break;
+        if (mt.type == 2) {
+            // the producer dropped the rest of a part read blind: nothing is posted
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[st]);
+            if (++st == VS_NS) {
+                st = 0;
+                ph ^= 1u;
+            }
+            mc = -F_INF;
+            s = 0.0f;
+            zd = 0.0f;
+            fl = 0;
+            continue;
+        }
         const uint8_t *sb = vs_buf + st * VS_STAGE;
         if (mt.type == 1) {
             // a residual stage: the masses of its 256-token segments
@@ -1039,53 +1217,6 @@ __global__ void __launch_bounds__(VS_T) vr_stream(const __grid_constant__ RowsPa
         ep[nit % VS_EPN].item = -1;
         mbar_arrive(&epf[nit % VS_EPN]);
     }
-}
-
-// ---------------------------------------------------------------- 2. residual masses
-// The coefficients of the distribution sequence b samples at its end j, from
-// the statistics t of its target row j and d of its draft row j (j < K).
-__device__ __forceinline__ ResK res_coef(const RowsParams &P, const VrStat &t, const VrStat &d, int j)
-{
-    ResK k;
-    k.Mt = t.m;
-    k.c = P.c;
-    k.dLhi = k.dLlo = 0.0f;
-    if (j < P.K) {
-        // dL = (Md - Mt) + log2 Sd - log2 St as a float pair
-        int et, ed;
-        float ft, fd;
-        log2_split(DF{t.s_hi, t.s_lo}, et, ft);
-        log2_split(DF{d.s_hi, d.s_lo}, ed, fd);
-        DF dl = two_sum(d.m, -t.m);
-        dl = df_add(dl, DF{(float)(ed - et), 0.0f});
-        dl = df_add(dl, DF{fd - ft, 0.0f});
-        k.dLhi = dl.hi;
-        k.dLlo = dl.lo;
-    }
-    return k;
-}
-// The same, loading the statistics (the draft row's only where it is used).
-__device__ __forceinline__ ResK vr_coef(const RowsParams &P, int b, int j)
-{
-    const VrStat *st = P.stat + (size_t)b * (2 * P.K + 1);
-    const VrStat t = ld_vrstat(st + j);
-    ResK k;
-    k.Mt = t.m;
-    k.c = P.c;
-    k.dLhi = k.dLlo = 0.0f;
-    if (j < P.K) {
-        const VrStat d = ld_vrstat(st + P.K + 1 + j);
-        int et, ed;
-        float ft, fd;
-        log2_split(DF{t.s_hi, t.s_lo}, et, ft);
-        log2_split(DF{d.s_hi, d.s_lo}, ed, fd);
-        DF dl = two_sum(d.m, -t.m);
-        dl = df_add(dl, DF{(float)(ed - et), 0.0f});
-        dl = df_add(dl, DF{fd - ft, 0.0f});
-        k.dLhi = dl.hi;
-        k.dLlo = dl.lo;
-    }
-    return k;
 }
 
 // Sequence b has ended (word w): post its residual job -- the position j it
@@ -1585,6 +1716,7 @@ bool use_stream(const RowsParams &P)
 }
 
 constexpr long long kFusedMinRows = 1024;
+constexpr long long kFusedSmallRows = 256;   // below this (small calls routed here): fused as well
 
 // Whether vr_stream runs the residual pass: SPECVERIFY_ROWS_FUSED=1 always,
 // =0 never (vr_residual does), unset by the call's size (-1); for
@@ -1618,10 +1750,13 @@ cudaError_t launch_stream(RowsParams P, int sms, cudaStream_t stream)
     const int ncta = sms * VS_CPS;
     const long long rows = (long long)P.B * (2 * P.K + 1);
     constexpr int STOK = VS_STAGE / E::ES;
-    int S = (int)std::min<long long>(VR_SMAX, (2LL * ncta + rows - 1) / rows);
+    // at most VS_SMAX parts: 16 parts per row (B = 64, K = 4, residual pass in
+    // its own launch) ran every call into the bounded waits' limit; the cause
+    // is not known, and more than 8 parts never measured faster
+    int S = (int)std::min<long long>(VS_SMAX, (2LL * ncta + rows - 1) / rows);
     S = std::max(1, std::min(S, P.V / (2 * STOK)));
     if (const char *ev = std::getenv("SPECVERIFY_ROWS_PARTS"))
-        S = std::max(1, std::min(VR_SMAX, std::atoi(ev)));
+        S = std::max(1, std::min(VS_SMAX, std::atoi(ev)));
     P.span = ((P.V + S - 1) / S + 7) / 8 * 8;
     P.parts = (P.V + P.span - 1) / P.span;
     vr_stream<E><<<ncta, VS_T, smem, stream>>>(P);
@@ -1642,9 +1777,11 @@ cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream, int &launches)
         // the residual pass in the same launch, in chunks of four stages, for
         // calls of at least kFusedMinRows rows (measured: B = 256, K = 4 at
         // 122 us against 138 us with vr_residual; B = 64, K = 4 at 64.5 us
-        // against 61.5 us)
+        // against 61.5 us) and for the small calls the dispatch sends here
+        // (B = 1, K = 4: 39 us against 44 us; B = 8, K = 8: 56 against 57)
         const int fm = fused_mode();
-        P.fused = fm == 1 || (fm < 0 && (long long)P.B * (2 * P.K + 1) >= kFusedMinRows) ? 1 : 0;
+        const long long nrows = (long long)P.B * (2 * P.K + 1);
+        P.fused = fm == 1 || (fm < 0 && (nrows >= kFusedMinRows || nrows < kFusedSmallRows)) ? 1 : 0;
         constexpr int RT = VR2_HALF / E::ES;
         const int nst = (P.V + RT - 1) / RT;
         P.rcs = 4;

@@ -37,7 +37,8 @@ def kernel(request):
     kernel (each falls back to the next for shapes it does not serve);
     "rows" runs the residual pass inside the statistics stream at every size,
     "rows-unfused" keeps it in its own launch."""
-    saved = {k: os.environ.get(k) for k in ("SPECVERIFY_KERNEL", "SPECVERIFY_ROWS_STREAM", "SPECVERIFY_ROWS_FUSED")}
+    keys = ("SPECVERIFY_KERNEL", "SPECVERIFY_ROWS_STREAM", "SPECVERIFY_ROWS_FUSED")
+    saved = {k: os.environ.get(k) for k in keys}
     os.environ["SPECVERIFY_KERNEL"] = "rows" if request.param.startswith("rows") else request.param
     if request.param == "rows-stats":
         os.environ["SPECVERIFY_ROWS_STREAM"] = "0"
