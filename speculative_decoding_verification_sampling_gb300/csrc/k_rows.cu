@@ -328,7 +328,10 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
              : static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + i) * (size_t)V * E::ES;
     const int32_t *lst = slrow ? P.sl + b * P.sl_seq + i * P.sl_pos : nullptr;
     const int dt = i < K ? __ldg(P.tokens + (size_t)b * K + i) : -1;
-    const int t0 = min(nrow, part * P.span), t1 = min(nrow, t0 + P.span);
+    // a shortlisted draft row is cut by its own length, so that its list
+    // entries (the slow part of the row) spread over every part
+    const int span = slrow ? ((nrow + P.parts - 1) / P.parts + 7) / 8 * 8 : P.span;
+    const int t0 = min(nrow, part * span), t1 = min(nrow, t0 + span);
     const int u0 = t0 / 8, nu = (t1 - t0 + 7) / 8;   // this part's units of 8 tokens
     const float c = P.c;
     float mc = -F_INF, s = 0.0f, bv = -F_INF, zd = 0.0f;
@@ -1245,9 +1248,11 @@ __device__ __noinline__ void vr_post_end(const RowsParams &P, int b, unsigned lo
 // scattered into a per-warp buffer of VSEG floats; tokens off the list read
 // -inf, i.e. p = 0.
 template <class E>
-// lo, hi: the segment's list range when known (lo >= 0), else loaded here.
+// lo, hi: the segment's list range when known (lo >= 0), else loaded here;
+// pidx >= 0: this lane's first entry (list index lo + lane) already loaded,
+// with its draft value pval.
 __device__ __forceinline__ void sl_pairs(const RowsParams &P, int b, int j, int seg, int lane, float *buf, f2 *XD,
-                                         int lo = -1, int hi = -1)
+                                         int lo = -1, int hi = -1, int pidx = -1, float pval = 0.0f)
 {
 #pragma unroll
     for (int e = 0; e < 8; ++e)
@@ -1261,7 +1266,14 @@ __device__ __forceinline__ void sl_pairs(const RowsParams &P, int b, int j, int 
             lo = __ldcg(lb + seg);
             hi = __ldcg(lb + seg + 1);
         }
-        for (int si = lo + lane; si < hi; si += 32) {
+        int si0 = lo + lane;
+        if (pidx >= 0) {
+            const int pos = pidx - seg * VSEG;
+            if ((unsigned)pos < (unsigned)VSEG)
+                buf[pos] = pval;
+            si0 += 32;
+        }
+        for (int si = si0; si < hi; si += 32) {
             const int pos = __ldg(lst + si) - seg * VSEG;
             if ((unsigned)pos < (unsigned)VSEG)
                 buf[pos] = E::load(drow, (size_t)si);
@@ -1334,6 +1346,24 @@ __global__ void __launch_bounds__(VRT, E::ES == 2 ? 3 : 1) vr_residual(const __g
                 ud[q] = fetch_unit<E>(drow, unit_x0(q), V, P.vec);
         }
     for (int t0 = 0; t0 < nsteps; t0 += 4) {
+        // a shortlisted draft: each lane's first list entry of the four steps,
+        // loaded at once (one round trip for the group, not one per step)
+        int pidx[4];
+        float pval[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            pidx[q] = -1;
+            pval[q] = 0.0f;
+            if (pre) {
+                const int t = t0 + q;
+                const int lo = __shfl_sync(0xffffffffu, blo, t & 31), hi = __shfl_sync(0xffffffffu, bhi, t & 31);
+                if (t < nsteps && lo + lane < hi) {
+                    pidx[q] = __ldg(P.sl + b * P.sl_seq + j * P.sl_pos + lo + lane);
+                    pval[q] = E::load(static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + j) * (size_t)P.S * E::ES,
+                                      (size_t)(lo + lane));
+                }
+            }
+        }
         // the (r', q') sums of four steps' units, reduced over the lanes at once
         float v[8];
 #pragma unroll
@@ -1346,7 +1376,8 @@ __global__ void __launch_bounds__(VRT, E::ES == 2 ? 3 : 1) vr_residual(const __g
                 if (slist) {
                     // the segment's list range: loaded up front (lane t holds step t's)
                     const int lo = __shfl_sync(0xffffffffu, blo, t & 31), hi = __shfl_sync(0xffffffffu, bhi, t & 31);
-                    sl_pairs<E>(P, b, j, s_lo + t * NW + warp, lane, sl_buf[warp], XD, pre ? lo : -1, hi);
+                    sl_pairs<E>(P, b, j, s_lo + t * NW + warp, lane, sl_buf[warp], XD, pre ? lo : -1, hi,
+                                pidx[q], pval[q]);
                 } else if (!qonly) {
                     unit_pairs<E>(ud[q], XD);
                 }
@@ -1693,7 +1724,11 @@ cudaError_t launch_stats(RowsParams P, int pos, int npos, int sms, cudaStream_t 
     const int rows = rpp * npos;
     const long long want = (long long)sms * 2048;
     int S = (int)std::min<long long>(VR_SMAX, (want + (long long)rows * VST_T - 1) / ((long long)rows * VST_T));
-    S = std::max(1, std::min(S, P.V / 4096));
+    // parts of at most 32768 tokens whatever the count of rows: most rows of a
+    // later launch may skip, and those that do not should not be one CTA's
+    // (a part that skips costs a launch and one load)
+    S = std::max(S, (P.V + 32767) / 32768);
+    S = std::max(1, std::min(std::min(S, VR_SMAX), P.V / 4096));
     P.pos = pos;
     P.npos = npos;
     P.span = ((P.V + S - 1) / S + 7) / 8 * 8;
@@ -1803,6 +1838,10 @@ cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream, int &launches)
     if (e != cudaSuccess)
         return e;
     if (!P.greedy && !P.fused) {
+        // a shortlisted draft's segments scatter their list entries, a round
+        // trip per step: four times the CTAs per sequence, a quarter of the steps
+        if (P.sl)
+            P.nch = 4 * VR_NCH;
         e = launch_after(vr_residual<E>, P.B * P.nch, VRT, 0, stream, P);
         launches += 1;
         if (e != cudaSuccess)
