@@ -262,7 +262,7 @@ struct RowsShortlist {
 spec_status_t run_rows(bool greedy, const void *target, spec_dtype_t tdt, const void *draft, const int32_t *tokens,
                        int B, int K, int V, float T, uint64_t seed, int32_t *out_tokens, int32_t *out_len,
                        void *workspace, const sv::WsLayout &L, const spec_aux_t *aux, void *stream,
-                       const RowsShortlist &sl = RowsShortlist())
+                       const RowsShortlist &sl = RowsShortlist(), bool probs = false)
 {
     if ((long long)B * (2 * K + 1) > INT32_MAX || (long long)B * sv::rows_chunks() > INT32_MAX)
         return SPEC_ERR_UNSUPPORTED;
@@ -302,6 +302,11 @@ spec_status_t run_rows(bool greedy, const void *target, spec_dtype_t tdt, const 
     P.skip = (P.aux_q || P.aux_p || P.aux_lse) ? 0 : 1;
     P.vec = ((long long)V * es) % 16 == 0 && reinterpret_cast<uintptr_t>(target) % 16 == 0 &&
             (greedy || reinterpret_cast<uintptr_t>(draft) % 16 == 0);
+    if (probs && !greedy) {
+        // float32 probability rows, read by the residual pass in 16-byte copies
+        P.probs = 1;
+        P.vec = P.vec && ((long long)V * 4) % 16 == 0;
+    }
     if (sl.idx && !greedy) {
         P.sl = sl.idx;
         P.sl_seq = sl.seq;
@@ -319,7 +324,10 @@ spec_status_t run_rows(bool greedy, const void *target, spec_dtype_t tdt, const 
         std::fprintf(stderr, "specverify: rows kernels %s %s B=%d K=%d V=%d skip=%d vec=%d\n",
                      greedy ? "greedy" : "stochastic", tdt == SPEC_BF16 ? "bf16" : "f32", B, K, V, P.skip, P.vec);
     int nl = 0;
-    if (sv::launch_rows(P, tdt == SPEC_BF16 ? 1 : 0, static_cast<cudaStream_t>(stream), &nl) != cudaSuccess)
+    const cudaError_t le = sv::launch_rows(P, tdt == SPEC_BF16 ? 1 : 0, static_cast<cudaStream_t>(stream), &nl);
+    if (le == cudaErrorNotSupported)
+        return SPEC_ERR_UNSUPPORTED;
+    if (le != cudaSuccess)
         return SPEC_ERR_CUDA;
     g_launches.fetch_add((uint64_t)nl, std::memory_order_relaxed);
     return SPEC_OK;
@@ -462,6 +470,17 @@ spec_status_t run(int mode, const void *target, spec_dtype_t tdt, const void *dr
             sl.S = S;
             const spec_status_t rs = run_rows(false, target, tdt, draft, tokens, B, K, V, T, seed, out_tokens,
                                               out_len, workspace, L, aux, stream, sl);
+            if (rs != SPEC_ERR_UNSUPPORTED)
+                return rs;
+        }
+    }
+    // draft probabilities with the rows' layout the stream reads: the
+    // row-parallel path streams the target rows alone (same size rule as logits)
+    if (mode == sv::MODE_STOCH && probs) {
+        const KernelChoice kc = kernel_choice();
+        if (kc == KC_ROWS || (kc == KC_AUTO && ((long long)B * (2 * K + 1) >= kRowsMinRows || B <= 2 || K >= 6))) {
+            const spec_status_t rs = run_rows(false, target, tdt, draft, tokens, B, K, V, T, seed, out_tokens,
+                                              out_len, workspace, L, aux, stream, RowsShortlist(), true);
             if (rs != SPEC_ERR_UNSUPPORTED)
                 return rs;
         }

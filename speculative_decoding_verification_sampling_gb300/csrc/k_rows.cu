@@ -135,6 +135,24 @@ __device__ __forceinline__ int vr_decide(const RowsParams &P, int b, int i, int 
         return ST_NONFINITE;
     if (i == P.K)
         return 0;
+    if (P.probs) {
+        // the given p_i(d_i): finite and >= 0; 0 accepts; else
+        // log2(q(d) / p(d)) = zt c - Mt - log2 St - log2 p(d)
+        const float pd = __ldg(static_cast<const float *>(P.draft) + ((size_t)b * P.K + i) * (size_t)P.V + dt);
+        if (!(pd >= 0.0f) || pd == F_INF)
+            return ST_NONFINITE;
+        if (pd == 0.0f) {
+            accept = true;
+            return 0;
+        }
+        int et;
+        float ft;
+        log2_split(DF{t.s_hi, t.s_lo}, et, ft);
+        const float X = t.zd * P.c - (t.m + ((float)et + ft)) - lg2a(pd);
+        const uint4 w = philox10((uint32_t)i, (uint32_t)b, 0u, 0u, P.key0, P.key1);
+        accept = X >= 0.0f || u24_below(w.x, ex2a(X));
+        return 0;
+    }
     if ((d.flags & VR_BAD) || !(d.m > -F_INF) || !(d.s_hi > 0.0f))
         return ST_NONFINITE;
     int et, ed;
@@ -571,7 +589,17 @@ __device__ __forceinline__ ResK res_coef(const RowsParams &P, const VrStat &t, c
     k.Mt = t.m;
     k.c = P.c;
     k.dLhi = k.dLlo = 0.0f;
-    if (j < P.K) {
+    if (j < P.K && P.probs) {
+        // given probabilities: x_d c stands for log2 p(x) and dL = -(Mt + log2 St),
+        // so that delta = log2(p St / q') as for logits
+        int et;
+        float ft;
+        log2_split(DF{t.s_hi, t.s_lo}, et, ft);
+        DF dl = two_sum(-t.m, -(float)et);
+        dl = df_add(dl, DF{-ft, 0.0f});
+        k.dLhi = dl.hi;
+        k.dLlo = dl.lo;
+    } else if (j < P.K) {
         // dL = (Md - Mt) + log2 Sd - log2 St as a float pair
         int et, ed;
         float ft, fd;
@@ -590,23 +618,8 @@ __device__ __forceinline__ ResK vr_coef(const RowsParams &P, int b, int j)
 {
     const VrStat *st = P.stat + (size_t)b * (2 * P.K + 1);
     const VrStat t = ld_vrstat(st + j);
-    ResK k;
-    k.Mt = t.m;
-    k.c = P.c;
-    k.dLhi = k.dLlo = 0.0f;
-    if (j < P.K) {
-        const VrStat d = ld_vrstat(st + P.K + 1 + j);
-        int et, ed;
-        float ft, fd;
-        log2_split(DF{t.s_hi, t.s_lo}, et, ft);
-        log2_split(DF{d.s_hi, d.s_lo}, ed, fd);
-        DF dl = two_sum(d.m, -t.m);
-        dl = df_add(dl, DF{(float)(ed - et), 0.0f});
-        dl = df_add(dl, DF{fd - ft, 0.0f});
-        k.dLhi = dl.hi;
-        k.dLlo = dl.lo;
-    }
-    return k;
+    const VrStat d = (j < P.K && !P.probs) ? ld_vrstat(st + P.K + 1 + j) : VrStat{};
+    return res_coef(P, t, d, j);
 }
 
 // ---------------------------------------------------------------- 1b. row statistics from a bulk-copy stream
@@ -676,6 +689,13 @@ __device__ __forceinline__ bool vs_wait(unsigned long long *bar, uint32_t par, u
 // of every sequence side by side, position K the B target rows.
 __device__ __forceinline__ void vs_row(const RowsParams &P, int r, int &i, int &b, int &kind)
 {
+    if (P.probs) {
+        // draft probabilities: the target rows alone, position-major
+        i = r / P.B;
+        b = r - i * P.B;
+        kind = 0;
+        return;
+    }
     const int nk = 2 * P.B * P.K;
     if (r < nk) {
         i = r / (2 * P.B);
@@ -801,7 +821,7 @@ __device__ __noinline__ void vs_commit(const RowsParams &P, int b, int i, int ki
 {
     const int K = P.K;
     const size_t rt = (size_t)b * (2 * K + 1) + i, rd = (size_t)b * (2 * K + 1) + K + 1 + i;
-    const int nrows = i < K ? 2 : 1;
+    const int nrows = i < K && !P.probs ? 2 : 1;   // given probabilities: no draft row is streamed
     VrStat t = st, d{};
     if (P.parts > 1 || nrows > 1) {
         P.vpart[(kind ? rd : rt) * VR_SMAX + part] = st;
@@ -861,7 +881,7 @@ __global__ void __launch_bounds__(VS_T, VS_CPS) vr_stream(const __grid_constant_
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    const int nitems = P.B * (2 * K + 1) * P.parts;
+    const int nitems = P.B * (P.probs ? K + 1 : 2 * K + 1) * P.parts;
 
     if (warp == VS_NCW) {
         // ---- producer
@@ -979,26 +999,30 @@ __global__ void __launch_bounds__(VS_T, VS_CPS) vr_stream(const __grid_constant_
             const VrJob jb = P.jobs[e];
             const int b = b1 - 1, j = jb.j;
             const bool qonly = j == K;
+            // tokens of each row per residual stage: half a stage of target
+            // logits, or (given probabilities, 4 bytes each) a quarter
+            const int rt = P.probs ? VR2_HALF / 4 : RT;
+            const int des = P.probs ? 4 : E::ES;   // bytes of a draft element
             const uint8_t *trow =
                 static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + j) * (size_t)V * E::ES;
             const uint8_t *drow =
                 qonly ? trow
-                      : static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + j) * (size_t)V * E::ES;
+                      : static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + j) * (size_t)V * des;
             for (int sg = 0; sg < P.rcs; ++sg) {
-                const int tok0 = (ch * P.rcs + sg) * RT;
+                const int tok0 = (ch * P.rcs + sg) * rt;
                 if (tok0 >= V)
                     break;
-                const int n = min(RT, V - tok0);
+                const int n = min(rt, V - tok0);
                 if (!vs_wait(&empty[st], ph ^ 1u, lim, tflag)) {
                     ok = false;
                     break;
                 }
                 meta[st] = VsMeta{-2, tok0, n, 0, -1, 1, b, j, qonly ? 1 : 0, jb.Mt, jb.dLhi, jb.dLlo};
-                const uint32_t nb = (uint32_t)(n * E::ES);
-                mbar_arrive_tx(&full[st], qonly ? nb : 2u * nb);
+                const uint32_t nb = (uint32_t)(n * E::ES), nd = qonly ? 0u : (uint32_t)(n * des);
+                mbar_arrive_tx(&full[st], nb + nd);
                 bulk_g2s(vs_buf + st * VS_STAGE, trow + (size_t)tok0 * E::ES, nb, &full[st]);
                 if (!qonly)
-                    bulk_g2s(vs_buf + st * VS_STAGE + VR2_HALF, drow + (size_t)tok0 * E::ES, nb, &full[st]);
+                    bulk_g2s(vs_buf + st * VS_STAGE + VR2_HALF, drow + (size_t)tok0 * des, nd, &full[st]);
                 if (++st == VS_NS) {
                     st = 0;
                     ph ^= 1u;
@@ -1104,6 +1128,60 @@ __global__ void __launch_bounds__(VS_T, VS_CPS) vr_stream(const __grid_constant_
             continue;
         }
         const uint8_t *sb = vs_buf + st * VS_STAGE;
+        if (mt.type == 1 && P.probs) {
+            // a residual stage with given probabilities: 2048 tokens, one
+            // 256-token segment per warp; x_d c = log2 p (lg2 of each
+            // probability); a probability that is negative, NaN or +inf puts
+            // the sequence in error (its position j was a rejection)
+            const ResK k{mt.Mt, mt.dLhi, mt.dLlo, c};
+            const float ic = 1.0f / c;
+            const int x = warp * VSEG + lane * 8;   // token within the stage
+            float v0 = 0.0f, v1 = 0.0f;
+            bool bad = false;
+            if (x < mt.ntok) {
+                const uint4 *pt = reinterpret_cast<const uint4 *>(sb + (size_t)x * E::ES);
+                Unit<E> ut;
+                ut.a = pt[0];
+                if constexpr (E::ES == 4) {
+                    const uint4 ninf = make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+                    ut.b = x + 8 <= mt.ntok ? pt[1] : ninf;
+                }
+                f2 XT[4], XD[4], R[4], Q[4];
+                unit_pairs<E>(ut, XT);
+                if (mt.qonly) {
+#pragma unroll
+                    for (int p = 0; p < 4; ++p)
+                        XD[p] = XT[p];
+                } else {
+                    const float4 *pp = reinterpret_cast<const float4 *>(sb + VR2_HALF + (size_t)x * 4);
+                    const float4 pa = pp[0], pb = x + 8 <= mt.ntok ? pp[1] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    const float pv[8] = {pa.x, pa.y, pa.z, pa.w, pb.x, pb.y, pb.z, pb.w};
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        const float a0 = pv[2 * p], a1 = pv[2 * p + 1];
+                        bad |= !(a0 >= 0.0f) || a0 == F_INF || !(a1 >= 0.0f) || a1 == F_INF;
+                        XD[p] = pk(lg2a(a0) * ic, lg2a(a1) * ic);
+                    }
+                }
+                vr_res8(XT, XD, k, mt.qonly != 0, R, Q);
+                v0 = sum4p(R);
+                v1 = sum4p(Q);
+            }
+            if (__any_sync(0xffffffffu, bad) && lane == 0)
+                P.errc[(size_t)mt.b * (K + 1) + mt.j] = ST_NONFINITE;
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[st]);
+            if (++st == VS_NS) {
+                st = 0;
+                ph ^= 1u;
+            }
+            const float vv[2] = {v0, v1};
+            const float tot = xpose_sum<2>(vv, lane);   // lane 0: r', lane 16: q'
+            if ((lane & 15) == 0 && warp * VSEG < mt.ntok)
+                reinterpret_cast<float *>(P.segm + (size_t)mt.b * P.nseg + mt.tok0 / VSEG + warp)[lane >> 4] = tot;
+            continue;
+        }
         if (mt.type == 1) {
             // a residual stage: the masses of its 256-token segments
             constexpr int SPW = VR2_HALF / E::ES / VSEG / VS_NCW;   // segments per warp
@@ -1444,20 +1522,31 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
         for (int i = tid; i < 2 * K + 1; i += VST) {
             bool ok;
             const float l2 = row_l2(ld_vrstat(st + i), ok);
-            if (P.aux_lse)
-                P.aux_lse[(size_t)b * (2 * K + 1) + i] = ok ? l2 * 0.6931471805599453f : nan;
+            if (P.aux_lse)   // given probabilities have no draft logits: NaN there
+                P.aux_lse[(size_t)b * (2 * K + 1) + i] = ok && !(P.probs && i > K) ? l2 * 0.6931471805599453f : nan;
         }
-        // q_i(d_i) and p_i(d_i) where both rows of the position and the token are usable
+        // q_i(d_i) and p_i(d_i) where both rows of the position (given
+        // probabilities: the target row and p_i(d_i)) and the token are usable
         for (int i = tid; i < K; i += VST) {
-            const VrStat t = ld_vrstat(st + i), d = ld_vrstat(st + K + 1 + i);
+            const VrStat t = ld_vrstat(st + i);
             bool okt, okd;
-            const float lt = row_l2(t, okt), ld = row_l2(d, okd);
+            const float lt = row_l2(t, okt);
             const int dt = __ldg(P.tokens + (size_t)b * K + i);
+            float pv;
+            if (P.probs) {
+                pv = dt >= 0 && dt < V ? __ldg(static_cast<const float *>(P.draft) + ((size_t)b * K + i) * (size_t)V + dt)
+                                       : nan;
+                okd = pv >= 0.0f && pv != F_INF;
+            } else {
+                const VrStat d = ld_vrstat(st + K + 1 + i);
+                const float ld = row_l2(d, okd);
+                pv = ex2a(fmaf(d.zd, P.c, -ld));
+            }
             const bool ok = okt && okd && dt >= 0 && dt < V;
             if (P.aux_q)
                 P.aux_q[(size_t)b * K + i] = ok ? ex2a(fmaf(t.zd, P.c, -lt)) : nan;
             if (P.aux_p)
-                P.aux_p[(size_t)b * K + i] = ok ? ex2a(fmaf(d.zd, P.c, -ld)) : nan;
+                P.aux_p[(size_t)b * K + i] = ok ? pv : nan;
         }
     }
     if (tid == 0)
@@ -1603,15 +1692,31 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
                 const int x0 = seg * VSEG + lane * 8;
                 const Unit<E> ut = fetch_unit<E>(trow, x0, V, P.vec);
                 Unit<E> ud{};
-                if (!qonly && !slist)
+                Unit<F32> up{};
+                if (!qonly && P.probs)
+                    up = fetch_unit<F32>(static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + j) * (size_t)V * 4,
+                                         x0, V, P.vec);
+                else if (!qonly && !slist)
                     ud = fetch_unit<E>(static_cast<const uint8_t *>(P.draft) +
                                            ((size_t)b * K + j) * (size_t)V * E::ES, x0, V, P.vec);
                 f2 XT[4], XD[4];
                 unit_pairs<E>(ut, XT);
-                if (slist)
+                if (slist) {
                     sl_pairs<E>(P, b, j, seg, lane, sl_buf0, XD);
-                else if (!qonly)
+                } else if (!qonly && P.probs) {
+                    // x_d c = log2 p, as in the residual pass
+                    f2 PP[4];
+                    unit_pairs<F32>(up, PP);
+                    const float ic = 1.0f / P.c;
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        float a0, a1;
+                        upk(PP[p], a0, a1);
+                        XD[p] = pk(lg2a(a0) * ic, lg2a(a1) * ic);
+                    }
+                } else if (!qonly) {
                     unit_pairs<E>(ud, XD);
+                }
                 f2 R[4], Q[4];
                 vr_res8(XT, XD, k, qonly, R, Q);
                 float r[8];
@@ -1808,6 +1913,8 @@ cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream, int &launches)
     if (e != cudaSuccess)
         return e;
     launches = 0;
+    if (P.probs && !use_stream(P))
+        return cudaErrorNotSupported;   // given probabilities: the stream alone serves them
     if (use_stream(P)) {
         // the residual pass in the same launch, in chunks of four stages, for
         // calls of at least kFusedMinRows rows (measured: B = 256, K = 4 at
@@ -1817,8 +1924,10 @@ cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream, int &launches)
         const int fm = fused_mode();
         const long long nrows = (long long)P.B * (2 * P.K + 1);
         P.fused = fm == 1 || (fm < 0 && (nrows >= kFusedMinRows || nrows < kFusedSmallRows)) ? 1 : 0;
-        constexpr int RT = VR2_HALF / E::ES;
+        const int RT = P.probs ? VR2_HALF / 4 : VR2_HALF / E::ES;   // tokens of a row per residual stage
         const int nst = (P.V + RT - 1) / RT;
+        if (P.probs)
+            P.fused = 1;   // the residual pass over given probabilities runs in the stream only
         P.rcs = 4;
         P.rnch = (nst + P.rcs - 1) / P.rcs;
         e = launch_stream<E>(P, sms, stream);

@@ -258,6 +258,10 @@ struct RowsParams {
     int32_t *lb;               // [B][K][nseg + 1]
     int parts, span;           // vr_stats: parts per row, tokens per part (a multiple of 8)
     int greedy, skip, vec;
+    // draft probabilities (float32 [B][K][V], probs != 0): only target rows
+    // are streamed; p_i(d_i) is read where a position is decided, the row p_j
+    // by the residual pass
+    int probs;
     float c;
     uint32_t key0, key1;
     // the call's counters, each on its own 128-byte line (index VC_* * 32)

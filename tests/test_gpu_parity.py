@@ -310,6 +310,43 @@ def test_draft_probabilities(B, K, V, dtype):
         assert_parity(t, l, _oracle(pc, seed, probs=True), "probs")
 
 
+def test_draft_probabilities_throughput_size():
+    """Draft probabilities at B=256 K=4 V=128256 (the row-parallel path reads
+    the target rows and, at each sequence's end, its probability row)."""
+    cfg = _cached(("tp", 256, 4), lambda: synth.throughput(B=256, K=4, seed=260))
+    pc = _cached(("tp-probs", 256, 4), lambda: dict(cfg, draft=torch.softmax(cfg["draft"].float(), dim=-1)))
+    ref = _cached(("tp-probs-ref", 256, 4), lambda: _oracle(pc, 17, probs=True))
+    t, l = _gpu_run(pc, 17, probs=True)
+    assert_parity(t, l, ref, "draft probabilities B=256 K=4")
+
+
+def test_draft_probability_errors_where_read():
+    """Bad given probabilities are errors only where the rule reads them: the
+    drafted token's p_i(d_i) at an examined position, and the whole row p_j at
+    a rejection (its residual); an entry elsewhere in an accepted row is never
+    read.  64 sequences of each kind, so the call takes the row-parallel path."""
+    B, K, V = 256, 2, 4096
+    q = torch.full((V,), 1.0 / V)
+    tgt = torch.log(q).expand(B, K + 1, V).contiguous()
+    drf = q.expand(B, K, V).contiguous().clone()
+    tok = torch.zeros((B, K), dtype=torch.int32)
+    for b in range(0, B, 4):
+        drf[b, 0, 5] = -0.25            # p == q at the drafted token: accepted, entry 5 never read
+        drf[b + 1, 0, 0] = math.nan     # the drafted token's own probability
+        drf[b + 2, 0, 0] = 2.0 / V      # q/p = 0.5: some seeds reject, then the row is read
+        drf[b + 2, 0, 3] = math.inf
+        drf[b + 3, 1, 7] = -1.0         # position 1 row: read if position 1 rejects
+        drf[b + 3, 1, 0] = 4.0 / V
+    cfg = dict(target=tgt, draft=drf, draft_tokens=tok, T=1.0)
+    for seed in (2, 3):
+        ref = _oracle(cfg, seed, probs=True)
+        t, l = _gpu_run(cfg, seed, probs=True)
+        np.testing.assert_array_equal(l, ref["accept_len"])
+        np.testing.assert_array_equal(t, ref["tokens"])
+        assert (ref["accept_len"][0::4] == K).all() and (ref["accept_len"][1::4] == -2).all()
+        assert -2 in ref["accept_len"][2::4] and (ref["accept_len"][2::4] != -2).any()
+
+
 # ------------------------------------------------------------------ per-position outputs
 @pytest.mark.parametrize("kind", ["logits", "probs", "shortlist"])
 def test_per_position_outputs(kind):
