@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(HERE, "lib")
 LIB = os.path.join(LIBDIR, "libspecverify.so")
-SOURCES = ["api.cu", "k_stoch.cu", "k_greedy.cu", "k_short.cu", "k_cluster.cu", "k_sweep.cu", "k_draft.cu", "k_rows.cu", "k_greedy_rows.cu", "k_kv.cu", "k_tree.cu"]
+SOURCES = ["api.cu", "k_stoch.cu", "k_greedy.cu", "k_short.cu", "k_cluster.cu", "k_draft.cu", "k_rows.cu", "k_greedy_rows.cu", "k_kv.cu", "k_tree.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

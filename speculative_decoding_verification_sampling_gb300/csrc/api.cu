@@ -87,32 +87,26 @@ spec_status_t device_setup(int *sms, int mode, int tdt, bool probs, sv::KernelEn
     return SPEC_OK;
 }
 
-// Batches from this size on go to the sweep kernel first (measured: B=512 K=8
-// 395 us against 462 us for the cluster kernel; B=256 K=4 is faster on the
-// cluster kernel).
-constexpr int kSweepMinB = 512;
 
 // Largest shared-memory footprint per CTA for the cluster kernel: three CTAs
 // (three sequences in flight) per SM at V = 128256 bf16 with clusters of 8.
 constexpr uint32_t kClusterSmemMax = 72 * 1024;
 
 // Stochastic calls with at least this many logit rows (B (2K + 1)) go to the
-// row-parallel kernels: measured faster than the cluster and sweep kernels
+// row-parallel kernels: measured faster than the cluster kernel
 // from B = 32, K = 7 and B = 64, K = 4 up (B = 256, K = 4: 160 us against
 // 202 us); smaller calls cannot fill the GPU with rows.
 constexpr long long kRowsMinRows = 256;
 
 // Kernel choice (SPECVERIFY_KERNEL), for measurement and tests.  By default
-// the dispatch in run() picks the kernel; "cluster", "sweep" and "rows" skip
-// the others of those three; "general" forces the chunk-scheduled kernel.
-enum KernelChoice { KC_AUTO = 0, KC_SWEEP = 1, KC_GENERAL = 2, KC_ROWS = 3, KC_CLUSTER = 4 };
+// the dispatch in run() picks the kernel; "cluster" and "rows" skip the other
+// of those two; "general" forces the chunk-scheduled kernel.
+enum KernelChoice { KC_AUTO = 0, KC_GENERAL = 2, KC_ROWS = 3, KC_CLUSTER = 4 };
 KernelChoice kernel_choice()
 {
     const char *s = std::getenv("SPECVERIFY_KERNEL");
     if (s && std::strcmp(s, "general") == 0)
         return KC_GENERAL;
-    if (s && std::strcmp(s, "sweep") == 0)
-        return KC_SWEEP;
     if (s && std::strcmp(s, "rows") == 0)
         return KC_ROWS;
     if (s && std::strcmp(s, "cluster") == 0)
@@ -152,100 +146,6 @@ bool sizes_ok(int B, int K, int V, int S)
     const long long rows = (long long)B * (2LL * K + 1);
     const long long chunks = (long long)(V / 1024 + 1);
     return rows * chunks < (1LL << 31);
-}
-
-// The sweep kernel (sv_sweep.cuh): stochastic verification with draft logits
-// and greedy verification, when no per-position output is requested, rows
-// start 16-byte aligned and V is at most entry.max_v.
-spec_status_t run_sweep(bool greedy, const void *target, spec_dtype_t tdt, const void *draft,
-                        const int32_t *tokens, int B, int K, int V, float T, uint64_t seed, int32_t *out_tokens,
-                        int32_t *out_len, void *workspace, const sv::WsLayout &L, const spec_aux_t *aux,
-                        void *stream)
-{
-    if (kernel_choice() == KC_GENERAL)
-        return SPEC_ERR_UNSUPPORTED;
-    if (aux && (aux->q_draft || aux->p_draft || aux->row_lse) && !greedy)
-        return SPEC_ERR_UNSUPPORTED;
-    const int es = tdt == SPEC_F32 ? 4 : 2;
-    if (((long long)V * es) % 16 != 0 || reinterpret_cast<uintptr_t>(target) % 16 != 0 ||
-        (!greedy && reinterpret_cast<uintptr_t>(draft) % 16 != 0))
-        return SPEC_ERR_UNSUPPORTED;
-    const int tix = tdt == SPEC_BF16 ? 1 : 0;
-    const sv::SweepEntry entry = sv::entry_sweep(tix);
-    if (V > entry.max_v)
-        return SPEC_ERR_UNSUPPORTED;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess)
-        return SPEC_ERR_CUDA;
-    int occ = 0, sms = 0;
-    {
-        std::lock_guard<std::mutex> lock(g_mu);
-        const auto key = std::make_tuple(dev, 32 + tix, 0, 0u);
-        auto it = g_max_clusters.find(key);
-        if (it == g_max_clusters.end()) {
-            if (entry.occupancy(&occ) != cudaSuccess)
-                return SPEC_ERR_CUDA;
-            g_max_clusters[key] = occ;
-        } else {
-            occ = it->second;
-        }
-        sms = g_dev[dev].sms;
-    }
-    if (occ < 1 || sms < 1)
-        return SPEC_ERR_UNSUPPORTED;
-    // parts per row pair: as many as the workspace holds, none much below 1024 tokens
-    int S = sv::sweep_parts(B);
-    while (S > 1 && (long long)V < 1024LL * S)
-        S >>= 1;
-    char *w = static_cast<char *>(workspace);
-    sv::SweepParams P{};
-    P.target = target;
-    P.draft = greedy ? nullptr : draft;
-    P.tokens = tokens;
-    P.out_tokens = out_tokens;
-    P.out_len = out_len;
-    if (aux) {
-        P.aux_R = aux->residual_mass;
-        P.aux_status = aux->device_status;
-    }
-    P.ctl = reinterpret_cast<uint32_t *>(w + L.ctl);
-    P.reset_words = (uint32_t)((L.reset_end - L.ctl) / 4);
-    P.swc = reinterpret_cast<uint32_t *>(w + L.sw_ctl);
-    P.seq = reinterpret_cast<sv::SwSeq *>(w + L.sw_seq);
-    P.cnt = reinterpret_cast<uint32_t *>(w + L.sw_cnt);
-    P.part = reinterpret_cast<sv::SwStat *>(w + L.sw_part);
-    P.stat = reinterpret_cast<sv::SwStat *>(w + L.sw_stat);
-    P.res = reinterpret_cast<sv::SwRes *>(w + L.sw_res);
-    P.res_ready = reinterpret_cast<uint32_t *>(w + L.sw_res_ready);
-    P.res_done = reinterpret_cast<uint32_t *>(w + L.sw_res_done);
-    P.resm = reinterpret_cast<sv::DF2 *>(w + L.sw_resm);
-    P.B = B;
-    P.K = K;
-    P.V = V;
-    P.S = S;
-    P.span = cdiv(cdiv(V, S), 8) * 8;
-    // sampling jobs in parts of whole stages: about SW_RPARTS of them
-    const int st_tokens = 8192 / es;
-    int rparts = sv::SW_RPARTS;
-    if (const char *e = std::getenv("SPECVERIFY_SWEEP_RPARTS"))
-        rparts = std::max(1, std::atoi(e));
-    P.rspan = cdiv(cdiv(V, rparts), st_tokens) * st_tokens;
-    P.RS = cdiv(V, P.rspan);
-    P.greedy = greedy ? 1 : 0;
-    P.c = greedy ? 1.0f : (float)(1.4426950408889634 / (double)T);
-    P.key0 = (uint32_t)(seed & 0xffffffffu);
-    P.key1 = (uint32_t)(seed >> 32);
-    P.spin_limit = spin_limit();
-    P.n_items = (uint32_t)((long long)(K + 1) * B * S);
-    const int grid = (int)std::min<long long>((long long)occ * sms, P.n_items);
-    if (debug_enabled())
-        std::fprintf(stderr, "specverify: sweep kernel %s %s B=%d K=%d V=%d: %d parts of %d tokens, %u items, "
-                     "grid %d (%d per SM)\n", greedy ? "greedy" : "stochastic", tdt == SPEC_BF16 ? "bf16" : "f32",
-                     B, K, V, S, P.span, P.n_items, grid, occ);
-    if (entry.launch(P, grid, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return SPEC_ERR_CUDA;
-    g_launches.fetch_add(1, std::memory_order_relaxed);
-    return SPEC_OK;
 }
 
 // Row-parallel verification (k_rows.cu): logit draft rows (or greedy), no
@@ -510,21 +410,10 @@ spec_status_t run(int mode, const void *target, spec_dtype_t tdt, const void *dr
         }
         if (!(full && mode != sv::MODE_GREEDY)) {
             uint32_t *ctl = reinterpret_cast<uint32_t *>(static_cast<char *>(workspace) + L.ctl);
-            // large batches: the sweep keeps HBM busier than one sequence per cluster
-            if (kc == KC_AUTO && B >= kSweepMinB) {
-                const spec_status_t ss = run_sweep(mode == sv::MODE_GREEDY, target, tdt, draft, tokens, B, K, V, T,
-                                                   seed, out_tokens, out_len, workspace, L, aux, stream);
-                if (ss != SPEC_ERR_UNSUPPORTED)
-                    return ss;
-            }
             const spec_status_t cs = run_cluster(mode == sv::MODE_GREEDY, target, tdt, draft, tokens, B, K, V, T,
                                                  seed, out_tokens, out_len, ctl, aux, stream);
             if (cs != SPEC_ERR_UNSUPPORTED)
                 return cs;
-            const spec_status_t ss = run_sweep(mode == sv::MODE_GREEDY, target, tdt, draft, tokens, B, K, V, T,
-                                               seed, out_tokens, out_len, workspace, L, aux, stream);
-            if (ss != SPEC_ERR_UNSUPPORTED)
-                return ss;
         }
     }
 

@@ -29,14 +29,6 @@ uint32_t cluster_header_bytes();   // shared memory ahead of the row slices
 constexpr int STATIC_SCRATCH_WORDS = 64;
 cudaError_t static_scratch_address(uint32_t **addr);   // current device
 
-// The sweep kernel: (position, sequence, part) items over persistent CTAs.
-struct SweepEntry {
-    cudaError_t (*launch)(const SweepParams &P, int grid, cudaStream_t stream);
-    cudaError_t (*occupancy)(int *ctas_per_sm);
-    int max_v;   // largest vocabulary it accepts (a row streamed by one CTA)
-};
-SweepEntry entry_sweep(int tdt);
-
 // Row-parallel verification (k_rows.cu): statistics per row, residual masses
 // per sequence chunk, then sampling per sequence (greedy: no residual kernel).
 int rows_chunks();

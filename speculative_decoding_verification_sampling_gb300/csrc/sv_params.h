@@ -115,88 +115,6 @@ struct ClusterParams {
     uint32_t spin_limit;       // bound on every on-device wait loop
 };
 
-// A float pair as stored in the workspace.
-struct DF2 {
-    float hi, lo;
-};
-
-// Sweep kernel (sv_sweep.cuh): per-sequence decision state (in the region a
-// call must find zeroed) and per-(sequence, position) statistics.
-struct SwSeq {
-    uint32_t lock;     // 1 while a CTA advances the decisions
-    uint32_t front;    // next undecided position
-    uint32_t end;      // 0 while undecided; 1 + j once the sequence ended at position j; 0x80000000 | code on error
-    uint32_t fin;      // 1 once the outputs are written
-};
-// Statistics of one part of one (sequence, position), or of the whole row
-// pair once merged: stochastic: target reference and sum, draft reference
-// and sum (log2 units, sums as float pairs); greedy: mt = maximum, st_hi holds
-// its index's bits.  flags: bit 0 target NaN/+inf, bit 1 draft NaN/+inf.
-struct alignas(16) SwStat {
-    float mt, st_hi, st_lo, md, sd_hi, sd_lo;
-    int flags, pad;
-};
-constexpr int SW_SMAX = 16;   // largest number of parts per row pair
-constexpr int SW_MAXST = 64;  // stages per row (8 KB of one row each)
-constexpr int SW_RPARTS = 1;  // parts of a sampling job (measured best as one: finer parts cost more than they spread)
-// The sweep's global counters, each on its own 128-byte line (they are polled
-// and updated by every CTA): stats items handed out, sampling jobs posted,
-// sampling parts handed out, sequences finished, abort flag, CTAs done.
-enum SweepCounter { SWC_ITEMS = 0, SWC_RES_ALLOC = 32, SWC_RES_CLAIM = 64, SWC_FIN = 96, SWC_ABORT = 128,
-                    SWC_EXIT = 160, SWC_WORDS = 192 };
-constexpr int SW_WARPS = 8;   // consumer warps per CTA
-
-// A residual (or bonus) sampling job, posted by the CTA whose decision ended
-// the sequence; any CTA streams its parts.  flags: bit 0 bonus (q_{K+1}),
-// bit 1 sample q_j itself (the residual mass was 0).
-struct alignas(16) SwRes {
-    int b, j, flags, pad;
-    float Mt, dLhi, dLlo;          // residual coefficients
-    uint32_t vw;                   // the Philox word of the sampling uniform
-    float St_hi, St_lo, R_hi, R_lo;   // target sum (to report R), residual mass of an earlier attempt
-};
-constexpr uint32_t SW_READY = 0x80000000u;   // sw_cnt bit: merged statistics written
-
-// Parts per row pair for a batch of B sequences: enough (position, sequence,
-// part) items to cover the GPU at position 0.
-inline int sweep_parts(int B)
-{
-    int S = 1;
-    while (S < SW_SMAX && (long long)B * S < 512)
-        S <<= 1;
-    return S;
-}
-
-struct SweepParams {
-    const void *target;        // [B][K+1][V]
-    const void *draft;         // [B][K][V] draft logits; nullptr for greedy
-    const int32_t *tokens;     // [B][K]
-    int32_t *out_tokens;       // [B][K+1]
-    int32_t *out_len;          // [B]
-    float *aux_R;              // [B] or nullptr
-    int32_t *aux_status;       // [1] or nullptr
-    uint32_t *ctl;             // [CTL_WORDS] at the start of the workspace
-    uint32_t reset_words;      // 32-bit words from ctl a call leaves zeroed
-    uint32_t *swc;             // [SWC_WORDS] the sweep's counters, one per 128-byte line
-    SwSeq *seq;                // [B]
-    uint32_t *cnt;             // [B][K+1] parts done (| SW_READY once merged)
-    SwStat *part;              // [B][K+1][S]
-    SwStat *stat;              // [B][K+1]
-    SwRes *res;                // [2B] sampling jobs
-    uint32_t *res_ready;       // [2B] 1 once the job is written
-    uint32_t *res_done;        // [2B] parts done
-    DF2 *resm;                 // [2B][SW_MAXST][SW_WARPS] residual mass per (stage, warp) chunk, token order
-    int B, K, V;
-    int S;                     // parts per row pair
-    int span;                  // tokens per part (a multiple of 8)
-    int RS;                    // parts of a sampling job
-    int rspan;                 // tokens per sampling part (a multiple of the stage)
-    int greedy;
-    float c;                   // log2(e) / T
-    uint32_t key0, key1;       // Philox key (seed low, seed high)
-    uint32_t spin_limit;
-    uint32_t n_items;          // (K + 1) * B * S
-};
 
 // Workspace layout for (B, K, V, S); every array starts 256-byte aligned.
 // Row-parallel verification (k_rows.cu): the statistics of one logit row.
@@ -276,8 +194,8 @@ struct RowsParams {
 };
 
 struct WsLayout {
-    size_t ctl, state, res_rec, pair_cnt, res_cnt, fin, errres, sw_ctl, sw_seq, sw_cnt, sw_res_ready, sw_res_done,
-        vr_pair, vr_rej, vr_rowcnt, vr_ctl, vr_dw, vr_jobs, errcode, terminal, gtok, dec, part, seg, sl_lb, sw_part, sw_stat, sw_res, sw_resm,
+    size_t ctl, state, res_rec, pair_cnt, res_cnt, fin, errres,
+        vr_pair, vr_rej, vr_rowcnt, vr_ctl, vr_dw, vr_jobs, errcode, terminal, gtok, dec, part, seg, sl_lb,
         vr_stat, vr_errc, vr_part, vr_segm, vr_lb, total;
     size_t reset_end;   // [ctl, reset_end) holds what a call must find zeroed
     int npt_max, nseg;
@@ -302,11 +220,6 @@ inline WsLayout ws_layout(int B, int K, int V, int S)
     w.res_cnt = o;  o = align256(o + Bz * 4);
     w.fin = o;      o = align256(o + Bz * 4);
     w.errres = o;   o = align256(o + Bz * 4);
-    w.sw_ctl = o;   o = align256(o + SWC_WORDS * 4);
-    w.sw_seq = o;   o = align256(o + Bz * sizeof(SwSeq));
-    w.sw_cnt = o;   o = align256(o + Bz * P * 4);
-    w.sw_res_ready = o; o = align256(o + 2 * Bz * 4);
-    w.sw_res_done = o;  o = align256(o + 2 * Bz * 4);
     w.vr_pair = o;  o = align256(o + Bz * P * 4);
     w.vr_rej = o;   o = align256(o + Bz * 4);
     w.vr_rowcnt = o; o = align256(o + Bz * (2 * P - 1) * 4);
@@ -321,10 +234,6 @@ inline WsLayout ws_layout(int B, int K, int V, int S)
     w.part = o;     o = align256(o + Bz * P * (size_t)w.npt_max * sizeof(Partial));
     w.seg = o;      o = align256(o + Bz * (size_t)w.nseg * sizeof(SegMass));
     w.sl_lb = o;    o = align256(o + (S > 0 ? Bz * (size_t)(w.nseg + 1) * 4 : 0));
-    w.sw_part = o;  o = align256(o + Bz * P * (size_t)sweep_parts(B) * sizeof(SwStat));
-    w.sw_stat = o;  o = align256(o + Bz * P * sizeof(SwStat));
-    w.sw_res = o;   o = align256(o + 2 * Bz * sizeof(SwRes));
-    w.sw_resm = o;  o = align256(o + 2 * Bz * (size_t)SW_MAXST * SW_WARPS * sizeof(DF2));
     w.vr_stat = o;  o = align256(o + Bz * (2 * P - 1) * sizeof(VrStat));
     w.vr_errc = o;  o = align256(o + Bz * P * 4);
     w.vr_part = o;  o = align256(o + Bz * (2 * P - 1) * (size_t)VR_SMAX * sizeof(VrStat));

@@ -28,10 +28,10 @@ def _device():
 
 
 @pytest.fixture(scope="module", autouse=True,
-                params=["auto", "cluster", "sweep", "rows", "rows-stats", "rows-unfused", "general"])
+                params=["auto", "cluster", "rows", "rows-stats", "rows-unfused", "general"])
 def kernel(request):
     """Every case runs under the default dispatch and under each kernel forced
-    in turn: the cluster kernel, the sweep kernel, the row-parallel kernels
+    in turn: the cluster kernel, the row-parallel kernels
     (with the bulk-copy statistics stream, and with the per-position
     statistics launches in its place: "rows-stats") and the chunk-scheduled
     kernel (each falls back to the next for shapes it does not serve);
