@@ -852,9 +852,12 @@ __device__ __noinline__ void vs_commit(const RowsParams &P, int b, int i, int ki
     }
 }
 
-template <class E>
+// DM: the draft kind, fixed per instantiation so that each variant carries
+// only its own stage types -- 0 draft logits, 1 given probabilities.
+template <class E, int DM>
 __global__ void __launch_bounds__(VS_T, VS_CPS) vr_stream(const __grid_constant__ RowsParams P)
 {
+    constexpr bool PROBS = DM == 1;
     pdl_trigger();
     extern __shared__ __align__(128) uint8_t vs_buf[];
     __shared__ unsigned long long full[VS_NS], empty[VS_NS], epf[VS_EPN], epe[VS_EPN], mg[VS_MB];
@@ -881,7 +884,7 @@ __global__ void __launch_bounds__(VS_T, VS_CPS) vr_stream(const __grid_constant_
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    const int nitems = P.B * (P.probs ? K + 1 : 2 * K + 1) * P.parts;
+    const int nitems = P.B * (PROBS ? K + 1 : 2 * K + 1) * P.parts;
 
     if (warp == VS_NCW) {
         // ---- producer
@@ -1001,8 +1004,8 @@ __global__ void __launch_bounds__(VS_T, VS_CPS) vr_stream(const __grid_constant_
             const bool qonly = j == K;
             // tokens of each row per residual stage: half a stage of target
             // logits, or (given probabilities, 4 bytes each) a quarter
-            const int rt = P.probs ? VR2_HALF / 4 : RT;
-            const int des = P.probs ? 4 : E::ES;   // bytes of a draft element
+            const int rt = PROBS ? VR2_HALF / 4 : RT;
+            const int des = PROBS ? 4 : E::ES;   // bytes of a draft element
             const uint8_t *trow =
                 static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + j) * (size_t)V * E::ES;
             const uint8_t *drow =
@@ -1128,7 +1131,7 @@ __global__ void __launch_bounds__(VS_T, VS_CPS) vr_stream(const __grid_constant_
             continue;
         }
         const uint8_t *sb = vs_buf + st * VS_STAGE;
-        if (mt.type == 1 && P.probs) {
+        if (mt.type == 1 && PROBS) {
             // a residual stage with given probabilities: 2048 tokens, one
             // 256-token segment per warp; x_d c = log2 p (lg2 of each
             // probability); a probability that is negative, NaN or +inf puts
@@ -1368,7 +1371,8 @@ __device__ __forceinline__ void sl_pairs(const RowsParams &P, int b, int j, int 
         XD[p] = pk(x[2 * p], x[2 * p + 1]);
 }
 
-template <class E>
+// SLR: the call has a shortlisted draft (its list code is compiled only then).
+template <class E, bool SLR>
 __global__ void __launch_bounds__(VRT, E::ES == 2 ? 3 : 1) vr_residual(const __grid_constant__ RowsParams P)
 {
     pdl_wait();
@@ -1390,7 +1394,7 @@ __global__ void __launch_bounds__(VRT, E::ES == 2 ? 3 : 1) vr_residual(const __g
         return;
     const int j = sm_j;
     const bool qonly = j == K;
-    const bool slist = P.sl && !qonly;   // draft values come from the shortlist
+    const bool slist = SLR && !qonly;   // draft values come from the shortlist
     const ResK k = vr_coef(P, b, j);
     const uint8_t *trow = static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + j) * (size_t)V * E::ES;
     const uint8_t *drow =
@@ -1875,17 +1879,19 @@ int fused_mode()
 template <class E>
 cudaError_t launch_stream(RowsParams P, int sms, cudaStream_t stream)
 {
-    static bool attr_set[kMaxDevicesRows] = {};
+    static bool attr_set[kMaxDevicesRows][2] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
+    const int dm = P.probs ? 1 : 0;
+    auto kern = dm ? vr_stream<E, 1> : vr_stream<E, 0>;
     const int smem = VS_NS * VS_STAGE;
-    if (dev < kMaxDevicesRows && !attr_set[dev]) {
-        e = cudaFuncSetAttribute(vr_stream<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (dev < kMaxDevicesRows && !attr_set[dev][dm]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess)
             return e;
-        attr_set[dev] = true;
+        attr_set[dev][dm] = true;
     }
     const int ncta = sms * VS_CPS;
     const long long rows = (long long)P.B * (2 * P.K + 1);
@@ -1899,7 +1905,7 @@ cudaError_t launch_stream(RowsParams P, int sms, cudaStream_t stream)
         S = std::max(1, std::min(VS_SMAX, std::atoi(ev)));
     P.span = ((P.V + S - 1) / S + 7) / 8 * 8;
     P.parts = (P.V + P.span - 1) / P.span;
-    vr_stream<E><<<ncta, VS_T, smem, stream>>>(P);
+    kern<<<ncta, VS_T, smem, stream>>>(P);
     return cudaGetLastError();
 }
 
@@ -1951,7 +1957,8 @@ cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream, int &launches)
         // trip per step: four times the CTAs per sequence, a quarter of the steps
         if (P.sl)
             P.nch = 4 * VR_NCH;
-        e = launch_after(vr_residual<E>, P.B * P.nch, VRT, 0, stream, P);
+        e = P.sl ? launch_after(vr_residual<E, true>, P.B * P.nch, VRT, 0, stream, P)
+                 : launch_after(vr_residual<E, false>, P.B * P.nch, VRT, 0, stream, P);
         launches += 1;
         if (e != cudaSuccess)
             return e;
