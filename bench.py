@@ -381,8 +381,9 @@ def run_gb300(args) -> int:
         all_rows_bytes = (2 * K + 1) * B * V * 2
         mean_len = float(ref_l.double().mean())
 
-        ev_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        # the K calls run back to back on one stream between one pair of events
+        # (an event between two calls would keep the next call's launch from
+        # overlapping the end of the one before it)
         start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         launches0 = sv.spec_launch_count()
         barrier(dev)
@@ -390,9 +391,7 @@ def run_gb300(args) -> int:
         with torch.cuda.stream(stream):
             start.record(stream)
             for i in range(args.steps):
-                ev_s[i].record(stream)
                 call(i)
-                ev_e[i].record(stream)
             stop.record(stream)
         torch.cuda.synchronize(dev)
         barrier(dev)
@@ -400,10 +399,9 @@ def run_gb300(args) -> int:
         clock_samples = clocks.samples()
 
     elapsed_ms = start.elapsed_time(stop)
-    kernel_ms = [a.elapsed_time(b) for a, b in zip(ev_s, ev_e)]
+    mean_kernel_s = elapsed_ms / args.steps / 1e3   # this rank's mean duration of one call
     elapsed_ms = max_over_ranks(elapsed_ms, dev)
     value = world * B * K * args.steps / (elapsed_ms / 1e3)
-    mean_kernel_s = statistics.fmean(kernel_ms) / 1e3
 
     # end to end: pinned host inputs in, results out, every step
     pin_t, pin_d, pin_k = host_t.pin_memory(), host_d.pin_memory(), host_k.pin_memory()
@@ -447,7 +445,8 @@ def run_gb300(args) -> int:
         line["roofline"] = {
             "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": recorded_traffic(digest=digest), "peak_source": src,
-            "kernel": PATH_KERNELS, "scope": "the whole verification call (all its kernels)",
+            "kernel": PATH_KERNELS, "scope": "the whole verification call (all its kernels), the mean over "
+                                             "the timed calls run back to back",
             "algorithmic_bytes_per_launch": alg_bytes, "mean_kernel_us": mean_kernel_s * 1e6,
             "all_rows_bytes_per_launch": all_rows_bytes,
             "all_rows_gbs": all_rows_bytes / mean_kernel_s / 1e9,
@@ -503,7 +502,20 @@ def config_points(dev, stream, calls: int = 40):
     out = []
     errors = []
 
-    def timed(fn):
+    def on_copies(call, *tensors):
+        """call(*inputs) on device copies of the inputs, enough that a back to
+        back run reads at least 300 MB of distinct inputs; None for inputs under
+        16 MB (those are timed cold only)."""
+        nb = sum(x.numel() * x.element_size() for x in tensors)
+        if nb < 16e6:
+            return None
+        sets = [tuple(x.clone() for x in tensors) for _ in range(max(0, math.ceil(300e6 / nb) - 1))]
+        return [lambda x=x: call(*x) for x in sets]
+
+    def timed(fn, more=None):
+        """Mean device time of one call: cold (each call alone, after a read of
+        256 MB that evicts the L2), and, given calls on copies of the inputs,
+        back to back over the copies in turn (the host queued ahead first)."""
         # the inputs were made on the default stream: the calls come after them
         stream.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(stream):
@@ -519,9 +531,22 @@ def config_points(dev, stream, calls: int = 40):
                 r = fn()
                 ee[n].record(stream)
             stream.synchronize()
-        return statistics.fmean(a.elapsed_time(b) for a, b in zip(es, ee)) * 1e3, r
+            cold = statistics.fmean(a.elapsed_time(b) for a, b in zip(es, ee)) * 1e3
+            b2b = None
+            if more is not None:
+                fns = [fn, *more]
+                for f in fns:
+                    f()
+                torch.cuda._sleep(50_000_000)   # a wait on the device while the host queues the calls
+                es[0].record(stream)
+                for n in range(4 * calls):
+                    fns[n % len(fns)]()
+                ee[0].record(stream)
+                stream.synchronize()
+                b2b = es[0].elapsed_time(ee[0]) * 1e3 / (4 * calls)
+        return cold, r, b2b
 
-    def record(name, cfg, us, res, elem_bytes, greedy=False, extra_bytes=0, all_rows=None, units=None):
+    def record(name, cfg, us, res, elem_bytes, greedy=False, extra_bytes=0, all_rows=None, units=None, b2b=None):
         B, K, V = cfg["B"], cfg["K"], cfg["V"]
         acc = res[1].cpu().tolist()
         bad = [L for L in acc if L < 0]
@@ -542,6 +567,9 @@ def config_points(dev, stream, calls: int = 40):
                "roofline": {"bound": "hbm", "achieved": rule / us / 1e3, "peak": peak, "unit": "GB/s",
                             "frac": rule / us / 1e3 / peak, "peak_source": src,
                             "all_rows_gbs": allb / us / 1e3}}
+        if b2b is not None:
+            rec["back_to_back"] = {"us_per_call": b2b, "value": n_units / (b2b * 1e-6),
+                                   "rule_gbs": rule / b2b / 1e3, "frac": rule / b2b / 1e3 / peak}
         out.append(rec)
         return rec
 
@@ -549,60 +577,79 @@ def config_points(dev, stream, calls: int = 40):
     # 1. B=1 K=4 V=32000 fp32
     c = synth.small_stochastic(seed=0, device=dev)
     t, d, k = c["target"], c["draft"], c["draft_tokens"]
-    us, r = timed(lambda: sv.spec_verify(t, d, k, 1.0, VERIFY_SEED, stream=stream))
+    us, r, _ = timed(lambda: sv.spec_verify(t, d, k, 1.0, VERIFY_SEED, stream=stream))
     record("small: B=1 K=4 V=32000 fp32 T=1, target N(0, 2^2), draft = target + N(0, 0.5^2)", c, us, r, 4)
     # 2. greedy B=64 K=5 V=128256 bf16
     c = synth.greedy(device=dev)
     t, k = c["target"], c["draft_tokens"]
-    us, r = timed(lambda: sv.spec_verify_greedy(t, k, stream=stream))
+    more = on_copies(lambda a, b: sv.spec_verify_greedy(a, b, stream=stream), t, k)
+    us, r, b2b = timed(lambda: sv.spec_verify_greedy(t, k, stream=stream), more)
     record("greedy: B=64 K=5 V=128256 bf16 T=0, target N(0, 3^2), drafts = argmax with probability 0.8",
-           c, us, r, 2, greedy=True)
+           c, us, r, 2, greedy=True, b2b=b2b)
+    del more
     # 3. Zipf B=32 K=7 V=152064 bf16 T=0.7 at three draft noises
     for sigma in (0.25, 0.5, 1.0):
         c = synth.zipf(sigma=sigma, device=dev)
         t, d, k = c["target"], c["draft"], c["draft_tokens"]
-        us, r = timed(lambda: sv.spec_verify(t, d, k, c["T"], VERIFY_SEED, stream=stream))
-        rec = record(f"zipf: B=32 K=7 V=152064 bf16 T=0.7, draft = target + N(0, {sigma}^2)", c, us, r, 2)
+        more = on_copies(lambda a, b, e: sv.spec_verify(a, b, e, c["T"], VERIFY_SEED, stream=stream), t, d, k)
+        us, r, b2b = timed(lambda: sv.spec_verify(t, d, k, c["T"], VERIFY_SEED, stream=stream), more)
+        rec = record(f"zipf: B=32 K=7 V=152064 bf16 T=0.7, draft = target + N(0, {sigma}^2)", c, us, r, 2, b2b=b2b)
         rec["sigma"] = sigma
+        del more
     # 4. shortlisted draft, B=64 K=6 V=262144, 32768-token per-sequence lists
     c = synth.shortlist(device=dev)
     Bs, Ks, Vs = c["B"], c["K"], c["V"]
     S = c["shortlist"].shape[1]
     t, d, sl, k = c["target"], c["draft"], c["shortlist"], c["draft_tokens"]
-    us, r = timed(lambda: sv.spec_verify_shortlist(t, d, sl, k, 1.0, VERIFY_SEED, stream=stream))
+    more = on_copies(lambda a, b, e, f: sv.spec_verify_shortlist(a, b, e, f, 1.0, VERIFY_SEED, stream=stream),
+                     t, d, sl, k)
+    us, r, b2b = timed(lambda: sv.spec_verify_shortlist(t, d, sl, k, 1.0, VERIFY_SEED, stream=stream), more)
+    del more
     acc = r[1].cpu().tolist()
     # rule bytes: target rows 0..j at V, draft rows 0..min(j, K-1) at S, and the sequence's list once
     need = sum((min(int(L), Ks) + 1) * Vs * 2 + min(int(L) + 1, Ks) * S * 2 for L in acc) + Bs * S * 4
     rec = record("shortlist (compact): B=64 K=6 V=262144 bf16 T=1, Zipf target, 8 of 64 clusters per sequence "
                  "(S=32768), draft = target + N(0, 0.5^2) on the list", c, us, r, 2,
-                 all_rows=Bs * (Ks + 1) * Vs * 2 + Bs * Ks * S * 2 + Bs * S * 4)
+                 all_rows=Bs * (Ks + 1) * Vs * 2 + Bs * Ks * S * 2 + Bs * S * 4, b2b=b2b)
     rec["rule_bytes"] = need
     rec["roofline"].update(achieved=need / us / 1e3, frac=need / us / 1e3 / peak)
+    if b2b is not None:
+        rec["back_to_back"].update(rule_gbs=need / b2b / 1e3, frac=need / b2b / 1e3 / peak)
     full = torch.full((Bs, Ks, Vs), float("-inf"), dtype=torch.bfloat16, device=dev)
     full.scatter_(2, sl.long().unsqueeze(1).expand(Bs, Ks, S), d)
-    us, r = timed(lambda: sv.spec_verify(t, full, k, 1.0, VERIFY_SEED, stream=stream))
-    record("shortlist (full-vocabulary draft, -inf off the list): B=64 K=6 V=262144 bf16 T=1", c, us, r, 2)
+    more = on_copies(lambda a, b, e: sv.spec_verify(a, b, e, 1.0, VERIFY_SEED, stream=stream), t, full, k)
+    us, r, b2b = timed(lambda: sv.spec_verify(t, full, k, 1.0, VERIFY_SEED, stream=stream), more)
+    del more
+    record("shortlist (full-vocabulary draft, -inf off the list): B=64 K=6 V=262144 bf16 T=1", c, us, r, 2,
+           b2b=b2b)
     del full, t, d, sl, k, c
     # 5. throughput sweep
     for Kp in (4, 8):
         for Bp in (1, 8, 64, 256, 512):
             c = synth.throughput(B=Bp, K=Kp, seed=DATA_SEED, device=dev)
             t, d, k = c["target"], c["draft"], c["draft_tokens"]
-            us, r = timed(lambda: sv.spec_verify(t, d, k, T1, VERIFY_SEED, stream=stream))
-            record(f"throughput: B={Bp} K={Kp} V=128256 bf16 T=1", c, us, r, 2)
-            del t, d, k, c
+            more = on_copies(lambda a, b, e: sv.spec_verify(a, b, e, T1, VERIFY_SEED, stream=stream), t, d, k)
+            us, r, b2b = timed(lambda: sv.spec_verify(t, d, k, T1, VERIFY_SEED, stream=stream), more)
+            record(f"throughput: B={Bp} K={Kp} V=128256 bf16 T=1", c, us, r, 2, b2b=b2b)
+            del t, d, k, c, more
     # draft probabilities at B=256 K=4
     c = synth.throughput(B=256, K=4, seed=DATA_SEED, device=dev)
     t, k = c["target"], c["draft_tokens"]
     probs = torch.softmax(c["draft"].float(), dim=-1)
     del c["draft"]
-    us, r = timed(lambda: sv.spec_verify(t, probs, k, T1, VERIFY_SEED, draft_is_probs=True, stream=stream))
+    more = on_copies(lambda a, b, e: sv.spec_verify(a, b, e, T1, VERIFY_SEED, draft_is_probs=True, stream=stream),
+                     t, probs, k)
+    us, r, b2b = timed(lambda: sv.spec_verify(t, probs, k, T1, VERIFY_SEED, draft_is_probs=True, stream=stream),
+                       more)
+    del more
     acc = r[1].cpu().tolist()
     need = sum((min(int(L), 4) + 1) * V * 2 + min(int(L) + 1, 4) * V * 4 for L in acc)
     rec = record("draft probabilities: B=256 K=4 V=128256, bf16 target logits, fp32 draft probabilities", c, us, r,
-                 2, all_rows=256 * 5 * V * 2 + 256 * 4 * V * 4)
+                 2, all_rows=256 * 5 * V * 2 + 256 * 4 * V * 4, b2b=b2b)
     rec["rule_bytes"] = need
     rec["roofline"].update(achieved=need / us / 1e3, frac=need / us / 1e3 / peak)
+    if b2b is not None:
+        rec["back_to_back"].update(rule_gbs=need / b2b / 1e3, frac=need / b2b / 1e3 / peak)
     if errors:
         out.append({"data_errors": errors})
     return out

@@ -106,13 +106,6 @@ __device__ __forceinline__ uint32_t vr_atom_add(uint32_t *p, uint32_t v)
     return old;
 }
 
-// Programmatic dependent launch: a kernel launched with it may start while
-// the one before it in the stream is finishing; pdl_wait() blocks until that
-// kernel has completed and its writes are visible (a no-op otherwise), and
-// pdl_trigger() lets the next kernel start launching.
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
 // Decide position i of sequence b from the statistics of its target row t and
 // draft row d (the drafted token dt).  Returns 0 and sets accept, or a status
 // code.  Checks in the oracle's order: token, target row, draft row.
@@ -859,6 +852,7 @@ __global__ void __launch_bounds__(VS_T, VS_CPS) vr_stream(const __grid_constant_
 {
     constexpr bool PROBS = DM == 1;
     pdl_trigger();
+    pdl_wait();
     extern __shared__ __align__(128) uint8_t vs_buf[];
     __shared__ unsigned long long full[VS_NS], empty[VS_NS], epf[VS_EPN], epe[VS_EPN], mg[VS_MB];
     __shared__ VsMeta meta[VS_NS];
@@ -1488,6 +1482,7 @@ template <class E>
 __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsParams P)
 {
     pdl_wait();
+    pdl_trigger();
     constexpr int NW = VST / 32;
     __shared__ int sm_seg, sm_last[NW], sm_x, sm_e[32];
     __shared__ uint32_t sm_m, sm_tf;
@@ -1802,24 +1797,6 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
     }
 }
 
-// Launch kern(P) so that it may begin while the previous kernel in the
-// stream finishes (it waits for that kernel's results with pdl_wait).
-template <class Kern>
-cudaError_t launch_after(Kern kern, int grid, int block, int smem, cudaStream_t stream, const RowsParams &P)
-{
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3((unsigned)block);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, P);
-}
-
 // A vr_stats launch over `rows` rows: each row is cut into parts so that the
 // launch brings about as many threads as the GPU holds (the bytes in flight
 // grow with them), with parts of at least 4096 tokens.
@@ -1844,10 +1821,8 @@ cudaError_t launch_stats(RowsParams P, int pos, int npos, int sms, cudaStream_t 
     P.parts = (P.V + P.span - 1) / P.span;
     // the first launch of a call waits for whatever came before it in full
     if (P.sl)
-        return pos == 0 ? (vr_stats<E, VST_T, true><<<rows * P.parts, VST_T, 0, stream>>>(P), cudaGetLastError())
-                        : launch_after(vr_stats<E, VST_T, true>, rows * P.parts, VST_T, 0, stream, P);
-    return pos == 0 ? (vr_stats<E, VST_T, false><<<rows * P.parts, VST_T, 0, stream>>>(P), cudaGetLastError())
-                    : launch_after(vr_stats<E, VST_T, false>, rows * P.parts, VST_T, 0, stream, P);
+        return launch_after(vr_stats<E, VST_T, true>, rows * P.parts, VST_T, 0, stream, P);
+    return launch_after(vr_stats<E, VST_T, false>, rows * P.parts, VST_T, 0, stream, P);
 }
 
 // Whether vr_stream serves the call: stochastic, draft logits, aligned rows.
@@ -1905,8 +1880,7 @@ cudaError_t launch_stream(RowsParams P, int sms, cudaStream_t stream)
         S = std::max(1, std::min(VS_SMAX, std::atoi(ev)));
     P.span = ((P.V + S - 1) / S + 7) / 8 * 8;
     P.parts = (P.V + P.span - 1) / P.span;
-    kern<<<ncta, VS_T, smem, stream>>>(P);
-    return cudaGetLastError();
+    return launch_after(kern, ncta, VS_T, smem, stream, P);
 }
 
 template <class E>

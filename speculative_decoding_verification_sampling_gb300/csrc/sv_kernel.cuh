@@ -78,6 +78,13 @@ __device__ __forceinline__ void mbar_init(unsigned long long *bar, uint32_t coun
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(saddr(bar)), "r"(count) : "memory");
 }
+// Programmatic dependent launch: a kernel launched with it may start while
+// the one before it in the stream is finishing; pdl_wait() blocks until that
+// kernel has completed and its writes are visible (a no-op otherwise), and
+// pdl_trigger() lets the next kernel start launching.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_arrive(unsigned long long *bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(saddr(bar)) : "memory");

@@ -6,6 +6,25 @@
 
 namespace sv {
 
+// Launch kern(P) with programmatic dependent launch: it may begin while the
+// previous kernel in the stream finishes, and waits for that kernel's results
+// itself (griddepcontrol.wait before its first access to global memory).
+template <class Kern, class Par>
+cudaError_t launch_after(Kern kern, int grid, int block, int smem, cudaStream_t stream, const Par &P)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3((unsigned)block);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
 struct KernelEntry {
     cudaError_t (*launch)(const Params &P, int grid, cudaStream_t stream);
     cudaError_t (*occupancy)(int *ctas_per_sm);

@@ -36,8 +36,9 @@ def kernel(request):
     statistics launches in its place: "rows-stats") and the chunk-scheduled
     kernel (each falls back to the next for shapes it does not serve);
     "rows" runs the residual pass inside the statistics stream at every size,
-    "rows-unfused" keeps it in its own launch."""
-    keys = ("SPECVERIFY_KERNEL", "SPECVERIFY_ROWS_STREAM", "SPECVERIFY_ROWS_FUSED")
+    "rows-unfused" keeps it in its own launch and runs greedy calls on the
+    register-load argmax kernel even where rows are aligned for bulk copies."""
+    keys = ("SPECVERIFY_KERNEL", "SPECVERIFY_ROWS_STREAM", "SPECVERIFY_ROWS_FUSED", "SPECVERIFY_GREEDY_CFG")
     saved = {k: os.environ.get(k) for k in keys}
     os.environ["SPECVERIFY_KERNEL"] = "rows" if request.param.startswith("rows") else request.param
     if request.param == "rows-stats":
@@ -46,6 +47,7 @@ def kernel(request):
         os.environ["SPECVERIFY_ROWS_FUSED"] = "1"
     if request.param == "rows-unfused":
         os.environ["SPECVERIFY_ROWS_FUSED"] = "0"
+        os.environ["SPECVERIFY_GREEDY_CFG"] = "256,2"
     yield request.param
     for k, v in saved.items():
         if v is None:
@@ -111,6 +113,39 @@ def test_greedy_full_size_bit_exact():
 ])
 def test_greedy_edge_shapes(B, K, V, dtype):
     cfg = synth.greedy(B=B, K=K, V=V, dtype=dtype, seed=B * 100 + K)
+    t, l = _gpu_run(cfg, 0)
+    ref = _oracle(cfg, 0)
+    np.testing.assert_array_equal(l, ref["accept_len"])
+    np.testing.assert_array_equal(t, ref["tokens"])
+
+
+@pytest.mark.parametrize("B,K,V,dtype", [
+    (96, 3, 32768, torch.bfloat16),    # 2.5 rows per SM, rows of exactly four copy stages
+    (48, 7, 16388, torch.float32),     # a last stage of 16 bytes
+    (256, 5, 40000, torch.bfloat16),   # several waves of CTAs
+])
+def test_greedy_many_rows(B, K, V, dtype):
+    """Many aligned rows of 64 KB or more run on the bulk-copy kernel, one CTA
+    per row (the "rows-unfused" pass runs them on the register-load kernel)."""
+    cfg = _cached(("gm", B, K, V), lambda: synth.greedy(B=B, K=K, V=V, dtype=dtype, seed=B + V))
+    ref = _cached(("gm-ref", B, K, V), lambda: _oracle(cfg, 0))
+    t, l = _gpu_run(cfg, 0)
+    np.testing.assert_array_equal(l, ref["accept_len"])
+    np.testing.assert_array_equal(t, ref["tokens"])
+
+
+@pytest.mark.parametrize("B,V", [(40, 20000), (64, 40000)])
+def test_greedy_heavy_ties_across_parts(B, V):
+    """Integer logits in [-2, 2]: the maximum appears in many parts of a row
+    (B=40: several parts per row; B=64: one CTA per row, many warps); the
+    lowest index must win."""
+    g = torch.Generator().manual_seed(6)
+    K = 5
+    target = torch.randint(-2, 3, (B, K + 1, V), generator=g).to(torch.bfloat16)
+    target[:, :, :V // 2] = torch.clamp(target[:, :, :V // 2], max=1)   # the first 2s sit past the middle
+    best = torch.argmax(target[:, :K].float(), dim=-1)
+    tokens = torch.where(torch.rand(B, K, generator=g) < 0.8, best, torch.randint(0, V, (B, K), generator=g))
+    cfg = dict(target=target, draft=None, draft_tokens=tokens.to(torch.int32), T=0.0)
     t, l = _gpu_run(cfg, 0)
     ref = _oracle(cfg, 0)
     np.testing.assert_array_equal(l, ref["accept_len"])
