@@ -401,8 +401,14 @@ spec_status_t run(int mode, const void *target, spec_dtype_t tdt, const void *dr
         // cluster kernel's one position at a time (B = 1, K = 4 bf16: 39 us
         // against 53 us; B = 8, K = 8: 51 us against 64 us; B = 8, K = 4 stays
         // with the cluster kernel, 43 us against 45 us)
+        // and small calls whose rows all fit the shared memory of the GPU's
+        // resident CTAs
+        const int es = tdt == SPEC_BF16 ? 2 : 4;
+        const bool aligned = ((long long)V * es) % 16 == 0 && reinterpret_cast<uintptr_t>(target) % 16 == 0 &&
+                             reinterpret_cast<uintptr_t>(draft) % 16 == 0;
         if (kc == KC_AUTO && mode == sv::MODE_STOCH &&
-            ((long long)B * (2 * K + 1) >= kRowsMinRows || B <= 2 || K >= 6)) {
+            ((long long)B * (2 * K + 1) >= kRowsMinRows || B <= 2 || K >= 6 ||
+             (aligned && sv::rows_resident_fits(B, K, V, tdt == SPEC_BF16 ? 1 : 0)))) {
             const spec_status_t rs = run_rows(false, target, tdt, draft, tokens, B, K, V, T, seed, out_tokens,
                                               out_len, workspace, L, aux, stream);
             if (rs != SPEC_ERR_UNSUPPORTED)

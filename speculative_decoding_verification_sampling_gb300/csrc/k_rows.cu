@@ -287,7 +287,7 @@ __device__ __noinline__ void vr_commit(const RowsParams &P, size_t ridx, int b, 
         // completing the sequence's end posts its residual job
         const unsigned long long bits = (1ull << i) | ((ends || i == K) ? (1ull << (32 + i)) : 0ull);
         const unsigned long long old = vr_atom_or64(P.dw + b, bits);
-        if (!vr_ended(old) && vr_ended(old | bits))
+        if (P.fused == 1 && !vr_ended(old) && vr_ended(old | bits))
             vr_post_end(P, b, old | bits);
     }
 }
@@ -1476,6 +1476,236 @@ __global__ void __launch_bounds__(VRT, E::ES == 2 ? 3 : 1) vr_residual(const __g
     }
 }
 
+// ---------------------------------------------------------------- 2b. small calls, rows resident
+// When every row of the call fits in the shared memory of the GPU's resident
+// CTAs, one cooperative launch reads each row once and keeps it: CTA
+// (b, i, part) copies part `part` of target row i and draft row i of sequence
+// b (position K: the target row alone) into shared memory with cp.async.bulk,
+// reduces both, and commits the part (rs_commit: the last part of a position
+// to count merges both rows and decides it, and the decision word records
+// decided and ending positions).  Every CTA then waits (bounded) for its
+// sequence's end; the parts of the pair the sequence ended at form the
+// residual masses of their 256-token segments from the rows still in shared
+// memory, and the others leave.  vr_sample draws the token.  Nothing is read
+// twice, and a call's latency is one copy, one commit chain and one pass over
+// shared memory.
+constexpr int VRS_T = 256;          // threads of a resident CTA (the slice reductions' block size)
+constexpr int VRS_SMEM = 65536;     // a part of both rows of a position
+static_assert(VRS_T == CL_THREADS, "thread_stats strides by CL_THREADS");
+
+__device__ __forceinline__ unsigned long long ld_acq64(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// One part of one row in shared memory (n tokens) as a part record: reference,
+// sum, flags, and the drafted token's logit when it lies in the part.
+template <class E>
+__device__ VrStat rs_part_stats(const uint8_t *base, int n, int t0, int dt, float c, float *sm_m, float *sm_hi,
+                                float *sm_lo, int *sm_f, int tid)
+{
+    constexpr int NW = VRS_T / 32;
+    const int lane = tid & 31, warp = tid >> 5;
+    float mc, sc;
+    int fl = 0;
+    thread_stats<E>(base, n, tid, c, mc, sc, fl, VR_BAD);
+    float M;
+    DF S;
+    merge_ms<32>(mc, DF{sc, 0.0f}, c, M, S);
+    fl = warp_or(fl);
+    if (lane == 0) {
+        sm_m[warp] = M;
+        sm_hi[warp] = S.hi;
+        sm_lo[warp] = S.lo;
+        sm_f[warp] = fl;
+    }
+    __syncthreads();
+    VrStat r{};
+    const bool in = lane < NW;
+    merge_ms<NW>(in ? sm_m[lane] : -F_INF, in ? DF{sm_hi[lane], sm_lo[lane]} : DF{0.0f, 0.0f}, c, M, S);
+    r.m = M;
+    r.s_hi = S.hi;
+    r.s_lo = S.lo;
+    r.flags = warp_or(in ? sm_f[lane] : 0);
+    if ((unsigned)(dt - t0) < (unsigned)n) {
+        const int o = dt - t0;
+        r.zd = E::ES == 2 ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t *>(base)[o] << 16)
+                          : reinterpret_cast<const float *>(base)[o];
+        r.flags |= VR_HASD;
+    }
+    __syncthreads();   // the shared partials are free again
+    return r;
+}
+
+// Warp 0 of a resident CTA: records its part of the position's rows (st, and
+// sd when the position has a draft row) and counts it, once per CTA; the last
+// part to count merges every part of both rows in one round trip (lane h
+// loads target part h, lane 8 + h draft part h; S <= 8), writes the rows'
+// statistics, decides the position and records it in the decision word.
+__device__ __noinline__ void rs_commit(const RowsParams &P, int b, int i, int part, int dt, VrStat st, VrStat sd,
+                                       bool two, int lane)
+{
+    const int K = P.K, S = P.parts;
+    const size_t rt = (size_t)b * (2 * K + 1) + i, rd = (size_t)b * (2 * K + 1) + K + 1 + i;
+    uint32_t prev = 0;
+    if (lane == 0) {
+        P.vpart[rt * VR_SMAX + part] = st;
+        if (two)
+            P.vpart[rd * VR_SMAX + part] = sd;
+        prev = vr_atom_add(P.pair + (size_t)b * (K + 1) + i, 1u);
+    }
+    if (__shfl_sync(0xffffffffu, prev, 0) != (uint32_t)(S - 1))
+        return;
+    __syncwarp();   // the other lanes read the records after lane 0's acquire
+    const int h = lane & 7;
+    const bool isd = lane >= 8;
+    float m = -F_INF, z = 0.0f;
+    DF sv{0.0f, 0.0f};
+    int f = 0;
+    if (lane < 16 && h < S && (!isd || two)) {
+        const VrStat *pp = P.vpart + (isd ? rd : rt) * VR_SMAX + h;
+        const float4 a = __ldcg(reinterpret_cast<const float4 *>(pp));
+        z = __ldcg(&pp->zd);
+        m = a.x;
+        sv = DF{a.y, a.z};
+        f = __float_as_int(a.w);
+    }
+    float M;
+    DF Sm;
+    merge_ms<8>(m, sv, 1.0f, M, Sm);   // lanes 0-7: the target row, 8-15: the draft row
+    int fo = f;
+#pragma unroll
+    for (int o = 4; o; o >>= 1)
+        fo |= __shfl_xor_sync(0xffffffffu, fo, o);
+    // the drafted token's logit, from the part holding it
+    const uint32_t hd = __ballot_sync(0xffffffffu, (f & VR_HASD) != 0);
+    const int srcT = __ffs(hd & 0xffu) - 1, srcD = __ffs(hd & 0xff00u) - 1;
+    const float zT = __shfl_sync(0xffffffffu, z, srcT < 0 ? 0 : srcT);
+    const float zD = __shfl_sync(0xffffffffu, z, srcD < 0 ? 8 : srcD);
+    const float MD = __shfl_sync(0xffffffffu, M, 8), hD = __shfl_sync(0xffffffffu, Sm.hi, 8),
+                lD = __shfl_sync(0xffffffffu, Sm.lo, 8);
+    const int fD = __shfl_sync(0xffffffffu, fo, 8);
+    if (lane != 0)
+        return;
+    const VrStat t{M, Sm.hi, Sm.lo, fo, srcT < 0 ? 0.0f : zT, 0, 0, 0};
+    const VrStat d{MD, hD, lD, fD, srcD < 0 ? 0.0f : zD, 0, 0, 0};
+    P.stat[rt] = t;
+    if (two)
+        P.stat[rd] = d;
+    bool acc = false;
+    const int code = vr_decide(P, b, i, dt, t, d, acc);
+    const bool ends = code || (!acc && i < K);
+    if (ends) {
+        P.errc[(size_t)b * (K + 1) + i] = code;
+        atomicOr(P.rej + b, 1u << i);
+    }
+    const unsigned long long bits = (1ull << i) | ((ends || i == K) ? (1ull << (32 + i)) : 0ull);
+    (void)vr_atom_or64(P.dw + b, bits);
+}
+
+template <class E>
+__global__ void __launch_bounds__(VRS_T) vr_resident(const __grid_constant__ RowsParams P)
+{
+    constexpr int NW = VRS_T / 32;
+    extern __shared__ __align__(128) uint8_t rs_buf[];
+    __shared__ unsigned long long bar;
+    __shared__ float sm_m[NW], sm_hi[NW], sm_lo[NW];
+    __shared__ int sm_f[NW], sm_j;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_trigger();   // vr_sample's CTAs may launch now and wait for this launch to finish
+    const int K = P.K, V = P.V, S = P.parts;
+    const int part = (int)blockIdx.x % S, pi = (int)blockIdx.x / S;
+    const int b = pi / (K + 1), i = pi - b * (K + 1);
+    const bool two = i < K;   // a position with a draft row
+    const int t0 = part * P.span, n = min(P.span, V - t0);
+    uint8_t *ts = rs_buf, *ds = rs_buf + (size_t)P.span * E::ES;
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        const uint32_t nb = (uint32_t)n * E::ES;
+        mbar_arrive_tx(&bar, two ? 2 * nb : nb);
+        const uint8_t *tr =
+            static_cast<const uint8_t *>(P.target) + (((size_t)b * (K + 1) + i) * (size_t)V + t0) * E::ES;
+        const uint8_t *dr = two ? static_cast<const uint8_t *>(P.draft) + (((size_t)b * K + i) * (size_t)V + t0) * E::ES
+                                : nullptr;
+        for (uint32_t o = 0; o < nb; o += 16384u) {
+            const uint32_t m = min(16384u, nb - o);
+            bulk_g2s(ts + o, tr + o, m, &bar);
+            if (two)
+                bulk_g2s(ds + o, dr + o, m, &bar);
+        }
+    }
+    const int dt = two ? __ldg(P.tokens + (size_t)b * K + i) : -1;
+    __syncthreads();
+    if (!__syncthreads_and(ring_wait(&bar, 0u, P.spin_limit))) {
+        // the copies did not land in time: no commit (the call reports a
+        // timeout); wait for them before leaving
+        if (tid == 0) {
+            atomicExch(P.vctl + VC_TIMEOUT * VC_LINE, 1u);
+            (void)mbar_wait(&bar, 0u, DRAIN_LIMIT, nullptr);
+        }
+        return;
+    }
+    const VrStat st = rs_part_stats<E>(ts, n, t0, dt, P.c, sm_m, sm_hi, sm_lo, sm_f, tid);
+    VrStat sd{};
+    if (two)
+        sd = rs_part_stats<E>(ds, n, t0, dt, P.c, sm_m, sm_hi, sm_lo, sm_f, tid);
+    if (warp == 0)
+        rs_commit(P, b, i, part, dt, st, sd, two, lane);
+    if (tid == 0) {
+        // the sequence's end: the first ending position, every position up to
+        // it decided (bounded: giving up reports a timeout for the call)
+        int j = -1;
+        for (uint32_t it = 0; it <= P.spin_limit; ++it) {
+            const unsigned long long w = ld_acq64(P.dw + b);
+            if (vr_ended(w)) {
+                j = __ffs((uint32_t)(w >> 32)) - 1;
+                break;
+            }
+            if (it > 16)
+                __nanosleep(64);
+        }
+        if (j < 0)
+            atomicExch(P.vctl + VC_TIMEOUT * VC_LINE, 1u);
+        else if (j == i && ((__ldcg(P.rej + b) >> j) & 1u) && __ldcg(P.errc + (size_t)b * (K + 1) + j))
+            j = -1;   // ended in error: no residual
+        sm_j = j;
+    }
+    __syncthreads();
+    if (sm_j != i)
+        return;
+    // the residual masses (r', q') of this part's 256-token segments
+    const VrStat tS = ld_vrstat(P.stat + (size_t)b * (2 * K + 1) + i);
+    const VrStat dS = two ? ld_vrstat(P.stat + (size_t)b * (2 * K + 1) + K + 1 + i) : VrStat{};
+    const ResK k = res_coef(P, tS, dS, i);
+    const bool qonly = !two;
+    const uint4 ninf = E::neg_inf();
+    const int nsg = (n + VSEG - 1) / VSEG;
+    VrSeg *sg = P.segm + (size_t)b * P.nseg + t0 / VSEG;
+    for (int q = warp; q < nsg; q += NW) {
+        const int x = q * VSEG + lane * 8;   // token within the part
+        Unit<E> ut, ud;
+        const uint4 *pt = reinterpret_cast<const uint4 *>(ts + (size_t)x * E::ES);
+        const uint4 *pd = reinterpret_cast<const uint4 *>(ds + (size_t)x * E::ES);
+        ut.a = x < n ? pt[0] : ninf;
+        ud.a = qonly ? ut.a : (x < n ? pd[0] : ninf);
+        if constexpr (E::ES == 4) {
+            const bool whole = x + 8 <= n;   // else its last four tokens are past the part
+            ut.b = whole ? pt[1] : ninf;
+            ud.b = qonly ? ut.b : (whole ? pd[1] : ninf);
+        }
+        f2 XT[4], XD[4], R[4], Q[4];
+        unit_pairs<E>(ut, XT);
+        unit_pairs<E>(ud, XD);
+        vr_res8(XT, XD, k, qonly, R, Q);
+        const float r = warp_sumf(sum4p(R)), qm = warp_sumf(sum4p(Q));
+        if (lane == 0)
+            sg[q] = VrSeg{r, qm};
+    }
+}
+
 // ---------------------------------------------------------------- 3. sampling and outputs
 
 template <class E>
@@ -1880,7 +2110,74 @@ cudaError_t launch_stream(RowsParams P, int sms, cudaStream_t stream)
         S = std::max(1, std::min(VS_SMAX, std::atoi(ev)));
     P.span = ((P.V + S - 1) / S + 7) / 8 * 8;
     P.parts = (P.V + P.span - 1) / P.span;
-    return launch_after(kern, ncta, VS_T, smem, stream, P);
+    int grid = ncta;
+    if (const char *ev = std::getenv("SPECVERIFY_ROWS_CTAS"))
+        grid = std::max(1, std::min(ncta, std::atoi(ev)));
+    return launch_after(kern, grid, VS_T, smem, stream, P);
+}
+
+// Resident small calls: the parts per row S and tokens per part (whole
+// 256-token segments) for which a part of both rows of a position fits
+// VRS_SMEM, and whether the launch of B (K+1) S CTAs is resident at once.
+// Returns the dynamic shared memory per CTA, or 0 when the call does not fit.
+template <class E>
+int resident_geometry(int B, int K, int V, int &S, int &span)
+{
+    static bool attr_set[kMaxDevicesRows] = {};
+    static int occ_dev[kMaxDevicesRows] = {};
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev >= kMaxDevicesRows ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    if (!attr_set[dev]) {
+        int occ = 0;
+        if (cudaFuncSetAttribute(vr_resident<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, VRS_SMEM) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, vr_resident<E>, VRS_T, VRS_SMEM) != cudaSuccess)
+            return 0;
+        occ_dev[dev] = occ;
+        attr_set[dev] = true;
+    }
+    S = (int)((2LL * V * E::ES + VRS_SMEM - 1) / VRS_SMEM);
+    for (;; ++S) {
+        span = ((V + S - 1) / S + VSEG - 1) / VSEG * VSEG;
+        if (2LL * span * E::ES <= VRS_SMEM)
+            break;
+    }
+    S = (V + span - 1) / span;
+    if (S > VR_SMAX || (long long)B * (K + 1) * S > (long long)sms * occ_dev[dev])
+        return 0;
+    return (int)(2LL * span * E::ES);
+}
+
+// Whether the resident path serves the call (stochastic, draft logits,
+// aligned rows; SPECVERIFY_ROWS_RESIDENT=0 or SPECVERIFY_ROWS_STREAM=0 turn it off).
+bool resident_enabled()
+{
+    const char *r = std::getenv("SPECVERIFY_ROWS_RESIDENT");
+    const char *st = std::getenv("SPECVERIFY_ROWS_STREAM");
+    return !(r && std::atoi(r) == 0) && !(st && std::atoi(st) == 0);
+}
+
+template <class E>
+cudaError_t launch_resident(RowsParams P, int S, int span, int smem, cudaStream_t stream)
+{
+    P.parts = S;
+    P.span = span;
+    P.fused = 2;   // decisions recorded in the decision word, no residual jobs
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(P.B * (P.K + 1) * S));
+    cfg.blockDim = dim3(VRS_T);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeCooperative;   // every CTA resident: they wait on each other
+    at[0].val.cooperative = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, vr_resident<E>, P);
+    if (e == cudaSuccess)
+        e = launch_after(vr_sample<E>, P.B, VST, 0, stream, P);
+    return e;
 }
 
 template <class E>
@@ -1893,6 +2190,14 @@ cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream, int &launches)
     if (e != cudaSuccess)
         return e;
     launches = 0;
+    if (!P.greedy && !P.sl && !P.probs && P.vec && resident_enabled()) {
+        int S = 0, span = 0;
+        const int smem = resident_geometry<E>(P.B, P.K, P.V, S, span);
+        if (smem > 0) {
+            launches = 2;
+            return launch_resident<E>(P, S, span, smem, stream);
+        }
+    }
     if (P.probs && !use_stream(P))
         return cudaErrorNotSupported;   // given probabilities: the stream alone serves them
     if (use_stream(P)) {
@@ -1944,6 +2249,13 @@ cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream, int &launches)
 
 }  // namespace
 
+bool rows_resident_fits(int B, int K, int V, int tdt)
+{
+    if (!resident_enabled())
+        return false;
+    int S = 0, span = 0;
+    return (tdt == 0 ? resident_geometry<F32>(B, K, V, S, span) : resident_geometry<BF16>(B, K, V, S, span)) > 0;
+}
 int rows_chunks() { return VR_NCH; }
 int rows_segment_tokens() { return VSEG; }
 cudaError_t launch_rows(const RowsParams &P, int tdt, cudaStream_t stream, int *launches)

@@ -51,6 +51,10 @@ cudaError_t static_scratch_address(uint32_t **addr);   // current device
 // Row-parallel verification (k_rows.cu): statistics per row, residual masses
 // per sequence chunk, then sampling per sequence (greedy: no residual kernel).
 int rows_chunks();
+// Whether a stochastic call with aligned rows of draft logits fits the
+// resident path (every row of the call held in the shared memory of CTAs
+// resident at once).
+bool rows_resident_fits(int B, int K, int V, int tdt);
 int rows_segment_tokens();
 // *launches: the kernels the call launched
 cudaError_t launch_rows(const RowsParams &P, int tdt, cudaStream_t stream, int *launches);

@@ -30,23 +30,27 @@ def _device():
 @pytest.fixture(scope="module", autouse=True,
                 params=["auto", "cluster", "rows", "rows-stats", "rows-unfused", "general"])
 def kernel(request):
-    """Every case runs under the default dispatch and under each kernel forced
-    in turn: the cluster kernel, the row-parallel kernels
+    """Every case runs under the default dispatch (small aligned calls: the
+    resident kernel) and under each kernel forced in turn: the cluster kernel,
+    the row-parallel kernels
     (with the bulk-copy statistics stream, and with the per-position
     statistics launches in its place: "rows-stats") and the chunk-scheduled
     kernel (each falls back to the next for shapes it does not serve);
     "rows" runs the residual pass inside the statistics stream at every size,
     "rows-unfused" keeps it in its own launch and runs greedy calls on the
     register-load argmax kernel even where rows are aligned for bulk copies."""
-    keys = ("SPECVERIFY_KERNEL", "SPECVERIFY_ROWS_STREAM", "SPECVERIFY_ROWS_FUSED", "SPECVERIFY_GREEDY_CFG")
+    keys = ("SPECVERIFY_KERNEL", "SPECVERIFY_ROWS_STREAM", "SPECVERIFY_ROWS_FUSED", "SPECVERIFY_GREEDY_CFG",
+            "SPECVERIFY_ROWS_RESIDENT")
     saved = {k: os.environ.get(k) for k in keys}
     os.environ["SPECVERIFY_KERNEL"] = "rows" if request.param.startswith("rows") else request.param
     if request.param == "rows-stats":
         os.environ["SPECVERIFY_ROWS_STREAM"] = "0"
     if request.param == "rows":
         os.environ["SPECVERIFY_ROWS_FUSED"] = "1"
+        os.environ["SPECVERIFY_ROWS_RESIDENT"] = "0"
     if request.param == "rows-unfused":
         os.environ["SPECVERIFY_ROWS_FUSED"] = "0"
+        os.environ["SPECVERIFY_ROWS_RESIDENT"] = "0"
         os.environ["SPECVERIFY_GREEDY_CFG"] = "256,2"
     yield request.param
     for k, v in saved.items():

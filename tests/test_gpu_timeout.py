@@ -8,6 +8,7 @@ once unless what they wait for is already there:
 
 - the row-parallel statistics stream: its producers' wait for every sequence
   to have ended, and for a posted residual job to be written;
+- the resident kernel for small calls: each CTA's wait for its sequence's end;
 - the cluster kernel: the exchange of per-CTA records inside a cluster;
 - the chunk-scheduled kernel: an idle worker's wait for its residual slot.
 
@@ -33,7 +34,7 @@ from speculative_decoding_verification_sampling_gb300 import synth
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
 TIMEOUT = 7
-KEYS = ("SPECVERIFY_KERNEL", "SPECVERIFY_ROWS_FUSED", "SPECVERIFY_SPIN_LIMIT")
+KEYS = ("SPECVERIFY_KERNEL", "SPECVERIFY_ROWS_FUSED", "SPECVERIFY_SPIN_LIMIT", "SPECVERIFY_ROWS_RESIDENT")
 
 
 @pytest.fixture(autouse=True)
@@ -92,6 +93,15 @@ def test_stream_waits_run_out_then_recover(B, K):
     os.environ["SPECVERIFY_KERNEL"] = "rows"
     os.environ["SPECVERIFY_ROWS_FUSED"] = "1"
     run_out_then_recover(synth.throughput(B=B, K=K, seed=B + 7), 5, f"stream B={B} K={K}", all_out=True)
+
+
+@pytest.mark.parametrize("B,K", [(1, 4), (8, 4)])
+def test_resident_waits_run_out_then_recover(B, K):
+    """The resident kernel's CTAs wait for their sequence's end; at spin limit
+    1 those that commit before it is known give up, and every sequence
+    reports 7."""
+    os.environ["SPECVERIFY_ROWS_RESIDENT"] = "1"
+    run_out_then_recover(synth.throughput(B=B, K=K, seed=B + 9), 6, f"resident B={B} K={K}", all_out=True)
 
 
 @pytest.mark.parametrize("B,K,V", [(24, 4, 128256), (16, 3, 8192)])
