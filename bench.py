@@ -858,9 +858,98 @@ def _shortlist_pos_workload(B: int, K: int, dev):
                 l2=f"inputs larger than L2: device copies of the {nbytes / 1e6:.0f} MB input set, rotated")
 
 
+def _greedy_workload(B: int, K: int, dev):
+    """Greedy verification (the benchmark table's config 2): B=64, K=5,
+    V=128256 bf16, target ~ N(0, 3^2), drafted tokens = the argmax with
+    probability 0.8.  B and K are fixed by the configuration."""
+    import torch
+    import oracle
+    import speculative_decoding_verification_sampling_gb300 as sv
+    from speculative_decoding_verification_sampling_gb300 import synth
+    Bg, Kg = 64, 5
+    cfg = synth.greedy(B=Bg, K=Kg, V=V, seed=DATA_SEED)
+    host_t, host_k = cfg["target"], cfg["draft_tokens"]
+    nbytes = host_t.numel() * host_t.element_size()
+    ref = oracle.verify(host_t, None, host_k, 0.0, 0)
+    need = _rule_rows(ref["accept_len"].tolist(), Kg, True) * V * 2 + Bg * Kg * 4 + Bg * (Kg + 2) * 4
+    ws = torch.zeros(sv.spec_workspace_bytes(Bg, Kg, V), dtype=torch.uint8, device=dev)
+
+    def make_sets(n):
+        t0, k0 = host_t.to(dev), host_k.to(dev)
+        return [[t0 if i == 0 else t0.clone(), k0, torch.empty(Bg, Kg + 1, dtype=torch.int32, device=dev),
+                 torch.empty(Bg, dtype=torch.int32, device=dev)] for i in range(max(n, 4))]
+
+    def call(st, stream):
+        t, k, ot, ol = st
+        sv.spec_verify_greedy(t, k, out_tokens=ot, out_accept_len=ol, workspace=ws, stream=stream)
+
+    def result(st):
+        return torch.cat([st[2].flatten(), st[3]]).cpu()
+
+    def oracle_run(i):
+        b = i % Bg
+        oracle.verify(host_t[b:b + 1], None, host_k[b:b + 1], 0.0, 0)
+        return Kg
+
+    return dict(metric="verified draft positions/s (greedy, V=128256 bf16); achieved HBM GB/s", unit="positions/s",
+                units=Bg * Kg, alg_bytes=need, h2d=nbytes + Bg * Kg * 4, d2h=Bg * (Kg + 2) * 4, make_sets=make_sets,
+                call=call, result=result, host_inputs=[host_t, host_k], upload=lambda st: st[:2],
+                oracle_run=oracle_run, kernel="vg_bulk (one launch: argmax of every target row, the walk)",
+                B=Bg, K=Kg,
+                workload=f"greedy B={Bg} K={Kg} V={V} bf16 T=0: target N(0, 3^2), drafts = argmax with "
+                         f"probability 0.8",
+                l2=f"inputs larger than L2: device copies of the {nbytes / 1e6:.0f} MB target rows, rotated")
+
+
+def _small_workload(B: int, K: int, dev):
+    """The smallest call of the benchmark table (config 1): B=1, K=4,
+    V=32000 float32, T=1, target ~ N(0, 2^2), draft = target + N(0, 0.5^2):
+    a latency figure.  Enough device copies of the 1.15 MB input set are
+    rotated that the calls read more than twice the L2."""
+    import torch
+    import oracle
+    import speculative_decoding_verification_sampling_gb300 as sv
+    from speculative_decoding_verification_sampling_gb300 import synth
+    cfg = synth.small_stochastic(seed=DATA_SEED)
+    Bs, Ks, Vs = 1, 4, 32000
+    host = [cfg["target"], cfg["draft"], cfg["draft_tokens"]]
+    nbytes = sum(h.numel() * h.element_size() for h in host)
+    ref = oracle.verify(cfg["target"], cfg["draft"], cfg["draft_tokens"], TEMPERATURE, VERIFY_SEED)
+    need = needed_bytes(ref["accept_len"].tolist(), Ks, Vs, 4)
+    ws = torch.zeros(sv.spec_workspace_bytes(Bs, Ks, Vs), dtype=torch.uint8, device=dev)
+    copies = math.ceil(2 * 129e6 / nbytes)
+
+    def make_sets(n):
+        d0 = [h.to(dev) for h in host]
+        return [(d0 if i == 0 else [x.clone() for x in d0]) +
+                [torch.empty(Bs, Ks + 1, dtype=torch.int32, device=dev), torch.empty(Bs, dtype=torch.int32, device=dev)]
+                for i in range(max(n, copies))]
+
+    def call(st, stream):
+        t, d, k, ot, ol = st
+        sv.spec_verify(t, d, k, TEMPERATURE, VERIFY_SEED, out_tokens=ot, out_accept_len=ol, workspace=ws,
+                       stream=stream)
+
+    def result(st):
+        return torch.cat([st[3].flatten(), st[4]]).cpu()
+
+    def oracle_run(i):
+        oracle.verify(cfg["target"], cfg["draft"], cfg["draft_tokens"], TEMPERATURE, VERIFY_SEED)
+        return Ks
+
+    return dict(metric="verified draft positions/s (B=1 K=4 V=32000 fp32: latency per call); achieved HBM GB/s",
+                unit="positions/s", units=Bs * Ks, alg_bytes=need, h2d=nbytes, d2h=Bs * (Ks + 2) * 4,
+                make_sets=make_sets, call=call, result=result, host_inputs=host, upload=lambda st: st[:3],
+                oracle_run=oracle_run, kernel="vr_resident + vr_sample (every row held in shared memory)",
+                B=Bs, K=Ks, V=Vs, dtype="f32",
+                workload=f"small B={Bs} K={Ks} V={Vs} fp32 T=1: target N(0, 2^2), draft = target + N(0, 0.5^2)",
+                l2=f"inputs larger than L2 in turn: {copies} device copies of the {nbytes / 1e6:.2f} MB input set, "
+                   f"rotated")
+
+
 EXTRA_WORKLOADS = {"shortlist_pos": _shortlist_pos_workload,
                    "draft_sample": _draft_sample_workload, "kv_commit": _kv_commit_workload,
-                   "tree_greedy": _tree_greedy_workload}
+                   "tree_greedy": _tree_greedy_workload, "greedy": _greedy_workload, "small": _small_workload}
 
 
 def run_extra(args) -> int:
@@ -940,8 +1029,9 @@ def run_extra(args) -> int:
         line = {
             "metric": w["metric"], "value": value, "unit": w["unit"], "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": elapsed_ms / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w["workload"], "B": w.get("B", args.batch), "K": w.get("K", args.k), "V": V,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.get("dtype", "bf16"), "data": "synthetic",
+            "config": {"workload": w["workload"], "B": w.get("B", args.batch), "K": w.get("K", args.k),
+                       "V": w.get("V", V),
                        "parallelism": f"replicas x{world}", "l2": w["l2"]},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": None, "peak_source": src, "kernel": w["kernel"],
