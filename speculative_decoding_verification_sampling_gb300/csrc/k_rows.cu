@@ -2110,10 +2110,7 @@ cudaError_t launch_stream(RowsParams P, int sms, cudaStream_t stream)
         S = std::max(1, std::min(VS_SMAX, std::atoi(ev)));
     P.span = ((P.V + S - 1) / S + 7) / 8 * 8;
     P.parts = (P.V + P.span - 1) / P.span;
-    int grid = ncta;
-    if (const char *ev = std::getenv("SPECVERIFY_ROWS_CTAS"))
-        grid = std::max(1, std::min(ncta, std::atoi(ev)));
-    return launch_after(kern, grid, VS_T, smem, stream, P);
+    return launch_after(kern, ncta, VS_T, smem, stream, P);
 }
 
 // Resident small calls: the parts per row S and tokens per part (whole
