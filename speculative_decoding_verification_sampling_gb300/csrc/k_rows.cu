@@ -1729,6 +1729,21 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
         sm_m = __ldcg(P.rej + b);
         sm_tf = __ldcg(P.vctl + VC_TIMEOUT * VC_LINE);
     }
+    // the segment masses of the pair the sequence ended at (the residual pass
+    // wrote them; they do not depend on where it ended), in the same round
+    // trip: a thread's segments stay in registers when there are at most PC
+    const int nseg = P.nseg;
+    const VrSeg *sg = P.segm + (size_t)b * nseg;
+    const int per = (nseg + VST - 1) / VST;
+    const int s0 = min(nseg, tid * per), s1 = min(nseg, s0 + per);
+    constexpr int PC = 8;
+    const bool cached = per <= PC && !P.greedy;
+    float2 cg[PC];
+    if (cached) {
+#pragma unroll
+        for (int k = 0; k < PC; ++k)
+            cg[k] = s0 + k < s1 ? __ldcg(reinterpret_cast<const float2 *>(sg + s0 + k)) : make_float2(0.0f, 0.0f);
+    }
     __syncthreads();
     const uint32_t msk = sm_m;
     const int j = msk ? __ffs(msk) - 1 : K;
@@ -1805,19 +1820,8 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
                 dS = ld_vrstat(st + K + 1 + j);
         }
         // totals of the residual and target masses of row pair j
-        const int nseg = P.nseg;
-        const VrSeg *sg = P.segm + (size_t)b * nseg;
-        const int per = (nseg + VST - 1) / VST;
-        const int s0 = min(nseg, tid * per), s1 = min(nseg, s0 + per);
-        // a thread's segments stay in registers when there are at most PC of them
-        constexpr int PC = 8;
-        const bool cached = per <= PC;
-        float2 cg[PC];
         DF ownr{0.0f, 0.0f}, ownq{0.0f, 0.0f};
         if (cached) {
-#pragma unroll
-            for (int k = 0; k < PC; ++k)
-                cg[k] = s0 + k < s1 ? __ldcg(reinterpret_cast<const float2 *>(sg + s0 + k)) : make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int k = 0; k < PC; ++k)
                 if (s0 + k < s1) {
