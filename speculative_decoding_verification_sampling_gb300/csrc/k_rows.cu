@@ -214,6 +214,51 @@ __device__ __forceinline__ bool vr_ended(unsigned long long w)
 }
 __device__ __noinline__ void vr_post_end(const RowsParams &P, int b, unsigned long long w);
 
+// The statistics of a row from its n parts' records (pp[0..n)): the largest
+// reference, the sums rescaled to it (exact powers of two) and added as a
+// float pair, the flags, the drafted token's logit from the part holding it.
+__device__ __forceinline__ VrStat merge_parts(const VrStat *pp, int n)
+{
+    constexpr int MU = 4;   // records loaded at once (a few registers: the kernel keeps 3 CTAs per SM)
+    float M = -F_INF, zd = 0.0f;
+    DF S{0.0f, 0.0f};
+    int fl = 0;
+    for (int h0 = 0; h0 < n; h0 += MU) {
+        float4 a[MU];
+        float z[MU];
+#pragma unroll
+        for (int k = 0; k < MU; ++k)
+            if (h0 + k < n) {
+                a[k] = __ldcg(reinterpret_cast<const float4 *>(pp + h0 + k));
+                z[k] = __ldcg(&pp[h0 + k].zd);
+            }
+#pragma unroll
+        for (int k = 0; k < MU; ++k)
+            if (h0 + k < n) {
+                const int f = __float_as_int(a[k].w);
+                fl |= f;
+                if (f & VR_HASD)
+                    zd = z[k];
+                const float mk = a[k].x;
+                if (mk > -F_INF) {
+                    if (mk > M) {
+                        S = M > -F_INF ? df_scale_pow2(S, M - mk) : DF{0.0f, 0.0f};
+                        M = mk;
+                    }
+                    S = df_add(S, df_scale_pow2(DF{a[k].y, a[k].z}, mk - M));
+                }
+            }
+    }
+    return VrStat{M, S.hi, S.lo, fl, zd, 0, 0, 0};
+}
+
+// The epilogue of vr_stream: part `part` of the target (kind 0) or draft
+// (kind 1) row of position i of sequence b has statistics st.  One counter per
+// position counts the parts of both rows; the last part to finish merges
+// every part (one round of loads), records the two rows and decides the
+// position.  A rejection or an error sets the position's bit in rej, and the
+// per-sequence word of decided and ending positions finds the sequence's end
+// (vr_commit's way).
 // A part's statistics st of row ridx (sequence b, position i; kind 1: the
 // draft row), from one CTA: the last part of the row to finish merges the
 // parts in part order and writes the row's statistics; the second row of a
@@ -231,14 +276,11 @@ __device__ __noinline__ void vr_commit(const RowsParams &P, size_t ridx, int b, 
         if (vr_atom_add(P.rowcnt + ridx, 1u) != (uint32_t)(P.parts - 1))
             return;
         VrStat m{};
-        m.zd = slrow ? -F_INF : 0.0f;
-        float Mx = -F_INF;
-        for (int h = 0; h < P.parts; ++h) {
-            const VrStat q = ld_vrstat(pp + h);
-            m.flags |= q.flags;
-            if (q.flags & VR_HASD)
-                m.zd = q.zd;
-            if (P.greedy) {
+        if (P.greedy) {
+            m.zd = 0.0f;
+            for (int h = 0; h < P.parts; ++h) {
+                const VrStat q = ld_vrstat(pp + h);
+                m.flags |= q.flags;
                 if (h == 0) {
                     m.m = q.m;
                     m.s_hi = q.s_hi;
@@ -247,20 +289,12 @@ __device__ __noinline__ void vr_commit(const RowsParams &P, size_t ridx, int b, 
                     argmax_merge(m.m, ix, q.m, __float_as_int(q.s_hi));
                     m.s_hi = __int_as_float(ix);
                 }
-            } else {
-                Mx = fmaxf(Mx, q.m);
             }
-        }
-        if (!P.greedy) {
-            DF S{0.0f, 0.0f};
-            for (int h = 0; h < P.parts; ++h) {
-                const VrStat q = ld_vrstat(pp + h);
-                if (q.m > -F_INF)
-                    S = df_add(S, df_scale_pow2(DF{q.s_hi, q.s_lo}, q.m - Mx));
-            }
-            m.m = Mx;
-            m.s_hi = S.hi;
-            m.s_lo = S.lo;
+        } else {
+            // the parts' records, four loads in flight at a time
+            m = merge_parts(pp, P.parts);
+            if (slrow && !(m.flags & VR_HASD))
+                m.zd = -F_INF;   // the drafted token is not on the list: p(d) = 0
         }
         st = m;
     }
@@ -765,51 +799,6 @@ __device__ __forceinline__ void vs_stage(const uint4 *p, int ntok, int tid, floa
     }
 }
 
-// The statistics of a row from its n parts' records (pp[0..n)): the largest
-// reference, the sums rescaled to it (exact powers of two) and added as a
-// float pair, the flags, the drafted token's logit from the part holding it.
-__device__ __forceinline__ VrStat merge_parts(const VrStat *pp, int n)
-{
-    constexpr int MU = 4;   // records loaded at once (a few registers: the kernel keeps 3 CTAs per SM)
-    float M = -F_INF, zd = 0.0f;
-    DF S{0.0f, 0.0f};
-    int fl = 0;
-    for (int h0 = 0; h0 < n; h0 += MU) {
-        float4 a[MU];
-        float z[MU];
-#pragma unroll
-        for (int k = 0; k < MU; ++k)
-            if (h0 + k < n) {
-                a[k] = __ldcg(reinterpret_cast<const float4 *>(pp + h0 + k));
-                z[k] = __ldcg(&pp[h0 + k].zd);
-            }
-#pragma unroll
-        for (int k = 0; k < MU; ++k)
-            if (h0 + k < n) {
-                const int f = __float_as_int(a[k].w);
-                fl |= f;
-                if (f & VR_HASD)
-                    zd = z[k];
-                const float mk = a[k].x;
-                if (mk > -F_INF) {
-                    if (mk > M) {
-                        S = M > -F_INF ? df_scale_pow2(S, M - mk) : DF{0.0f, 0.0f};
-                        M = mk;
-                    }
-                    S = df_add(S, df_scale_pow2(DF{a[k].y, a[k].z}, mk - M));
-                }
-            }
-    }
-    return VrStat{M, S.hi, S.lo, fl, zd, 0, 0, 0};
-}
-
-// The epilogue of vr_stream: part `part` of the target (kind 0) or draft
-// (kind 1) row of position i of sequence b has statistics st.  One counter per
-// position counts the parts of both rows; the last part to finish merges
-// every part (one round of loads), records the two rows and decides the
-// position.  A rejection or an error sets the position's bit in rej, and the
-// per-sequence word of decided and ending positions finds the sequence's end
-// (vr_commit's way).
 __device__ __noinline__ void vs_commit(const RowsParams &P, int b, int i, int kind, int part, int dt, VrStat st)
 {
     const int K = P.K;
