@@ -6,7 +6,7 @@
 // work is cut by rows instead of by sequences, so that every SM streams
 // independent rows at full bandwidth:
 //   1. Row statistics: each logit row is streamed once into its reference
-//      and sum (greedy: its argmax), keeping the logit at the drafted token.
+//      and sum, keeping the logit at the drafted token.
 //      The second row of a position to finish decides it; a rejection (or an
 //      error) sets the position's bit in the sequence's mask.  Rows of a
 //      sequence with a bit below their position skip their reads, so only the
@@ -16,7 +16,7 @@
 //        persistent launch; rows are claimed position-major from a counter
 //        and copied in 16 KB stages by cp.async.bulk into a shared-memory
 //        ring, reduced by consumer warps; an epilogue thread decides.
-//      - vr_stats (greedy, shortlisted drafts, unaligned rows): one launch for
+//      - vr_stats (shortlisted drafts, unaligned rows): one launch for
 //        positions 0-1 and one for the rest, one CTA per part of a row,
 //        16-byte loads with four in flight per thread.
 //   2. vr_residual: eight CTAs per sequence.  The mask gives the position j
@@ -27,7 +27,8 @@
 //      one crossing v * R, reads that segment again and locates the token
 //      (inverse CDF in ascending token order); it writes the outputs and
 //      re-zeroes the sequence's control words.
-// Greedy verification runs kernels 1 and 3 only.
+// Small calls whose rows all fit shared memory run on vr_resident and
+// vr_sample; greedy verification has its own kernels (k_greedy_rows.cu).
 #include "sv_cluster.cuh"
 #include "sv_launch.h"
 
@@ -117,13 +118,6 @@ __device__ __forceinline__ int vr_decide(const RowsParams &P, int b, int i, int 
         return ST_SHORTLIST;   // the position's shortlist, before its token
     if (i < P.K && !(dt >= 0 && dt < P.V))
         return ST_TOKEN;
-    if (P.greedy) {
-        const int g = __float_as_int(t.s_hi);
-        if ((t.flags & VR_BAD) || !(t.m > -F_INF) || g < 0)
-            return ST_NONFINITE;
-        accept = i < P.K && g == dt;
-        return 0;
-    }
     if ((t.flags & VR_BAD) || !(t.m > -F_INF) || !(t.s_hi > 0.0f))
         return ST_NONFINITE;
     if (i == P.K)
@@ -262,45 +256,28 @@ __device__ __forceinline__ VrStat merge_parts(const VrStat *pp, int n)
 // A part's statistics st of row ridx (sequence b, position i; kind 1: the
 // draft row), from one CTA: the last part of the row to finish merges the
 // parts in part order and writes the row's statistics; the second row of a
-// position to finish decides it (greedy and position K: the only row), and a
-// rejection or an error sets the position's bit in rej.
+// position to finish decides it (position K: the only row), and a rejection
+// or an error sets the position's bit in rej.
 __device__ __noinline__ void vr_commit(const RowsParams &P, size_t ridx, int b, int i, int kind, int part, int dt,
                                        VrStat st, bool slrow)
 {
     const int K = P.K;
-    const bool pairs = !P.greedy && i < K;
+    const bool pairs = i < K;
     if (P.parts > 1) {
         // the last part of the row to finish merges the parts, in part order
         VrStat *pp = P.vpart + ridx * VR_SMAX;
         pp[part] = st;
         if (vr_atom_add(P.rowcnt + ridx, 1u) != (uint32_t)(P.parts - 1))
             return;
-        VrStat m{};
-        if (P.greedy) {
-            m.zd = 0.0f;
-            for (int h = 0; h < P.parts; ++h) {
-                const VrStat q = ld_vrstat(pp + h);
-                m.flags |= q.flags;
-                if (h == 0) {
-                    m.m = q.m;
-                    m.s_hi = q.s_hi;
-                } else {
-                    int ix = __float_as_int(m.s_hi);
-                    argmax_merge(m.m, ix, q.m, __float_as_int(q.s_hi));
-                    m.s_hi = __int_as_float(ix);
-                }
-            }
-        } else {
-            // the parts' records, four loads in flight at a time
-            m = merge_parts(pp, P.parts);
-            if (slrow && !(m.flags & VR_HASD))
-                m.zd = -F_INF;   // the drafted token is not on the list: p(d) = 0
-        }
+        // the parts' records, four loads in flight at a time
+        VrStat m = merge_parts(pp, P.parts);
+        if (slrow && !(m.flags & VR_HASD))
+            m.zd = -F_INF;   // the drafted token is not on the list: p(d) = 0
         st = m;
     }
     P.stat[ridx] = st;
-    // the second row of a position to finish decides it (greedy and position K:
-    // the only row); a rejection or an error sets the position's bit
+    // the second row of a position to finish decides it (position K: the only
+    // row); a rejection or an error sets the position's bit
     VrStat t = st, d{};
     if (pairs) {
         if (vr_atom_add(P.pair + (size_t)b * (K + 1) + i, 1u) != 1u)
@@ -334,21 +311,21 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
     pdl_trigger();
     constexpr int NW = VT / 32;
     __shared__ float sm_m[NW], sm_hi[NW], sm_lo[NW];
-    __shared__ int sm_i[NW], sm_f[NW];
+    __shared__ int sm_f[NW];
     __shared__ float sm_zd;
     __shared__ int sm_skip;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int K = P.K, V = P.V;
     // this launch's rows, position-major over [P.pos, P.pos + P.npos): the
     // target and draft rows of each sequence side by side (the target row
-    // alone for greedy and at position K), each cut into P.parts parts of
-    // P.span tokens, one CTA each
-    const int rpp = P.greedy ? P.B : 2 * P.B;   // rows of a position below K
+    // alone at position K), each cut into P.parts parts of P.span tokens, one
+    // CTA each
+    const int rpp = 2 * P.B;   // rows of a position below K
     const int rg = (int)blockIdx.x / P.parts, part = (int)blockIdx.x % P.parts;
     const int i = P.pos + rg / rpp;
     const int rl = rg % rpp;
-    const int b = P.greedy ? rl : rl >> 1;
-    const int kind = P.greedy ? 0 : rl & 1;
+    const int b = rl >> 1;
+    const int kind = rl & 1;
     if (kind && i == K)
         return;   // position K has no draft row
     const size_t ridx = (size_t)b * (2 * K + 1) + (kind ? K + 1 + i : i);
@@ -379,8 +356,8 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
     const int t0 = min(nrow, part * span), t1 = min(nrow, t0 + span);
     const int u0 = t0 / 8, nu = (t1 - t0 + 7) / 8;   // this part's units of 8 tokens
     const float c = P.c;
-    float mc = -F_INF, s = 0.0f, bv = -F_INF, zd = 0.0f;
-    int fl = 0, bi = -1;
+    float mc = -F_INF, s = 0.0f, zd = 0.0f;
+    int fl = 0;
     bool hz = false;
     // four units in flight per thread; each buffer is refilled right after its use
     Unit<E> u[4];
@@ -428,7 +405,7 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
                         }
                         prev = cur;
                     }
-                } else if ((unsigned)(dt - x0) < 8u || P.greedy) {
+                } else if ((unsigned)(dt - x0) < 8u) {
                     float x[8];
 #pragma unroll
                     for (int p = 0; p < 4; ++p)
@@ -439,16 +416,9 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
                             zd = x[e];
                             hz = true;
                         }
-                        if (P.greedy) {
-                            if (!(x[e] == x[e]) || x[e] == F_INF)
-                                fl |= VR_BAD;
-                            else if (x[e] > bv)
-                                bv = x[e], bi = x0 + e;
-                        }
                     }
                 }
-                if (!P.greedy)
-                    acc_group(X, c, mc, s, fl, VR_BAD);
+                acc_group(X, c, mc, s, fl, VR_BAD);
             }
         }
     }
@@ -457,16 +427,7 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
         fl |= VR_HASD;
     }
     fl = warp_or(fl);
-    if (P.greedy) {
-#pragma unroll
-        for (int o = 16; o; o >>= 1)
-            argmax_merge(bv, bi, __shfl_xor_sync(0xffffffffu, bv, o), __shfl_xor_sync(0xffffffffu, bi, o));
-        if (lane == 0) {
-            sm_m[warp] = bv;
-            sm_i[warp] = bi;
-            sm_f[warp] = fl;
-        }
-    } else {
+    {
         float M;
         DF S;
         merge_ms<32>(mc, DF{s, 0.0f}, c, M, S);
@@ -486,13 +447,7 @@ __global__ void __launch_bounds__(VT) vr_stats(const __grid_constant__ RowsParam
     // the drafted token's logit, from the thread that held it (VR_HASD); a
     // shortlisted draft row without it gives p(d) = 0
     st.zd = (st.flags & VR_HASD) ? sm_zd : (slrow ? -F_INF : 0.0f);
-    if (P.greedy) {
-        float v = in ? sm_m[lane] : -F_INF;
-        int ix = in ? sm_i[lane] : -1;
-        warp_merge_argmax<NW>(v, ix);
-        st.m = v;
-        st.s_hi = __int_as_float(ix);
-    } else {
+    {
         float M;
         DF S;
         merge_ms<NW>(in ? sm_m[lane] : -F_INF, in ? DF{sm_hi[lane], sm_lo[lane]} : DF{0.0f, 0.0f}, c, M, S);
@@ -1726,7 +1681,7 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
     const int per = (nseg + VST - 1) / VST;
     const int s0 = min(nseg, tid * per), s1 = min(nseg, s0 + per);
     constexpr int PC = 8;
-    const bool cached = per <= PC && !P.greedy;
+    const bool cached = per <= PC;
     float2 cg[PC];
     if (cached) {
 #pragma unroll
@@ -1793,12 +1748,6 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
                 P.aux_R[b] = __int_as_float(0x7fc00000);
             if (P.aux_status)
                 atomicCAS(P.aux_status, 0, code);
-        }
-    } else if (P.greedy) {
-        if (tid == 0) {
-            sm_x = __float_as_int(ld_vrstat(st + j).s_hi);
-            if (P.aux_R)
-                P.aux_R[b] = __int_as_float(0x7fc00000);
         }
     } else {
         // the statistics of row pair j, loaded now for the coefficients used at the end
@@ -2027,7 +1976,7 @@ constexpr int VST_T = 256;   // threads of a vr_stats CTA
 template <class E>
 cudaError_t launch_stats(RowsParams P, int pos, int npos, int sms, cudaStream_t stream)
 {
-    const int rpp = P.greedy ? P.B : 2 * P.B;
+    const int rpp = 2 * P.B;
     // position K has the target row alone (B rows): launch it as rpp rows, the
     // draft half returning at once, to keep one row mapping
     const int rows = rpp * npos;
@@ -2054,7 +2003,7 @@ bool use_stream(const RowsParams &P)
     if (const char *ev = std::getenv("SPECVERIFY_ROWS_STREAM"))
         if (std::atoi(ev) == 0)
             return false;
-    return !P.greedy && !P.sl && P.vec;
+    return !P.sl && P.vec;
 }
 
 constexpr long long kFusedMinRows = 1024;
@@ -2180,7 +2129,7 @@ cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream, int &launches)
     if (e != cudaSuccess)
         return e;
     launches = 0;
-    if (!P.greedy && !P.sl && !P.probs && P.vec && resident_enabled()) {
+    if (!P.sl && !P.probs && P.vec && resident_enabled()) {
         int S = 0, span = 0;
         const int smem = resident_geometry<E>(P.B, P.K, P.V, S, span);
         if (smem > 0) {
@@ -2221,7 +2170,7 @@ cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream, int &launches)
     }
     if (e != cudaSuccess)
         return e;
-    if (!P.greedy && !P.fused) {
+    if (!P.fused) {
         // a shortlisted draft's segments scatter their list entries, a round
         // trip per step: four times the CTAs per sequence, a quarter of the steps
         if (P.sl)
