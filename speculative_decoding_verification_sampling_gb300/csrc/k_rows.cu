@@ -1652,9 +1652,13 @@ __global__ void __launch_bounds__(VRS_T) vr_resident(const __grid_constant__ Row
 
 // ---------------------------------------------------------------- 3. sampling and outputs
 
-template <class E>
+// DK: the draft kind, fixed per instantiation so that each variant carries
+// only its own locate code -- 0 draft logits, 1 given probabilities, 2 a
+// shortlisted draft.
+template <class E, int DK>
 __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsParams P)
 {
+    constexpr bool PROBS = DK == 1, SLIST = DK == 2;
     pdl_wait();
     pdl_trigger();
     constexpr int NW = VST / 32;
@@ -1711,7 +1715,7 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
             bool ok;
             const float l2 = row_l2(ld_vrstat(st + i), ok);
             if (P.aux_lse)   // given probabilities have no draft logits: NaN there
-                P.aux_lse[(size_t)b * (2 * K + 1) + i] = ok && !(P.probs && i > K) ? l2 * 0.6931471805599453f : nan;
+                P.aux_lse[(size_t)b * (2 * K + 1) + i] = ok && !(PROBS && i > K) ? l2 * 0.6931471805599453f : nan;
         }
         // q_i(d_i) and p_i(d_i) where both rows of the position (given
         // probabilities: the target row and p_i(d_i)) and the token are usable
@@ -1721,7 +1725,7 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
             const float lt = row_l2(t, okt);
             const int dt = __ldg(P.tokens + (size_t)b * K + i);
             float pv;
-            if (P.probs) {
+            if (PROBS) {
                 pv = dt >= 0 && dt < V ? __ldg(static_cast<const float *>(P.draft) + ((size_t)b * K + i) * (size_t)V + dt)
                                        : nan;
                 okd = pv >= 0.0f && pv != F_INF;
@@ -1857,14 +1861,14 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
             if (seg >= 0) {
                 const ResK k = res_coef(P, tS, dS, j);
                 const bool qonly = j == K || useq;
-                const bool slist = P.sl && !qonly;
+                const bool slist = SLIST && !qonly;
                 const uint8_t *trow =
                     static_cast<const uint8_t *>(P.target) + ((size_t)b * (K + 1) + j) * (size_t)V * E::ES;
                 const int x0 = seg * VSEG + lane * 8;
                 const Unit<E> ut = fetch_unit<E>(trow, x0, V, P.vec);
                 Unit<E> ud{};
                 Unit<F32> up{};
-                if (!qonly && P.probs)
+                if (!qonly && PROBS)
                     up = fetch_unit<F32>(static_cast<const uint8_t *>(P.draft) + ((size_t)b * K + j) * (size_t)V * 4,
                                          x0, V, P.vec);
                 else if (!qonly && !slist)
@@ -1874,7 +1878,7 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
                 unit_pairs<E>(ut, XT);
                 if (slist) {
                     sl_pairs<E>(P, b, j, seg, lane, sl_buf0, XD);
-                } else if (!qonly && P.probs) {
+                } else if (!qonly && PROBS) {
                     // x_d c = log2 p, as in the residual pass
                     f2 PP[4];
                     unit_pairs<F32>(up, PP);
@@ -1967,6 +1971,17 @@ __global__ void __launch_bounds__(VST) vr_sample(const __grid_constant__ RowsPar
                 P.vctl[w * VC_LINE] = 0u;
         }
     }
+}
+
+// vr_sample for the call's draft kind.
+template <class E>
+cudaError_t launch_sample(const RowsParams &P, cudaStream_t stream)
+{
+    if (P.probs)
+        return launch_after(vr_sample<E, 1>, P.B, VST, 0, stream, P);
+    if (P.sl)
+        return launch_after(vr_sample<E, 2>, P.B, VST, 0, stream, P);
+    return launch_after(vr_sample<E, 0>, P.B, VST, 0, stream, P);
 }
 
 // A vr_stats launch over `rows` rows: each row is cut into parts so that the
@@ -2115,7 +2130,7 @@ cudaError_t launch_resident(RowsParams P, int S, int span, int smem, cudaStream_
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, vr_resident<E>, P);
     if (e == cudaSuccess)
-        e = launch_after(vr_sample<E>, P.B, VST, 0, stream, P);
+        e = launch_sample<E>(P, stream);
     return e;
 }
 
@@ -2181,7 +2196,7 @@ cudaError_t launch_rows_t(RowsParams P, cudaStream_t stream, int &launches)
         if (e != cudaSuccess)
             return e;
     }
-    e = launch_after(vr_sample<E>, P.B, VST, 0, stream, P);
+    e = launch_sample<E>(P, stream);
     launches += 1;
     return e;
 }
