@@ -70,7 +70,7 @@ typedef enum {
     SPEC_ERR_NONFINITE = 2,    /* NaN / +inf logit, all -inf row, or bad draft probability */
     SPEC_ERR_TOKEN_RANGE = 3,  /* a drafted token outside [0, V) */
     SPEC_ERR_SHORTLIST = 4,    /* shortlist not ascending and unique inside [0, V) */
-    SPEC_ERR_UNSUPPORTED = 5,  /* no usable sm_103a device for this build */
+    SPEC_ERR_UNSUPPORTED = 5,  /* no usable sm_103a device, or a shape the entry point does not take */
     SPEC_ERR_CUDA = 6,         /* a CUDA runtime call or launch failed */
     SPEC_ERR_TIMEOUT = 7       /* a bounded on-device wait ran out (the kernel gave up) */
 } spec_status_t;
