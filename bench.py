@@ -643,7 +643,9 @@ def config_points(dev, stream, calls: int = 40):
                        more)
     del more
     acc = r[1].cpu().tolist()
-    need = sum((min(int(L), 4) + 1) * V * 2 + min(int(L) + 1, 4) * V * 4 for L in acc)
+    # rule bytes: target rows 0..j; p(d) at each decided position; the probability
+    # row itself only at a rejection (the residual)
+    need = sum((min(int(L), 4) + 1) * V * 2 + min(int(L) + 1, 4) * 4 + (V * 4 if int(L) < 4 else 0) for L in acc)
     rec = record("draft probabilities: B=256 K=4 V=128256, bf16 target logits, fp32 draft probabilities", c, us, r,
                  2, all_rows=256 * 5 * V * 2 + 256 * 4 * V * 4, b2b=b2b)
     rec["rule_bytes"] = need
@@ -947,9 +949,106 @@ def _small_workload(B: int, K: int, dev):
                    f"rotated")
 
 
+def _shortlist_workload(B: int, K: int, dev):
+    """The shortlisted configuration of the benchmark table (config 4): B=64,
+    K=6, V=262144 bf16, Zipf target, 8 of 64 clusters of 4096 tokens per
+    sequence (S=32768, compact draft rows), draft = target + N(0, 0.5^2) on
+    the list.  B and K are fixed by the configuration."""
+    import torch
+    import oracle
+    import speculative_decoding_verification_sampling_gb300 as sv
+    from speculative_decoding_verification_sampling_gb300 import synth
+    cfg = synth.shortlist(seed=DATA_SEED)
+    Bs, Ks, Vs = cfg["B"], cfg["K"], cfg["V"]
+    S = cfg["shortlist"].shape[1]
+    host = [cfg["target"], cfg["draft"], cfg["shortlist"], cfg["draft_tokens"]]
+    nbytes = sum(h.numel() * h.element_size() for h in host)
+    ref = oracle.verify(cfg["target"], cfg["draft"], cfg["draft_tokens"], TEMPERATURE, VERIFY_SEED,
+                        shortlist=cfg["shortlist"])
+    # rule bytes: target rows 0..j, draft rows 0..min(j, K-1) at S, the sequence's list once
+    need = sum((min(int(L), Ks) + 1) * Vs * 2 + min(int(L) + 1, Ks) * S * 2 for L in ref["accept_len"].tolist())
+    need += Bs * S * 4
+    ws = torch.zeros(sv.spec_workspace_bytes(Bs, Ks, Vs, S), dtype=torch.uint8, device=dev)
+
+    def make_sets(n):
+        d0 = [h.to(dev) for h in host]
+        return [(d0 if i == 0 else [x.clone() for x in d0]) + [None] for i in range(max(n, 2))]
+
+    def call(st, stream):
+        t, d, sl, k, _ = st
+        st[4] = sv.spec_verify_shortlist(t, d, sl, k, TEMPERATURE, VERIFY_SEED, workspace=ws, stream=stream)
+
+    def result(st):
+        return st[4][1].cpu()
+
+    def oracle_run(i):
+        b = i % Bs
+        oracle.verify(cfg["target"][b:b + 1], cfg["draft"][b:b + 1], cfg["draft_tokens"][b:b + 1], TEMPERATURE,
+                      VERIFY_SEED, shortlist=cfg["shortlist"][b:b + 1], seq_ids=[b], threads=1)
+        return Ks
+
+    return dict(metric="verified draft positions/s with a per-sequence shortlisted draft (V=262144 bf16); "
+                       "achieved HBM GB/s", unit="positions/s", units=Bs * Ks, alg_bytes=need, h2d=nbytes,
+                d2h=Bs * (Ks + 2) * 4, make_sets=make_sets, call=call, result=result, host_inputs=host,
+                upload=lambda st: st[:4], oracle_run=oracle_run,
+                kernel="vr_stats x2 + vr_residual + vr_sample (row-parallel, shortlisted draft)", B=Bs, K=Ks, V=Vs,
+                workload=f"shortlist B={Bs} K={Ks} V={Vs} S={S} bf16 T=1: Zipf target, 8 of 64 clusters of 4096 "
+                         f"per sequence, draft = target + N(0, 0.5^2) on the list",
+                l2=f"inputs larger than L2: device copies of the {nbytes / 1e6:.0f} MB input set, rotated")
+
+
+def _probs_workload(B: int, K: int, dev):
+    """Draft probabilities: B=256, K=4, V=128256, bf16 target logits and
+    float32 draft probabilities (the softmax of the throughput workload's
+    draft logits), T=1.  B and K are fixed."""
+    import torch
+    import oracle
+    import speculative_decoding_verification_sampling_gb300 as sv
+    from speculative_decoding_verification_sampling_gb300 import synth
+    Bp, Kp = 256, 4
+    cfg = synth.throughput(B=Bp, K=Kp, seed=DATA_SEED)
+    probs = torch.softmax(cfg["draft"].float(), dim=-1)
+    host = [cfg["target"], probs, cfg["draft_tokens"]]
+    nbytes = sum(h.numel() * h.element_size() for h in host)
+    ref = oracle.verify(cfg["target"], probs, cfg["draft_tokens"], TEMPERATURE, VERIFY_SEED, draft_is_probs=True)
+    # rule bytes: target rows 0..j; of the probabilities, p(d) at each decided
+    # position and the whole row only where a draft token is rejected (the residual)
+    need = sum((min(int(L), Kp) + 1) * V * 2 + min(int(L) + 1, Kp) * 4 + (V * 4 if int(L) < Kp else 0)
+               for L in ref["accept_len"].tolist())
+    ws = torch.zeros(sv.spec_workspace_bytes(Bp, Kp, V), dtype=torch.uint8, device=dev)
+
+    def make_sets(n):
+        d0 = [h.to(dev) for h in host]
+        return [(d0 if i == 0 else [x.clone() for x in d0]) + [None] for i in range(max(n, 2))]
+
+    def call(st, stream):
+        t, d, k, _ = st
+        st[3] = sv.spec_verify(t, d, k, TEMPERATURE, VERIFY_SEED, draft_is_probs=True, workspace=ws, stream=stream)
+
+    def result(st):
+        return st[3][1].cpu()
+
+    def oracle_run(i):
+        b = i % Bp
+        oracle.verify(cfg["target"][b:b + 1], probs[b:b + 1], cfg["draft_tokens"][b:b + 1], TEMPERATURE,
+                      VERIFY_SEED, draft_is_probs=True, seq_ids=[b], threads=1)
+        return Kp
+
+    return dict(metric="verified draft positions/s with draft probabilities (V=128256, bf16 target, fp32 "
+                       "probabilities); achieved HBM GB/s", unit="positions/s", units=Bp * Kp, alg_bytes=need,
+                h2d=nbytes, d2h=Bp * (Kp + 2) * 4, make_sets=make_sets, call=call, result=result, host_inputs=host,
+                upload=lambda st: st[:3], oracle_run=oracle_run,
+                kernel="vr_stream<BF16, probabilities> + vr_sample (target rows streamed, p(d) at the decision)",
+                B=Bp, K=Kp,
+                workload=f"draft probabilities B={Bp} K={Kp} V={V}: bf16 target N(0, 2^2), fp32 probabilities of "
+                         f"target + N(0, 0.5^2), T=1",
+                l2=f"inputs larger than L2: device copies of the {nbytes / 1e6:.0f} MB input set, rotated")
+
+
 EXTRA_WORKLOADS = {"shortlist_pos": _shortlist_pos_workload,
                    "draft_sample": _draft_sample_workload, "kv_commit": _kv_commit_workload,
-                   "tree_greedy": _tree_greedy_workload, "greedy": _greedy_workload, "small": _small_workload}
+                   "tree_greedy": _tree_greedy_workload, "greedy": _greedy_workload, "small": _small_workload,
+                   "shortlist": _shortlist_workload, "probs": _probs_workload}
 
 
 def run_extra(args) -> int:
