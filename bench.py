@@ -120,6 +120,36 @@ def needed_bytes(accept_len, K: int, V: int, elem_bytes: int) -> int:
     return needed_rows(accept_len, K) * V * elem_bytes + B * K * 4 + B * (K + 1) * 4 + B * 4
 
 
+def probs_rule_bytes(accept_len, K: int, V: int, elem_bytes: int = 2) -> int:
+    """Bytes the left-to-right rule reads with given draft probabilities:
+    target rows 0..j (elem_bytes each), p_i(d_i) at every decided position
+    (4 bytes), and the float32 probability row only where a draft token is
+    rejected (the residual needs it; an accepted position needs p(d) alone)."""
+    total = 0
+    for L in accept_len:
+        L = int(L)
+        if L < 0:
+            raise ValueError("a sequence reported a data error")
+        total += (min(L, K) + 1) * V * elem_bytes + min(L + 1, K) * 4 + (V * 4 if L < K else 0)
+    return total
+
+
+def shortlist_rule_bytes(accept_len, K: int, V: int, lens, one_list: bool, elem_bytes: int = 2) -> int:
+    """Bytes the left-to-right rule reads with shortlisted drafts: target rows
+    0..j at V, compact draft rows 0..min(j, K-1) at their list lengths
+    lens[t], and the int32 lists -- once per sequence when one list serves
+    every position (one_list), else each position's list beside its row."""
+    total = 0
+    for L in accept_len:
+        L = int(L)
+        if L < 0:
+            raise ValueError("a sequence reported a data error")
+        npos = min(L + 1, K)
+        total += (min(L, K) + 1) * V * elem_bytes + sum(lens[t] for t in range(npos)) * elem_bytes
+        total += lens[0] * 4 if one_list else sum(lens[t] for t in range(npos)) * 4
+    return total
+
+
 def kernel_sources_digest() -> str:
     """sha256 over the CUDA and C++ sources of the library, in name order."""
     h = hashlib.sha256()
@@ -606,8 +636,7 @@ def config_points(dev, stream, calls: int = 40):
     us, r, b2b = timed(lambda: sv.spec_verify_shortlist(t, d, sl, k, 1.0, VERIFY_SEED, stream=stream), more)
     del more
     acc = r[1].cpu().tolist()
-    # rule bytes: target rows 0..j at V, draft rows 0..min(j, K-1) at S, and the sequence's list once
-    need = sum((min(int(L), Ks) + 1) * Vs * 2 + min(int(L) + 1, Ks) * S * 2 for L in acc) + Bs * S * 4
+    need = shortlist_rule_bytes(acc, Ks, Vs, [S] * Ks, True)
     rec = record("shortlist (compact): B=64 K=6 V=262144 bf16 T=1, Zipf target, 8 of 64 clusters per sequence "
                  "(S=32768), draft = target + N(0, 0.5^2) on the list", c, us, r, 2,
                  all_rows=Bs * (Ks + 1) * Vs * 2 + Bs * Ks * S * 2 + Bs * S * 4, b2b=b2b)
@@ -643,9 +672,7 @@ def config_points(dev, stream, calls: int = 40):
                        more)
     del more
     acc = r[1].cpu().tolist()
-    # rule bytes: target rows 0..j; p(d) at each decided position; the probability
-    # row itself only at a rejection (the residual)
-    need = sum((min(int(L), 4) + 1) * V * 2 + min(int(L) + 1, 4) * 4 + (V * 4 if int(L) < 4 else 0) for L in acc)
+    need = probs_rule_bytes(acc, 4, V)
     rec = record("draft probabilities: B=256 K=4 V=128256, bf16 target logits, fp32 draft probabilities", c, us, r,
                  2, all_rows=256 * 5 * V * 2 + 256 * 4 * V * 4, b2b=b2b)
     rec["rule_bytes"] = need
@@ -823,10 +850,7 @@ def _shortlist_pos_workload(B: int, K: int, dev):
     ref = oracle.verify(cfg["target"], cfg["draft"], cfg["draft_tokens"], TEMPERATURE, VERIFY_SEED,
                         shortlist=cfg["shortlist"], shortlist_len=lens)
     # bytes the left-to-right rule reads: target rows 0..j, draft rows and lists 0..min(j, K-1)
-    need = 0
-    for j in ref["accept_len"].tolist():
-        j = Ks if j < 0 else j
-        need += (j + 1) * Vs * 2 + sum(lens[t] * 6 for t in range(min(j + 1, Ks)))
+    need = shortlist_rule_bytes(ref["accept_len"].tolist(), Ks, Vs, lens, False)
     need += Bs * (Ks * 4 + (Ks + 1) * 4 + 4)
 
     def make_sets(n):
@@ -965,9 +989,7 @@ def _shortlist_workload(B: int, K: int, dev):
     nbytes = sum(h.numel() * h.element_size() for h in host)
     ref = oracle.verify(cfg["target"], cfg["draft"], cfg["draft_tokens"], TEMPERATURE, VERIFY_SEED,
                         shortlist=cfg["shortlist"])
-    # rule bytes: target rows 0..j, draft rows 0..min(j, K-1) at S, the sequence's list once
-    need = sum((min(int(L), Ks) + 1) * Vs * 2 + min(int(L) + 1, Ks) * S * 2 for L in ref["accept_len"].tolist())
-    need += Bs * S * 4
+    need = shortlist_rule_bytes(ref["accept_len"].tolist(), Ks, Vs, [S] * Ks, True)
     ws = torch.zeros(sv.spec_workspace_bytes(Bs, Ks, Vs, S), dtype=torch.uint8, device=dev)
 
     def make_sets(n):
@@ -1011,10 +1033,7 @@ def _probs_workload(B: int, K: int, dev):
     host = [cfg["target"], probs, cfg["draft_tokens"]]
     nbytes = sum(h.numel() * h.element_size() for h in host)
     ref = oracle.verify(cfg["target"], probs, cfg["draft_tokens"], TEMPERATURE, VERIFY_SEED, draft_is_probs=True)
-    # rule bytes: target rows 0..j; of the probabilities, p(d) at each decided
-    # position and the whole row only where a draft token is rejected (the residual)
-    need = sum((min(int(L), Kp) + 1) * V * 2 + min(int(L) + 1, Kp) * 4 + (V * 4 if int(L) < Kp else 0)
-               for L in ref["accept_len"].tolist())
+    need = probs_rule_bytes(ref["accept_len"].tolist(), Kp, V)
     ws = torch.zeros(sv.spec_workspace_bytes(Bp, Kp, V), dtype=torch.uint8, device=dev)
 
     def make_sets(n):

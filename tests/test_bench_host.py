@@ -35,6 +35,31 @@ def test_needed_bytes_counts_rows_tokens_and_outputs():
     assert got == rows * V * 2 + B * K * 4 + B * (K + 1) * 4 + B * 4
 
 
+def test_probability_rule_bytes_read_the_row_only_at_a_rejection():
+    K, V = 2, 10
+    # rejection at the first draft: target row 0 (20 B), p(d) once, the probability row (40 B)
+    assert bench.probs_rule_bytes([0], K, V) == 20 + 4 + 40
+    # rejection at the second: target rows 0..1, p(d) twice, the probability row
+    assert bench.probs_rule_bytes([1], K, V) == 40 + 8 + 40
+    # every draft accepted: K + 1 target rows and p(d) at each position, no probability row
+    assert bench.probs_rule_bytes([2], K, V) == 60 + 8
+    assert bench.probs_rule_bytes([0, 1, 2], K, V) == 64 + 88 + 68
+    with pytest.raises(ValueError):
+        bench.probs_rule_bytes([-2], K, V)
+
+
+def test_shortlist_rule_bytes_count_rows_at_their_list_lengths():
+    K, V = 2, 10
+    # one list per sequence (4 entries): read once, 16 B
+    assert bench.shortlist_rule_bytes([0], K, V, [4, 4], True) == 20 + 8 + 16
+    assert bench.shortlist_rule_bytes([2], K, V, [4, 4], True) == 60 + 16 + 16
+    # a list per position (4 and 2 entries), each read with its row
+    assert bench.shortlist_rule_bytes([1], K, V, [4, 2], False) == 40 + 12 + 24
+    assert bench.shortlist_rule_bytes([0], K, V, [4, 2], False) == 20 + 8 + 16
+    with pytest.raises(ValueError):
+        bench.shortlist_rule_bytes([-1], K, V, [4, 4], True)
+
+
 def test_clock_samples_parse_and_summarize():
     lines = [
         "2026/12/02 10:00:00.000, 1965, 2070, 900.1, 100, Not Active, Not Active, Not Active, Active\n",
