@@ -13,8 +13,11 @@ Philox against Triton's interpreter, the worked single-position example of the
 runelab.ai post, brute-force enumeration on V <= 4, K <= 2, chi-square and
 total-variation checks of the emitted distribution, the closed form for the
 expected number of tokens per round, and special cases (p == q, one-hot q,
-one-hot p, greedy against numpy.argmax).  Parity unpinned: the exact token
-identity drawn for one given seed (no outside reference exists for it).
+one-hot p, greedy against numpy.argmax); and, in ``tests/test_oracle_outputs.py``,
+the per-position outputs and margins against scipy, and the tokens drawn for a
+given seed: the accept decisions against u < min(1, q/p) evaluated by numpy and
+the emitted token against numpy.searchsorted on the float64 CDF, both with the
+uniforms rebuilt from the (Triton-pinned) Philox words.
 """
 from __future__ import annotations
 
