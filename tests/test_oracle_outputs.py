@@ -183,3 +183,43 @@ def test_sample_margin_and_residual_mass_by_searchsorted():
         lower_nearer += lo < hi
         upper_nearer += hi < lo
     assert lower_nearer > 20 and upper_nearer > 20
+
+
+def test_draws_with_given_probabilities_by_numpy():
+    """With draft probabilities given, the accept decisions are u_i <
+    min(1, q_i(d_i) / p_i(d_i)) with p read as given (no softmax, no T), and
+    the emitted token is numpy.searchsorted of v in the normalised CDF of
+    max(0, q_j - p_j) (q_K for the bonus); residual_mass is its total.
+
+    Caught mistakes the logit pins cannot: the temperature applied to the given
+    probabilities, or their logarithm taken as logits."""
+    B, K, V, T, seed = 160, 3, 29, 0.9, 4242
+    tgt, drf, tok = _case(B, K, V, T, seed=31, sigma=0.8)
+    zd = drf.double().numpy()
+    probs = np.stack([[softmax(zd[b, i]) for i in range(K)] for b in range(B)])   # not the T-softmax
+    out = oracle.verify(tgt, torch.tensor(probs, dtype=torch.float32), tok, T, seed=seed, draft_is_probs=True)
+    p32 = torch.tensor(probs, dtype=torch.float32).double().numpy()   # the values the oracle was given
+    zt = tgt.double().numpy()
+    n_rej = n_bonus = 0
+    for b in range(B):
+        L = K
+        for i in range(K):
+            q = softmax(zt[b, i] / T)
+            pd = p32[b, i, tok[b, i]]
+            acc = pd == 0.0 or _uniform(seed, b, i, 0) < min(1.0, q[tok[b, i]] / pd)
+            if not acc:
+                L = i
+                break
+        assert int(out["accept_len"][b]) == L, b
+        q = softmax(zt[b, L] / T)
+        r = q if L == K else np.maximum(0.0, q - p32[b, L])
+        R = r.sum()
+        if L < K:
+            assert abs(out["residual_mass"][b] - R) < 1e-12, b
+            n_rej += 1
+        else:
+            n_bonus += 1
+        x = int(np.searchsorted(np.cumsum(r) / R, _uniform(seed, b, L, 1), side="right"))
+        assert out["tokens"][b, L] == x, b
+        assert list(out["tokens"][b, :L]) == list(tok[b, :L]), b
+    assert n_rej > 20 and n_bonus > 5
