@@ -223,3 +223,48 @@ def test_draws_with_given_probabilities_by_numpy():
         assert out["tokens"][b, L] == x, b
         assert list(out["tokens"][b, :L]) == list(tok[b, :L]), b
     assert n_rej > 20 and n_bonus > 5
+
+
+def test_draws_with_a_shortlisted_draft_by_numpy():
+    """With a shortlisted draft (compact logits over a per-sequence list), p_i
+    is the softmax of the listed logits at T placed on the listed tokens and 0
+    elsewhere; the accept decisions are u_i < min(1, q_i(d_i) / p_i(d_i))
+    (always when p_i(d_i) = 0) and the emitted token is numpy.searchsorted of v
+    in the normalised CDF of max(0, q_j - p_j) over the full vocabulary.
+
+    Caught mistakes: the list's logits scattered one token off; the residual
+    taken over the listed tokens only."""
+    B, K, V, S, T, seed = 120, 3, 37, 12, 0.8, 99
+    rng = np.random.default_rng(5)
+    zt = rng.normal(0, 2.0, size=(B, K + 1, V))
+    lists = np.stack([np.sort(rng.choice(V, size=S, replace=False)) for _ in range(B)]).astype(np.int32)
+    zd = np.stack([zt[b, :K][:, lists[b]] for b in range(B)]) + rng.normal(0, 0.7, size=(B, K, S))
+    tok = np.zeros((B, K), dtype=np.int32)
+    for b in range(B):
+        for i in range(K):
+            # mostly listed tokens, now and then one off the list (p = 0: accepted)
+            tok[b, i] = lists[b][rng.choice(S, p=softmax(zd[b, i] / T))] if rng.random() > 0.05 else rng.integers(V)
+    tgt = torch.tensor(zt, dtype=torch.float32)
+    drf = torch.tensor(zd, dtype=torch.float32)
+    out = oracle.verify(tgt, drf, tok, T, seed=seed, shortlist=torch.tensor(lists))
+    zt32, zd32 = tgt.double().numpy(), drf.double().numpy()
+    n_rej = n_off = 0
+    for b in range(B):
+        p = np.zeros((K, V))
+        for i in range(K):
+            p[i, lists[b]] = softmax(zd32[b, i] / T)
+        L = K
+        for i in range(K):
+            q = softmax(zt32[b, i] / T)
+            pd = p[i, tok[b, i]]
+            n_off += pd == 0.0
+            if not (pd == 0.0 or _uniform(seed, b, i, 0) < min(1.0, q[tok[b, i]] / pd)):
+                L = i
+                break
+        assert int(out["accept_len"][b]) == L, b
+        q = softmax(zt32[b, L] / T)
+        r = q if L == K else np.maximum(0.0, q - p[L])
+        n_rej += L < K
+        x = int(np.searchsorted(np.cumsum(r) / r.sum(), _uniform(seed, b, L, 1), side="right"))
+        assert out["tokens"][b, L] == x, b
+    assert n_rej > 20 and n_off > 3
